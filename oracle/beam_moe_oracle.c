@@ -1,0 +1,346 @@
+/*
+ * Plain CPU oracle for one Beam-style sparse MoE layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct
+ * definition the GPU library is checked against.  Only the tests, the smoke
+ * check and the benchmark's CPU-baseline leg may load it.  It shares no code,
+ * header, table or helper with the CUDA library, and the CUDA library never
+ * calls it.
+ *
+ * Sources (web pages describing Reflection's Beam-1.0-501B-A23B model):
+ *  [P1-MoE]  "Reflection Beam 1.0: 501B open MoE model, 1M context, Apache 2.0"
+ *            (agentlenshq.com), section "Mixture of Experts: 256 experts,
+ *            8 routed per token": sigmoid scores over all experts, 8 groups of
+ *            32, groups ranked by the sum of their top-2 scores, the best 4
+ *            groups kept, top-8 experts chosen inside them, no shared expert,
+ *            expert outputs combined with the normalised router weights and
+ *            scaled by 2.5; each expert is a SwiGLU MLP of intermediate 2560.
+ *  [P1-FP32] same page, section "Residual stream", last paragraph: the router
+ *            and the SwiGLU product are computed in FP32.
+ *  [P4-MoE]  "Beam 501B open model" (aixai.ru), section "256 experts per
+ *            layer": the same routing restated.
+ *  [P5-MoE]  "Reflection 501B-parameter Beam model" (dothoosh.com), section
+ *            "Architecture and memory efficiency": the same routing restated;
+ *            FP32 pins restated in the section on residual-stream design.
+ *
+ * Readings where the pages are silent (each is listed in the design doc):
+ *  - router logits: l[t,e] = sum_h x[t,h]*Wr[h,e], FP32 fused multiply-add in
+ *    ascending h, starting from +0.0f.
+ *  - sigmoid: s = 1/(1+E) in FP32 where E is exp(-l) rounded to FP32 (computed
+ *    through the double-precision exp and one rounding).
+ *  - group score: sum of the top min(2, group size) scores of the group (FP32).
+ *  - ties: lower group index / lower expert index wins.
+ *  - selected-slot order: score descending, expert index ascending.
+ *  - weights: S = FP32 sum of the selected scores in slot order,
+ *    w_k = (s_k / S) * scale, FP32 divide then FP32 multiply.
+ *  - expert: g = x.Wg[e]^T, u = x.Wu[e]^T accumulated in FP64 and rounded to
+ *    FP32; h = silu(g)*u in FP32 (the pinned product); y = h.Wd[e]^T in FP64.
+ *  - combine: out = bf16_rne(float(sum_k w_k*y_k)), FP64 sum in ascending k.
+ *  - permuted order: rows grouped by expert (ascending), tokens ascending
+ *    inside an expert.
+ *
+ * Everything here is written for clarity, not speed: no blocking, no fusion.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------- helpers */
+
+static float bf16_bits_to_float(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* IEEE round-to-nearest-even from FP32 to bfloat16 (NaN kept quiet). */
+static uint16_t float_to_bf16_bits_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* FP32 sigmoid as read from [P1-MoE]/[P1-FP32]: 1/(1+E), E = fp32(exp(-l)). */
+static float sigmoid_f32(float l)
+{
+    float e = (float)exp(-(double)l);
+    float den = 1.0f + e;
+    return 1.0f / den;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------ router step */
+
+/*
+ * Router logits and sigmoid scores, [P1-MoE] + [P1-FP32].
+ *   x      [T,H] bf16 bits      wr [H,E] fp32 (row-major, hidden-major)
+ *   logits [T,E] fp32 or NULL   scores [T,E] fp32
+ */
+void oracle_router_scores(const uint16_t *x, const float *wr, int64_t T, int H,
+                          int E, float *logits, float *scores)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        float *acc = (float *)malloc(sizeof(float) * (size_t)E);
+        for (int e = 0; e < E; ++e)
+            acc[e] = 0.0f;
+        /* every acc[e] sees the terms h = 0, 1, ..., H-1 in that order */
+        for (int h = 0; h < H; ++h) {
+            float xv = bf16_bits_to_float(x[t * H + h]);
+            const float *wrow = wr + (int64_t)h * E;
+            for (int e = 0; e < E; ++e)
+                acc[e] = fmaf(xv, wrow[e], acc[e]);
+        }
+        for (int e = 0; e < E; ++e) {
+            if (logits)
+                logits[t * E + e] = acc[e];
+            scores[t * E + e] = sigmoid_f32(acc[e]);
+        }
+        free(acc);
+    }
+}
+
+/* --------------------------------------------------------- selection step */
+
+/* "a ranks before b" for (value descending, index ascending). */
+static int ranks_before(float va, int ia, float vb, int ib)
+{
+    return va > vb || (va == vb && ia < ib);
+}
+
+/*
+ * Group-limited top-k on given FP32 scores, [P1-MoE], [P4-MoE], [P5-MoE].
+ *   scores [T,E]; ids [T,top_k] int32; w [T,top_k] fp32.
+ * Returns 0, or -1 on an invalid configuration or a non-finite score.
+ */
+int oracle_select(const float *scores, int64_t T, int E, int G, int topk_groups,
+                  int top_k, float scale, int32_t *ids, float *w)
+{
+    if (E <= 0 || G <= 0 || E % G != 0 || topk_groups <= 0 || topk_groups > G ||
+        top_k <= 0 || top_k > topk_groups * (E / G))
+        return -1;
+    const int gsize = E / G;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t t = 0; t < T; ++t) {
+        const float *s = scores + t * E;
+        float *gscore = (float *)malloc(sizeof(float) * (size_t)G);
+        char *gkept = (char *)calloc((size_t)G, 1);
+        char *taken = (char *)calloc((size_t)E, 1);
+        for (int e = 0; e < E; ++e)
+            if (!isfinite(s[e]))
+                bad = 1;
+
+        /* 1. group score = sum of the group's two largest scores */
+        for (int g = 0; g < G; ++g) {
+            const float *sg = s + g * gsize;
+            int i1 = 0;
+            for (int j = 1; j < gsize; ++j)
+                if (ranks_before(sg[j], j, sg[i1], i1))
+                    i1 = j;
+            if (gsize == 1) {
+                gscore[g] = sg[i1];
+                continue;
+            }
+            int i2 = -1;
+            for (int j = 0; j < gsize; ++j) {
+                if (j == i1)
+                    continue;
+                if (i2 < 0 || ranks_before(sg[j], j, sg[i2], i2))
+                    i2 = j;
+            }
+            gscore[g] = sg[i1] + sg[i2];
+        }
+
+        /* 2. keep the topk_groups best groups */
+        for (int r = 0; r < topk_groups; ++r) {
+            int best = -1;
+            for (int g = 0; g < G; ++g) {
+                if (gkept[g])
+                    continue;
+                if (best < 0 || ranks_before(gscore[g], g, gscore[best], best))
+                    best = g;
+            }
+            gkept[best] = 1;
+        }
+
+        /* 3. top_k experts among the kept groups, slot order = rank order */
+        for (int k = 0; k < top_k; ++k) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (!gkept[e / gsize] || taken[e])
+                    continue;
+                if (best < 0 || ranks_before(s[e], e, s[best], best))
+                    best = e;
+            }
+            taken[best] = 1;
+            ids[t * top_k + k] = best;
+        }
+
+        /* 4. normalise the selected scores to sum 1, then scale */
+        float S = 0.0f;
+        for (int k = 0; k < top_k; ++k)
+            S = S + s[ids[t * top_k + k]];
+        for (int k = 0; k < top_k; ++k) {
+            float q = s[ids[t * top_k + k]] / S;
+            w[t * top_k + k] = q * scale;
+        }
+        free(gscore);
+        free(gkept);
+        free(taken);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ---------------------------------------------------------- dispatch step */
+
+/*
+ * Expert histogram, exclusive offsets and the permutation that groups the
+ * (token, slot) pairs by expert, tokens ascending inside an expert.
+ *   ids [T,K] -> counts [E], offsets [E+1], row_of [T,K], row_src [T*K]
+ */
+int oracle_dispatch(const int32_t *ids, int64_t T, int K, int E, int32_t *counts,
+                    int32_t *offsets, int32_t *row_of, int32_t *row_src)
+{
+    for (int e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int64_t i = 0; i < T * K; ++i) {
+        if (ids[i] < 0 || ids[i] >= E)
+            return -1;
+        counts[ids[i]] += 1;
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+    int32_t *cursor = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    for (int64_t t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            int e = ids[t * K + k];
+            int32_t row = offsets[e] + cursor[e];
+            cursor[e] += 1;
+            row_of[t * K + k] = row;
+            row_src[row] = (int32_t)t;
+        }
+    free(cursor);
+    return 0;
+}
+
+/* ------------------------------------------------------------ expert step */
+
+/*
+ * One SwiGLU expert on one token, [P1-MoE] (SwiGLU MLP, intermediate I) and
+ * [P1-FP32] (the SwiGLU product in FP32).
+ *   xrow [H] bf16 bits; wg, wu [I,H] bf16 bits; wd [H,I] bf16 bits
+ *   hbuf [I] fp32 scratch; y [H] fp64 out
+ */
+static void expert_swiglu(const uint16_t *xrow, const uint16_t *wg,
+                          const uint16_t *wu, const uint16_t *wd, int H, int I,
+                          float *hbuf, double *y)
+{
+    for (int i = 0; i < I; ++i) {
+        double gd = 0.0, ud = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double xv = (double)bf16_bits_to_float(xrow[h]);
+            gd += xv * (double)bf16_bits_to_float(wg[(int64_t)i * H + h]);
+            ud += xv * (double)bf16_bits_to_float(wu[(int64_t)i * H + h]);
+        }
+        float g = (float)gd, u = (float)ud;
+        float silu = g * sigmoid_f32(g);
+        hbuf[i] = silu * u;
+    }
+    for (int j = 0; j < H; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i)
+            acc += (double)hbuf[i] * (double)bf16_bits_to_float(wd[(int64_t)j * I + i]);
+        y[j] = acc;
+    }
+}
+
+/* exported for the single-expert pin: y = SwiGLU expert applied to one row */
+void oracle_expert_row(const uint16_t *xrow, const uint16_t *wg,
+                       const uint16_t *wu, const uint16_t *wd, int H, int I,
+                       double *y)
+{
+    float *hbuf = (float *)malloc(sizeof(float) * (size_t)I);
+    expert_swiglu(xrow, wg, wu, wd, H, I, hbuf, y);
+    free(hbuf);
+}
+
+/* ----------------------------------------------------------- whole layer */
+
+/*
+ * The layer forward for a list of tokens (all tokens when tokens == NULL):
+ * router -> group-limited top-k -> experts -> weighted combine.
+ *   x [T,H] bf16; wr [H,E] fp32; wg, wu [E,I,H] bf16; wd [E,H,I] bf16
+ *   out [n,H] bf16 bits (row r is token tokens[r]);
+ *   ids_out [n,top_k], w_out [n,top_k] may be NULL.
+ */
+int oracle_forward(const uint16_t *x, const float *wr, const uint16_t *wg,
+                   const uint16_t *wu, const uint16_t *wd, int64_t T, int H,
+                   int I, int E, int G, int topk_groups, int top_k, float scale,
+                   const int64_t *tokens, int64_t n_tokens, uint16_t *out,
+                   int32_t *ids_out, float *w_out)
+{
+    if (E % G != 0 || top_k > topk_groups * (E / G))
+        return -1;
+    const int64_t n = tokens ? n_tokens : T;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t t = tokens ? tokens[r] : r;
+        if (t < 0 || t >= T) {
+            bad = 1;
+            continue;
+        }
+        const uint16_t *xrow = x + t * H;
+        float *scores = (float *)malloc(sizeof(float) * (size_t)E);
+        int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)top_k);
+        float *w = (float *)malloc(sizeof(float) * (size_t)top_k);
+        float *hbuf = (float *)malloc(sizeof(float) * (size_t)I);
+        double *y = (double *)malloc(sizeof(double) * (size_t)H);
+        double *acc = (double *)calloc((size_t)H, sizeof(double));
+
+        oracle_router_scores(xrow, wr, 1, H, E, NULL, scores);
+        if (oracle_select(scores, 1, E, G, topk_groups, top_k, scale, ids, w) != 0)
+            bad = 1;
+        for (int k = 0; k < top_k && !bad; ++k) {
+            const int64_t e = ids[k];
+            expert_swiglu(xrow, wg + e * I * H, wu + e * I * H, wd + e * H * I, H,
+                          I, hbuf, y);
+            for (int j = 0; j < H; ++j)
+                acc[j] += (double)w[k] * y[j];
+        }
+        for (int j = 0; j < H; ++j)
+            out[r * H + j] = float_to_bf16_bits_rne((float)acc[j]);
+        if (ids_out)
+            memcpy(ids_out + r * top_k, ids, sizeof(int32_t) * (size_t)top_k);
+        if (w_out)
+            memcpy(w_out + r * top_k, w, sizeof(float) * (size_t)top_k);
+        free(scores);
+        free(ids);
+        free(w);
+        free(hbuf);
+        free(y);
+        free(acc);
+    }
+    return bad ? -1 : 0;
+}

@@ -1,0 +1,163 @@
+"""numpy front end of the plain C oracle (``beam_moe_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers.  Nothing in the GPU library
+imports this module, and this module imports nothing from the GPU library.
+
+The C source states the method and every reading taken where the Beam pages
+are silent.  This file only marshals numpy arrays to it (bf16 tensors travel as
+their uint16 bit patterns).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "beam_moe_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+# -ffp-contract=off: no expression is fused unless the source calls fmaf.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+          "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library next to its source."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        p = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        i32 = ctypes.c_int
+        f32 = ctypes.c_float
+        L.oracle_num_threads.restype = i32
+        L.oracle_router_scores.argtypes = [p, p, i64, i32, i32, p, p]
+        L.oracle_router_scores.restype = None
+        L.oracle_select.argtypes = [p, i64, i32, i32, i32, i32, f32, p, p]
+        L.oracle_select.restype = i32
+        L.oracle_dispatch.argtypes = [p, i64, i32, i32, p, p, p, p]
+        L.oracle_dispatch.restype = i32
+        L.oracle_expert_row.argtypes = [p, p, p, p, i32, i32, p]
+        L.oracle_expert_row.restype = None
+        L.oracle_forward.argtypes = [p, p, p, p, p, i64, i32, i32, i32, i32, i32, i32,
+                                     f32, p, i64, p, p, p]
+        L.oracle_forward.restype = i32
+        _lib = L
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {a.dtype}")
+    return a
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+def router_scores(x_bits: np.ndarray, router_w: np.ndarray):
+    """FP32 logits and sigmoid scores, [T,E] each."""
+    x_bits = _c(x_bits, np.uint16)
+    router_w = _c(router_w, np.float32)
+    T, H = x_bits.shape
+    H2, E = router_w.shape
+    assert H == H2
+    logits = np.empty((T, E), np.float32)
+    scores = np.empty((T, E), np.float32)
+    lib().oracle_router_scores(_ptr(x_bits), _ptr(router_w), T, H, E, _ptr(logits), _ptr(scores))
+    return logits, scores
+
+
+def select(scores: np.ndarray, n_groups: int, topk_groups: int, top_k: int, scale: float):
+    """Group-limited top-k on given scores -> (ids [T,K] int32, w [T,K] fp32)."""
+    scores = _c(scores, np.float32)
+    T, E = scores.shape
+    ids = np.empty((T, top_k), np.int32)
+    w = np.empty((T, top_k), np.float32)
+    rc = lib().oracle_select(_ptr(scores), T, E, n_groups, topk_groups, top_k,
+                             float(scale), _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise ValueError("oracle_select rejected the configuration or the scores")
+    return ids, w
+
+
+def dispatch(ids: np.ndarray, n_experts: int):
+    """(counts [E], offsets [E+1], row_of [T,K], row_src [T*K]) for ids [T,K]."""
+    ids = _c(ids, np.int32)
+    T, K = ids.shape
+    counts = np.empty(n_experts, np.int32)
+    offsets = np.empty(n_experts + 1, np.int32)
+    row_of = np.empty((T, K), np.int32)
+    row_src = np.empty(T * K, np.int32)
+    rc = lib().oracle_dispatch(_ptr(ids), T, K, n_experts, _ptr(counts), _ptr(offsets),
+                               _ptr(row_of), _ptr(row_src))
+    if rc != 0:
+        raise ValueError("expert id out of range")
+    return counts, offsets, row_of, row_src
+
+
+def expert_row(x_row_bits, wg_bits, wu_bits, wd_bits):
+    """One SwiGLU expert on one token row -> y [H] float64."""
+    x_row_bits = _c(x_row_bits, np.uint16)
+    wg_bits = _c(wg_bits, np.uint16)
+    wu_bits = _c(wu_bits, np.uint16)
+    wd_bits = _c(wd_bits, np.uint16)
+    I, H = wg_bits.shape
+    y = np.empty(H, np.float64)
+    lib().oracle_expert_row(_ptr(x_row_bits), _ptr(wg_bits), _ptr(wu_bits), _ptr(wd_bits),
+                            H, I, _ptr(y))
+    return y
+
+
+def forward(x_bits, router_w, wg_bits, wu_bits, wd_bits, n_groups, topk_groups, top_k,
+            scale, tokens=None):
+    """Layer output for `tokens` (all when None).
+
+    Returns (out_bits [n,H] uint16, ids [n,K] int32, w [n,K] fp32).
+    """
+    x_bits = _c(x_bits, np.uint16)
+    router_w = _c(router_w, np.float32)
+    wg_bits = _c(wg_bits, np.uint16)
+    wu_bits = _c(wu_bits, np.uint16)
+    wd_bits = _c(wd_bits, np.uint16)
+    T, H = x_bits.shape
+    E, I, H2 = wg_bits.shape
+    assert H2 == H and wu_bits.shape == (E, I, H) and wd_bits.shape == (E, H, I)
+    assert router_w.shape == (H, E)
+    tok = None if tokens is None else _c(np.asarray(tokens, np.int64), np.int64)
+    n = T if tok is None else tok.shape[0]
+    out = np.empty((n, H), np.uint16)
+    ids = np.empty((n, top_k), np.int32)
+    w = np.empty((n, top_k), np.float32)
+    rc = lib().oracle_forward(_ptr(x_bits), _ptr(router_w), _ptr(wg_bits), _ptr(wu_bits),
+                              _ptr(wd_bits), T, H, I, E, n_groups, topk_groups, top_k,
+                              float(scale), _ptr(tok), n, _ptr(out), _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise ValueError("oracle_forward failed (bad configuration or token index)")
+    return out, ids, w
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
