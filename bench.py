@@ -1,0 +1,422 @@
+#!/usr/bin/env python
+"""Beam MoE layer forward throughput on B300 (tokens/s), with roofline.
+
+One step = one whole layer forward (router, selection, dispatch, gate/up and
+down grouped GEMMs, combine) over one batch of T synthetic tokens whose
+activations are already resident in HBM.  The expert weights (20 GB bf16)
+are larger than L2, so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Multi-GPU (torchrun): every rank runs an independent replica on its own batch
+(the layer is per-token independent; no collective on the data path).
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Beam MoE-layer tokens/s at 1 B300; % of HBM (decode) / tensor (prefill) roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# ratio of nominal dense fp4 to bf16 tensor rates
+NVFP4_OVER_BF16 = 13.5 / 2.25
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="decode",
+                    choices=["tiny", "decode", "prefill", "skewed", "nvfp4"])
+    ap.add_argument("--cpu-tokens", type=int, default=16,
+                    help="tokens of the batch the CPU oracle baseline computes")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- helpers
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_moe_layer_experts_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def workload_algorithmic(sh, n_active: int):
+    """Algorithmic bytes / FLOPs per launch of each kernel (compulsory traffic
+    of the kernel's own inputs and outputs; expert weights of active experts
+    only)."""
+    T, H, I, E, K = sh.T, sh.H, sh.I, sh.E, sh.top_k
+    R = T * K
+    w_gu = n_active * 2 * I * H * 2
+    w_d = n_active * H * I * 2
+    return {
+        "router_scores": dict(bytes=T * H * 2 + H * E * 4 + T * E * 4, flops=2 * T * H * E),
+        "select": dict(bytes=T * E * 4 + R * 8, flops=0),
+        "hist": dict(bytes=R * 8 + ((T + 255) // 256) * E * 4, flops=0),
+        "scan": dict(bytes=((T + 255) // 256) * E * 8, flops=0),
+        "permute": dict(bytes=T * H * 2 + R * H * 2, flops=0),
+        "gateup_gemm": dict(bytes=w_gu + R * H * 2 + R * I * 2, flops=2 * R * H * 2 * I),
+        "down_gemm": dict(bytes=w_d + R * I * 2 + R * H * 4, flops=2 * R * I * H),
+        "combine": dict(bytes=R * H * 4 + T * H * 2 + R * 8, flops=2 * R * H),
+        "layer": dict(bytes=w_gu + w_d + H * E * 4 + 2 * T * H * 2,
+                      flops=2 * T * H * E + 6 * R * H * I),
+    }
+
+
+# ------------------------------------------------------------------ oracle
+
+def host_sample(sh, d, toks):
+    """Host copies for the oracle: x, router and the weights of the experts
+    the sampled tokens route to (the rest stay zero pages)."""
+    import numpy as np
+    from oracle import oracle
+    from sparse_moe_layer_experts_b300 import synth
+    xh = synth.to_bits(d["x"])
+    rw = synth.to_f32(d["router_w"])
+    _, s = oracle.router_scores(xh[toks], rw)
+    ids, _ = oracle.select(s, sh.G, sh.topk_groups, sh.top_k, sh.scale)
+    host = dict(x=xh, router_w=rw)
+    for k in ("w_gate", "w_up", "w_down"):
+        a = np.zeros(tuple(d[k].shape), np.uint16)
+        for e in sorted(set(ids.reshape(-1).tolist())):
+            a[e] = synth.to_bits(d[k][e])
+        host[k] = a
+    return host
+
+
+def oracle_step(sh, host, toks):
+    from oracle import oracle
+    t0 = time.perf_counter()
+    oracle.forward(host["x"], host["router_w"], host["w_gate"], host["w_up"], host["w_down"],
+                   sh.G, sh.topk_groups, sh.top_k, sh.scale, tokens=toks)
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_run(sh, d, n_tokens, seed=0):
+    """Time the CPU oracle on `n_tokens` seeded tokens of the batch."""
+    import numpy as np
+    from oracle import oracle
+    rng = np.random.default_rng(seed)
+    toks = sorted(rng.choice(sh.T, size=min(n_tokens, sh.T), replace=False).tolist())
+    host = host_sample(sh, d, toks)
+    dt = oracle_step(sh, host, toks)
+    return len(toks) / dt, min(oracle.num_threads(), len(toks)), len(toks), dt
+
+
+# -------------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm (rank 0 only): each step computes
+    a fixed seeded sample of the batch's tokens on the host cores."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    from oracle import oracle
+    from sparse_moe_layer_experts_b300 import synth
+    sh = synth.shape(args.config)
+    # the inputs are drawn exactly as the GPU arm draws them
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    d = synth.make_inputs(sh, seed=0, device=dev, weights=True)
+    ntok = min(args.cpu_tokens, sh.T)
+    toks = sorted(np.random.default_rng(0).choice(sh.T, size=ntok, replace=False).tolist())
+    host = host_sample(sh, d, toks)
+    del d
+    times = [oracle_step(sh, host, toks) for _ in range(args.warmup + args.steps)]
+    total = sum(times[args.warmup:])
+    value = ntok * args.steps / total
+    cores = min(oracle.num_threads(), ntok)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32/f64", "data": "synthetic",
+        "config": {"workload": f"{args.config}: T={sh.T} tokens, hidden {sh.H}, "
+                               f"intermediate {sh.I}, {sh.E} experts",
+                   "sample": f"{ntok} seeded tokens of the batch per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{ntok} seeded tokens per step, {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    from sparse_moe_layer_experts_b300 import binding as B
+    from sparse_moe_layer_experts_b300 import build as build_mod
+    from sparse_moe_layer_experts_b300 import synth
+    from sparse_moe_layer_experts_b300.layer import BeamMoE
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    build_mod.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sh = synth.shape(args.config)
+    d = synth.make_inputs(sh, seed=0, device=dev, weights=True)
+    if rank > 0:  # each replica routes its own batch
+        d["x"] = synth.make_inputs(sh, seed=rank, device=dev, weights=False)["x"]
+    layer = BeamMoE(d["router_w"], d["w_gate"], d["w_up"], d["w_down"], n_groups=sh.G,
+                    topk_groups=sh.topk_groups, top_k=sh.top_k, routed_scale=sh.scale)
+    x = d["x"]
+    out = torch.empty_like(x)
+    r = layer.route(x, want_scores=False)
+    counts = r["counts"].cpu().numpy()
+    n_active = int((counts > 0).sum())
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        layer.forward(x, out)
+    torch.cuda.synchronize()
+    if layer.status() != 0:
+        raise SystemExit("device status word reports an error during warm-up")
+
+    # per-kernel events: one (start, stop) pair per stage per step
+    nst = len(B.KERNEL_STAGES)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nst)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = B.beam_moe_launch_count()
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        time.sleep(0.05)
+        start.record(stream)
+        for i in range(args.steps):
+            B.check(B.beam_moe_set_kernel_events([e[0].cuda_event for e in ev[i]],
+                                                 [e[1].cuda_event for e in ev[i]]), "events")
+            layer.forward(x, out)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    B.beam_moe_set_kernel_events([], [])
+    barrier(world)
+    launches = B.beam_moe_launch_count() - launches0
+    ms = start.elapsed_time(stop)
+    ms_max = max_over_ranks(ms, world, dev)
+    if layer.status() != 0:
+        raise SystemExit("device status word reports an error in the timed region")
+    per_kernel_ms = {name: sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps))
+                     / args.steps for j, name in enumerate(B.KERNEL_STAGES)}
+
+    # end to end through the host-I/O entry point (pinned host buffers)
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        for _ in range(max(1, args.warmup)):
+            layer.forward_host(xh, oh)
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            layer.forward_host(xh, oh)
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        nbytes = sh.T * sh.H * 2
+        e2e = {"value": world * sh.T * args.steps / dt, "unit": UNIT,
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+
+    value = world * sh.T * args.steps / (ms_max / 1e3)
+    peaks, peak_src = load_peaks()
+    alg = workload_algorithmic(sh, n_active)
+    dom = max(per_kernel_ms, key=per_kernel_ms.get)
+    a = alg[dom]
+    t_dom = per_kernel_ms[dom] / 1e3
+    t_bw = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_fl = a["flops"] / (peaks["bf16_tflops"] * 1e12) if a["flops"] else 0.0
+    if t_fl > t_bw:
+        achieved = a["flops"] / t_dom / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
+    else:
+        achieved = a["bytes"] / t_dom / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    roof["traffic"] = ncu_traffic(dom, args.config)
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else \
+        "fallback"
+    roof["algorithmic_bytes_per_launch"] = a["bytes"]
+    roof["algorithmic_flops_per_launch"] = a["flops"]
+    lay = alg["layer"]
+    t_step = ms_max / args.steps / 1e3
+    layer_roof = {
+        "hbm_frac": lay["bytes"] / t_step / 1e9 / peaks["hbm_gbs"],
+        "tensor_frac": lay["flops"] / t_step / 1e12 / peaks["bf16_tflops"],
+        "attainable_frac": max(lay["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                               lay["flops"] / (peaks["bf16_tflops"] * 1e12)) / t_step,
+    }
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, n, dt = cpu_oracle_run(sh, d, args.cpu_tokens)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{n} seeded tokens of the {args.config} batch ({dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02) bf16 weights)",
+            "config": {"workload": f"{args.config}: T={sh.T} tokens, hidden {sh.H}, "
+                                   f"intermediate {sh.I}, {sh.E} experts in {sh.G} groups, "
+                                   f"top-{sh.topk_groups} groups, top-{sh.top_k}",
+                       "tokens_per_step_per_gpu": sh.T, "active_experts": n_active,
+                       "max_expert_load_over_mean": float(counts.max() / counts.mean()),
+                       "l2": "no flush: expert weights read per step exceed the 126 MB L2",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "layer_roofline": layer_roof,
+            "kernels_ms": per_kernel_ms,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * beam_moe.h -- C ABI of the B300 (sm_103a) Beam-style sparse MoE layer.
+ *
+ * The layer (one forward pass, no shared expert):
+ *   1. router logits  l[t,e] = sum_h x[t,h] * Wr[h,e]          (FP32)
+ *   2. scores         s[t,e] = sigmoid(l[t,e])                 (FP32)
+ *   3. group score    gs[t,g] = sum of the two largest s in group g
+ *   4. keep the topk_groups groups with the largest gs
+ *   5. pick the top_k experts by s inside the kept groups
+ *   6. weights        w[t,k] = s_k / sum_j s_j * routed_scale
+ *   7. out[t] = sum_k w[t,k] * SwiGLU_{e_k}(x[t]),
+ *      SwiGLU_e(x) = W_down[e] (silu(W_gate[e] x) * (W_up[e] x))
+ * Source: "Reflection Beam 1.0: 501B open MoE model, 1M context, Apache 2.0"
+ * (agentlenshq.com), section "Mixture of Experts: 256 experts, 8 routed per
+ * token" (256 experts, sigmoid scores, 8 groups of 32, rank groups by the sum
+ * of their top-2 scores, keep 4 groups, top-8 experts, no shared expert,
+ * normalised weights scaled by 2.5, SwiGLU experts of intermediate 2560), and
+ * the same page's section "Residual stream", last paragraph (router and the
+ * SwiGLU product in FP32).  Restated by "Beam 501B open model" (aixai.ru),
+ * section "256 experts per layer", and by the dothoosh.com news article,
+ * section "Architecture and memory efficiency".
+ *
+ * Readings taken where the pages are silent: ties go to the lower group or
+ * expert index; the selected slots are ordered by score descending, index
+ * ascending; the router sums h = 0..H-1 in order with FP32 fused
+ * multiply-adds; sigmoid(l) = 1/(1 + fp32(exp(-l))).
+ *
+ * Conventions shared by every call:
+ *  - Pointers named as device pointers are CUDA device memory owned by the
+ *    caller.  The library never allocates, frees or synchronises device
+ *    memory, except where a function says so.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued asynchronously on it; host-detectable errors
+ *    return before anything is enqueued.
+ *  - Device-detected errors (a bounded wait that ran out, a failed debug
+ *    check) are written to a status word inside the workspace; read it with
+ *    beam_moe_read_status().
+ *  - bf16 tensors are IEEE bfloat16, row-major, densely packed.
+ *  - All device pointers must be 16-byte aligned.
+ *  - Calls that share a workspace must not overlap on the GPU; calls with
+ *    distinct workspaces may run concurrently from any threads.
+ */
+#ifndef BEAM_MOE_H
+#define BEAM_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes.  Negative = error. */
+typedef enum {
+    BEAM_MOE_OK = 0,
+    BEAM_MOE_ERR_INVALID_ARG = -1,  /* bad pointer, size or configuration  */
+    BEAM_MOE_ERR_UNSUPPORTED = -2,  /* valid but not implemented           */
+    BEAM_MOE_ERR_CUDA = -3,         /* a CUDA runtime/driver call failed   */
+    BEAM_MOE_ERR_WORKSPACE = -4,    /* workspace missing or too small      */
+    BEAM_MOE_ERR_TIMEOUT = -5,      /* device: a bounded wait ran out      */
+    BEAM_MOE_ERR_DEVICE = -6        /* device: an internal check failed    */
+} beam_moe_status;
+
+/* Expert weight formats. */
+typedef enum {
+    BEAM_MOE_W_BF16 = 0,
+    BEAM_MOE_W_NVFP4 = 1
+} beam_moe_wtype;
+
+/* debug_flags bits (tests only). */
+#define BEAM_MOE_DEBUG_DROP_ONE_LOAD 0x1u /* CTA 0 of the gate/up GEMM never
+                                             arms one pipeline stage, so its
+                                             consumer's bounded wait runs out
+                                             and the call reports
+                                             BEAM_MOE_ERR_TIMEOUT            */
+
+/*
+ * Layer configuration.  Beam: hidden 5120, inter 2560, n_experts 256,
+ * n_groups 8, topk_groups 4, top_k 8, routed_scale 2.5.
+ * Requirements: hidden, inter multiples of 128; 4 <= n_experts <= 256 with
+ * n_experts % 4 == 0; 1 <= n_groups <= 32; n_experts % n_groups == 0;
+ * n_experts / n_groups <= 32; 1 <= topk_groups <= n_groups;
+ * 1 <= top_k <= min(32, topk_groups * n_experts / n_groups).
+ * Anything else returns BEAM_MOE_ERR_INVALID_ARG with nothing enqueued.
+ */
+typedef struct {
+    int hidden;          /* H */
+    int inter;           /* I */
+    int n_experts;       /* E */
+    int n_groups;        /* G */
+    int topk_groups;     /* groups kept per token */
+    int top_k;           /* experts per token (K) */
+    float routed_scale;  /* 2.5 for Beam */
+    int wtype;           /* beam_moe_wtype */
+    /* NVFP4 weights only (else NULL): per-16-element E4M3 block scales and
+       FP32 per-(expert, projection) global scales, see beam_moe_quantize_nvfp4 */
+    const void *w_gate_sf, *w_up_sf, *w_down_sf;
+    const float *w_gate_gs, *w_up_gs, *w_down_gs;
+    /* caller-owned device scratch, >= beam_moe_workspace_size() bytes,
+       256-byte aligned */
+    void *workspace;
+    size_t workspace_bytes;
+    /* bounded device waits give up after this many nanoseconds (0 = 2 s) */
+    int64_t wait_timeout_ns;
+    unsigned debug_flags; /* 0 in production */
+} beam_moe_cfg;
+
+/* Fill *cfg with the Beam layer sizes and no workspace. */
+void beam_moe_cfg_init_beam(beam_moe_cfg *cfg);
+
+/*
+ * Bytes of device workspace a call with T tokens needs (0 on an invalid
+ * configuration).  The size grows linearly with T.
+ */
+size_t beam_moe_workspace_size(int64_t T, const beam_moe_cfg *cfg);
+
+/*
+ * Routing only (steps 1-6) plus the expert histogram.
+ *   x        [T,H] bf16, device
+ *   router_w [H,E] fp32, device (hidden-major)
+ *   topk_ids [T,K] int32, device, out: expert ids in slot order
+ *   topk_w   [T,K] fp32, device, out: combine weights (sum = routed_scale)
+ *   scores   [T,E] fp32, device, out, or NULL: the sigmoid scores
+ *   counts   [E]   int32, device, out, or NULL: tokens routed to each expert
+ *   offsets  [E+1] int32, device, out, or NULL: exclusive prefix of counts
+ *   row_of   [T,K] int32, device, out, or NULL: row of pair (t,k) in the
+ *            expert-grouped order (experts ascending, tokens ascending)
+ * T = 0 is a successful no-op.  Requires T * K < 2^31.
+ */
+int beam_moe_route(const void *x, const float *router_w, int64_t T,
+                   const beam_moe_cfg *cfg, int32_t *topk_ids, float *topk_w,
+                   float *scores, int32_t *counts, int32_t *offsets,
+                   int32_t *row_of, void *stream);
+
+/*
+ * The whole layer forward (steps 1-7).
+ *   x        [T,H] bf16, device
+ *   router_w [H,E] fp32, device
+ *   w_gate   [E,I,H] bf16, device (per expert: nn.Linear [out=I, in=H])
+ *   w_up     [E,I,H] bf16, device
+ *   w_down   [E,H,I] bf16, device (per expert: [out=H, in=I])
+ *   out      [T,H] bf16, device, written
+ * With cfg->wtype == BEAM_MOE_W_NVFP4 the three weight pointers are packed
+ * E2M1 codes as produced by beam_moe_quantize_nvfp4.
+ * Deterministic: the same inputs give bitwise the same output.
+ */
+int beam_moe_forward(const void *x, const float *router_w, const void *w_gate,
+                     const void *w_up, const void *w_down, int64_t T,
+                     const beam_moe_cfg *cfg, void *out, void *stream);
+
+/*
+ * beam_moe_forward with the activations in HOST memory: copies x_host
+ * ([T,H] bf16, pinned for best speed) to the workspace, runs the layer and
+ * copies the result back to out_host ([T,H] bf16).  Weights stay in device
+ * memory.  Synchronises `stream` before returning, so out_host is ready.
+ * Needs beam_moe_workspace_size(T) + 2*T*H*2 bytes of workspace.
+ */
+int beam_moe_forward_hostio(const void *x_host, const float *router_w,
+                            const void *w_gate, const void *w_up,
+                            const void *w_down, int64_t T,
+                            const beam_moe_cfg *cfg, void *out_host,
+                            void *stream);
+
+/* Extra workspace bytes beam_moe_forward_hostio needs on top of
+   beam_moe_workspace_size(). */
+size_t beam_moe_hostio_extra_bytes(int64_t T, const beam_moe_cfg *cfg);
+
+/*
+ * NVFP4 weight quantisation (E2M1 values, one E4M3 scale per 16 consecutive
+ * elements of a row, one FP32 global scale per matrix).
+ *   w        [n_mat, rows, cols] bf16, device; cols % 16 == 0
+ *   packed   [n_mat, rows, cols/2] uint8, device, out (two codes per byte,
+ *            element 2j in the low nibble)
+ *   block_sf [n_mat, rows, cols/16] uint8, device, out (E4M3 bits)
+ *   global_sf[n_mat] fp32, device, out: amax(|w|)/(6*448) per matrix
+ * The pages name the format only ("most parameters in 4 bits"); the exact
+ * recipe is a reading: sf = e4m3(amax16 / 6 / gs), q = e2m1(v / (sf * gs)),
+ * round to nearest even, saturating.
+ */
+int beam_moe_quantize_nvfp4(const void *w, int64_t n_mat, int64_t rows,
+                            int64_t cols, void *packed, void *block_sf,
+                            float *global_sf, void *stream);
+
+/*
+ * Synchronise `stream`, read the device status word of cfg->workspace and
+ * clear it.  Returns BEAM_MOE_OK, BEAM_MOE_ERR_TIMEOUT or BEAM_MOE_ERR_DEVICE
+ * (or BEAM_MOE_ERR_CUDA if the synchronisation itself failed).
+ */
+int beam_moe_read_status(const beam_moe_cfg *cfg, void *stream);
+
+/* Static text for a return code. */
+const char *beam_moe_status_string(int code);
+
+/* Number of kernels the library has launched from the calling host thread. */
+int64_t beam_moe_launch_count(void);
+
+/*
+ * Per-kernel timing hook for benchmarks.  With n > 0, each kernel the
+ * library launches from the calling host thread is bracketed by
+ * cudaEventRecord(start[i]) and cudaEventRecord(stop[i]) on its stream, i
+ * being the kernel's stage: 0 router scores, 1 selection, 2 histogram,
+ * 3 scan, 4 permute, 5 gate/up GEMM, 6 down GEMM, 7 combine.  Events are
+ * cudaEvent_t handles passed as void*, owned by the caller and alive while
+ * set; n = 0 turns the hook off.  Returns BEAM_MOE_ERR_INVALID_ARG for
+ * n < 0, n > 8 or NULL arrays.
+ */
+int beam_moe_set_kernel_events(void *const *start, void *const *stop, int n);
+
+/* Number of streaming multiprocessors of the current device (0 if none). */
+int beam_moe_device_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BEAM_MOE_H */

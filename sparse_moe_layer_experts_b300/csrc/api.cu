@@ -1,0 +1,444 @@
+// C ABI of libbeam_moe.so: argument checks, workspace layout, TMA tensor
+// maps and the launch sequence of one Beam MoE layer forward.
+//
+//   router_scores -> select -> hist -> scan -> permute -> gate/up GEMM
+//   -> down GEMM -> combine          (one stream, no host synchronisation)
+#include "../../include/beam_moe.h"
+#include "common.cuh"
+#include "internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace beam {
+
+static thread_local int64_t g_launches = 0;
+static thread_local cudaEvent_t g_ev_start[kNumStages];
+static thread_local cudaEvent_t g_ev_stop[kNumStages];
+static thread_local int g_ev_n = 0;
+
+void stage_begin(int stage, cudaStream_t s)
+{
+    if (stage < g_ev_n && g_ev_start[stage])
+        cudaEventRecord(g_ev_start[stage], s);
+}
+
+void stage_end(int stage, cudaStream_t s)
+{
+    ++g_launches;
+    if (stage < g_ev_n && g_ev_stop[stage])
+        cudaEventRecord(g_ev_stop[stage], s);
+}
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+    size_t status, scores, ids, wts, local_rank, cta_counts, cta_base, counts, offsets,
+        chunk_start, row_of, row_src, x_perm, h, y, total;
+};
+
+Layout make_layout(int64_t T, const beam_moe_cfg &c)
+{
+    const int64_t K = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
+    const int64_t n_cta = (T + kHistTokens - 1) / kHistTokens;
+    const int64_t R = T * K;
+    Layout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes);
+        return at;
+    };
+    L.status = take(256);
+    L.scores = take(sizeof(float) * T * E);
+    L.ids = take(sizeof(int32_t) * R);
+    L.wts = take(sizeof(float) * R);
+    L.local_rank = take(sizeof(int32_t) * R);
+    L.cta_counts = take(sizeof(int32_t) * n_cta * E);
+    L.cta_base = take(sizeof(int32_t) * n_cta * E);
+    L.counts = take(sizeof(int32_t) * E);
+    L.offsets = take(sizeof(int32_t) * (E + 1));
+    L.chunk_start = take(sizeof(int32_t) * (E + 1));
+    L.row_of = take(sizeof(int32_t) * R);
+    L.row_src = take(sizeof(int32_t) * R);
+    L.x_perm = take(2 * R * H);
+    L.h = take(2 * R * I);
+    L.y = take(4 * R * H);
+    L.total = o;
+    return L;
+}
+
+template <typename T>
+T *at(void *ws, size_t off)
+{
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_cfg(const beam_moe_cfg *c)
+{
+    if (!c)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (c->hidden <= 0 || c->inter <= 0 || c->hidden % 128 || c->inter % 128)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (c->n_experts < 1 || c->n_experts > 256 || c->n_experts % 4)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (c->n_groups < 1 || c->n_groups > 32 || c->n_experts % c->n_groups)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    const int gsize = c->n_experts / c->n_groups;
+    if (gsize > 32 || c->topk_groups < 1 || c->topk_groups > c->n_groups)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (c->top_k < 1 || c->top_k > 32 || c->top_k > c->topk_groups * gsize)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (!(c->routed_scale == c->routed_scale))  // NaN
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (c->wtype != BEAM_MOE_W_BF16 && c->wtype != BEAM_MOE_W_NVFP4)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    return BEAM_MOE_OK;
+}
+
+int check_T(int64_t T, const beam_moe_cfg *c)
+{
+    if (T < 0 || T * (int64_t)c->top_k >= (int64_t(1) << 31) || T > (int64_t(1) << 24))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    return BEAM_MOE_OK;
+}
+
+int check_ws(int64_t T, const beam_moe_cfg *c, size_t need)
+{
+    if (!c->workspace || (reinterpret_cast<uintptr_t>(c->workspace) & 255u))
+        return BEAM_MOE_ERR_WORKSPACE;
+    if (c->workspace_bytes < need)
+        return BEAM_MOE_ERR_WORKSPACE;
+    (void)T;
+    return BEAM_MOE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [outer, inner] (inner contiguous), box [box_outer, 64],
+// 128-byte swizzle, zero fill outside.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int device_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+GemmVariant pick_variant(int64_t T, const beam_moe_cfg &c)
+{
+    // decode: a handful of tokens per active expert
+    return (T * c.top_k <= 16LL * c.n_experts) ? GemmVariant::kDecode : GemmVariant::kPrefill;
+}
+
+#define BEAM_CUDA(call)                          \
+    do {                                         \
+        if ((call) != cudaSuccess)               \
+            return BEAM_MOE_ERR_CUDA;            \
+    } while (0)
+
+// Steps 1-6 plus histogram/scan into the workspace.
+int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cfg &c,
+              const Layout &L, float *scores, int32_t *ids, float *wts, int chunk_rows,
+              cudaStream_t s)
+{
+    void *ws = c.workspace;
+    int *status = at<int>(ws, L.status);
+    const int n_cta = (int)((T + kHistTokens - 1) / kHistTokens);
+    BEAM_CUDA(launch_router_scores(static_cast<const uint16_t *>(x), router_w, (int)T, c.hidden,
+                                   c.n_experts, scores, status, s));
+    BEAM_CUDA(launch_select(scores, (int)T, c.n_experts, c.n_groups, c.topk_groups, c.top_k,
+                            c.routed_scale, ids, wts, status, s));
+    BEAM_CUDA(launch_hist(ids, (int)T, c.top_k, c.n_experts, at<int32_t>(ws, L.local_rank),
+                          at<int32_t>(ws, L.cta_counts), status, s));
+    BEAM_CUDA(launch_scan(at<int32_t>(ws, L.cta_counts), n_cta, c.n_experts, chunk_rows,
+                          at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.counts),
+                          at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start), s));
+    return BEAM_MOE_OK;
+}
+
+int run_forward(const void *x, const float *router_w, const void *w_gate, const void *w_up,
+                const void *w_down, int64_t T, const beam_moe_cfg &c, void *out, cudaStream_t s)
+{
+    const Layout L = make_layout(T, c);
+    void *ws = c.workspace;
+    const GemmVariant v = pick_variant(T, c);
+    const int chunk = gemm_chunk_rows(v);
+    int rc = run_route(x, router_w, T, c, L, at<float>(ws, L.scores), at<int32_t>(ws, L.ids),
+                       at<float>(ws, L.wts), chunk, s);
+    if (rc != BEAM_MOE_OK)
+        return rc;
+    const int K = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
+    const int64_t R = T * K;
+    BEAM_CUDA(launch_permute(static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids),
+                             at<int32_t>(ws, L.local_rank), at<int32_t>(ws, L.cta_base),
+                             at<int32_t>(ws, L.offsets), (int)T, K, E, H, at<int32_t>(ws, L.row_of),
+                             at<int32_t>(ws, L.row_src), at<uint16_t>(ws, L.x_perm), s));
+
+    CUtensorMap m_wg, m_wu, m_wd, m_xp, m_h;
+    if (!make_map(&m_wg, w_gate, H, (uint64_t)E * I, 128) ||
+        !make_map(&m_wu, w_up, H, (uint64_t)E * I, 128) ||
+        !make_map(&m_wd, w_down, I, (uint64_t)E * H, 128) ||
+        !make_map(&m_xp, at<void>(ws, L.x_perm), H, (uint64_t)R, 16) ||
+        !make_map(&m_h, at<void>(ws, L.h), I, (uint64_t)R, 16))
+        return BEAM_MOE_ERR_CUDA;
+
+    const int sms = device_sms();
+    if (sms <= 0)
+        return BEAM_MOE_ERR_CUDA;
+    GemmArgs a{};
+    a.offsets = at<int32_t>(ws, L.offsets);
+    a.chunk_start = at<int32_t>(ws, L.chunk_start);
+    a.E = E;
+    a.status = at<int>(ws, L.status);
+    a.timeout_ns = c.wait_timeout_ns > 0 ? (unsigned long long)c.wait_timeout_ns : kDefaultTimeoutNs;
+    a.debug_flags = c.debug_flags;
+
+    a.m_tiles = I / 128;
+    a.ksteps = H / 64;
+    a.out = at<void>(ws, L.h);
+    a.out_ld = I;
+    BEAM_CUDA(launch_gateup(v, m_wg, m_wu, m_xp, a, sms, s));
+
+    a.m_tiles = H / 128;
+    a.ksteps = I / 64;
+    a.out = at<void>(ws, L.y);
+    a.out_ld = H;
+    a.debug_flags = 0;
+    BEAM_CUDA(launch_down(v, m_wd, m_h, a, sms, s));
+
+    BEAM_CUDA(launch_combine(at<float>(ws, L.y), at<float>(ws, L.wts), at<int32_t>(ws, L.row_of),
+                             (int)T, K, H, static_cast<uint16_t *>(out), s));
+    return BEAM_MOE_OK;
+}
+
+}  // namespace
+}  // namespace beam
+
+using namespace beam;
+
+extern "C" {
+
+void beam_moe_cfg_init_beam(beam_moe_cfg *cfg)
+{
+    if (!cfg)
+        return;
+    *cfg = beam_moe_cfg{};
+    cfg->hidden = 5120;
+    cfg->inter = 2560;
+    cfg->n_experts = 256;
+    cfg->n_groups = 8;
+    cfg->topk_groups = 4;
+    cfg->top_k = 8;
+    cfg->routed_scale = 2.5f;
+    cfg->wtype = BEAM_MOE_W_BF16;
+}
+
+size_t beam_moe_workspace_size(int64_t T, const beam_moe_cfg *cfg)
+{
+    if (check_cfg(cfg) != BEAM_MOE_OK || T < 0)
+        return 0;
+    return make_layout(T, *cfg).total;
+}
+
+size_t beam_moe_hostio_extra_bytes(int64_t T, const beam_moe_cfg *cfg)
+{
+    if (check_cfg(cfg) != BEAM_MOE_OK || T < 0)
+        return 0;
+    return 2 * align_up((size_t)T * cfg->hidden * 2);
+}
+
+int beam_moe_route(const void *x, const float *router_w, int64_t T, const beam_moe_cfg *cfg,
+                   int32_t *topk_ids, float *topk_w, float *scores, int32_t *counts,
+                   int32_t *offsets, int32_t *row_of, void *stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc != BEAM_MOE_OK)
+        return rc;
+    if ((rc = check_T(T, cfg)) != BEAM_MOE_OK)
+        return rc;
+    if (T == 0)
+        return BEAM_MOE_OK;
+    if (!x || !router_w || !topk_ids || !topk_w || !aligned16(x) || !aligned16(router_w))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    const beam_moe_cfg &c = *cfg;
+    const Layout L = make_layout(T, c);
+    if ((rc = check_ws(T, cfg, L.total)) != BEAM_MOE_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *ws = c.workspace;
+    float *sc = scores ? scores : at<float>(ws, L.scores);
+    rc = run_route(x, router_w, T, c, L, sc, topk_ids, topk_w, gemm_chunk_rows(pick_variant(T, c)),
+                   s);
+    if (rc != BEAM_MOE_OK)
+        return rc;
+    const int E = c.n_experts;
+    if (counts)
+        BEAM_CUDA(cudaMemcpyAsync(counts, at<int32_t>(ws, L.counts), sizeof(int32_t) * E,
+                                  cudaMemcpyDeviceToDevice, s));
+    if (offsets)
+        BEAM_CUDA(cudaMemcpyAsync(offsets, at<int32_t>(ws, L.offsets), sizeof(int32_t) * (E + 1),
+                                  cudaMemcpyDeviceToDevice, s));
+    if (row_of)
+        BEAM_CUDA(launch_rows(topk_ids, at<int32_t>(ws, L.local_rank), at<int32_t>(ws, L.cta_base),
+                              at<int32_t>(ws, L.offsets), (int)T, c.top_k, E, row_of, s));
+    return BEAM_MOE_OK;
+}
+
+int beam_moe_forward(const void *x, const float *router_w, const void *w_gate, const void *w_up,
+                     const void *w_down, int64_t T, const beam_moe_cfg *cfg, void *out,
+                     void *stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc != BEAM_MOE_OK)
+        return rc;
+    if ((rc = check_T(T, cfg)) != BEAM_MOE_OK)
+        return rc;
+    if (T == 0)
+        return BEAM_MOE_OK;
+    if (cfg->wtype != BEAM_MOE_W_BF16)
+        return BEAM_MOE_ERR_UNSUPPORTED;
+    if (!x || !router_w || !w_gate || !w_up || !w_down || !out)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(router_w) || !aligned16(w_gate) || !aligned16(w_up) ||
+        !aligned16(w_down) || !aligned16(out))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(T, cfg, make_layout(T, *cfg).total)) != BEAM_MOE_OK)
+        return rc;
+    return run_forward(x, router_w, w_gate, w_up, w_down, T, *cfg, out,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int beam_moe_forward_hostio(const void *x_host, const float *router_w, const void *w_gate,
+                            const void *w_up, const void *w_down, int64_t T,
+                            const beam_moe_cfg *cfg, void *out_host, void *stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc != BEAM_MOE_OK)
+        return rc;
+    if ((rc = check_T(T, cfg)) != BEAM_MOE_OK)
+        return rc;
+    if (T == 0)
+        return BEAM_MOE_OK;
+    if (!x_host || !out_host)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    const size_t base = make_layout(T, *cfg).total;
+    const size_t act = align_up((size_t)T * cfg->hidden * 2);
+    if ((rc = check_ws(T, cfg, base + 2 * act)) != BEAM_MOE_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *x_dev = at<void>(cfg->workspace, base);
+    void *o_dev = at<void>(cfg->workspace, base + act);
+    const size_t bytes = (size_t)T * cfg->hidden * 2;
+    BEAM_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s));
+    rc = beam_moe_forward(x_dev, router_w, w_gate, w_up, w_down, T, cfg, o_dev, stream);
+    if (rc != BEAM_MOE_OK)
+        return rc;
+    BEAM_CUDA(cudaMemcpyAsync(out_host, o_dev, bytes, cudaMemcpyDeviceToHost, s));
+    BEAM_CUDA(cudaStreamSynchronize(s));
+    return BEAM_MOE_OK;
+}
+
+int beam_moe_quantize_nvfp4(const void *w, int64_t n_mat, int64_t rows, int64_t cols,
+                            void *packed, void *block_sf, float *global_sf, void *stream)
+{
+    (void)w;
+    (void)n_mat;
+    (void)rows;
+    (void)cols;
+    (void)packed;
+    (void)block_sf;
+    (void)global_sf;
+    (void)stream;
+    return BEAM_MOE_ERR_UNSUPPORTED;
+}
+
+int beam_moe_read_status(const beam_moe_cfg *cfg, void *stream)
+{
+    if (!cfg || !cfg->workspace || cfg->workspace_bytes < 256)
+        return BEAM_MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int word = 0;
+    if (cudaMemcpyAsync(&word, cfg->workspace, sizeof(int), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return BEAM_MOE_ERR_CUDA;
+    if (cudaMemsetAsync(cfg->workspace, 0, sizeof(int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return BEAM_MOE_ERR_CUDA;
+    if (word & kStatusTimeout)
+        return BEAM_MOE_ERR_TIMEOUT;
+    if (word & kStatusDevice)
+        return BEAM_MOE_ERR_DEVICE;
+    return BEAM_MOE_OK;
+}
+
+const char *beam_moe_status_string(int code)
+{
+    switch (code) {
+    case BEAM_MOE_OK: return "ok";
+    case BEAM_MOE_ERR_INVALID_ARG: return "invalid argument";
+    case BEAM_MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case BEAM_MOE_ERR_CUDA: return "CUDA call failed";
+    case BEAM_MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case BEAM_MOE_ERR_TIMEOUT: return "device wait timed out";
+    case BEAM_MOE_ERR_DEVICE: return "device-side check failed";
+    default: return "unknown status";
+    }
+}
+
+int64_t beam_moe_launch_count(void) { return g_launches; }
+
+int beam_moe_set_kernel_events(void *const *start, void *const *stop, int n)
+{
+    if (n < 0 || n > kNumStages || (n > 0 && (!start || !stop)))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < kNumStages; ++i) {
+        g_ev_start[i] = i < n ? static_cast<cudaEvent_t>(start[i]) : nullptr;
+        g_ev_stop[i] = i < n ? static_cast<cudaEvent_t>(stop[i]) : nullptr;
+    }
+    g_ev_n = n;
+    return BEAM_MOE_OK;
+}
+
+int beam_moe_device_sms(void) { return device_sms(); }
+
+}  // extern "C"

@@ -1,0 +1,244 @@
+// Expert dispatch of the Beam MoE layer: histogram of the routed (token,
+// slot) pairs, exclusive offsets, the expert-grouped permutation of token
+// rows, and the deterministic weighted combine back to token order.
+//
+// The order of rows inside an expert's segment is token-ascending (the pages
+// do not fix it; this order makes the permutation unique and reproducible).
+// The combine sums the K expert outputs of a token in slot order k = 0..K-1
+// ("Reflection Beam 1.0" (agentlenshq.com), section "Mixture of Experts":
+// expert outputs are combined with the normalised router weights).
+#include "common.cuh"
+#include "internal.h"
+
+namespace beam {
+
+namespace {
+
+// CTA = 8 warps = 256 tokens.  mask[w][e] has bit l set when token
+// (warp w, lane l) routes to expert e; a pair's rank inside its expert and
+// CTA is the number of earlier tokens (lower warp, or lower lane in the same
+// warp) with that expert.
+__global__ void __launch_bounds__(256)
+hist_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int32_t *__restrict__ local_rank,
+            int32_t *__restrict__ cta_counts, int *status)
+{
+    __shared__ uint32_t mask[8][256];
+    __shared__ int32_t prefix[8][256];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < 8 * 256; i += 256)
+        (&mask[0][0])[i] = 0u;
+    __syncthreads();
+    const int t = blockIdx.x * kHistTokens + tid;
+    if (t < T) {
+        for (int k = 0; k < K; ++k) {
+            const int e = ids[(size_t)t * K + k];
+            if (e < 0 || e >= E) {
+                atomicOr(status, kStatusDevice);
+                continue;
+            }
+            atomicOr(&mask[warp][e], 1u << lane);
+        }
+    }
+    __syncthreads();
+    if (tid < E) {
+        int run = 0;
+        for (int w = 0; w < 8; ++w) {
+            prefix[w][tid] = run;
+            run += __popc(mask[w][tid]);
+        }
+        cta_counts[(size_t)blockIdx.x * E + tid] = run;
+    }
+    __syncthreads();
+    if (t < T) {
+        const uint32_t below = (1u << lane) - 1u;
+        for (int k = 0; k < K; ++k) {
+            const int e = ids[(size_t)t * K + k];
+            int r = 0;
+            if (e >= 0 && e < E)
+                r = prefix[warp][e] + __popc(mask[warp][e] & below);
+            local_rank[(size_t)t * K + k] = r;
+        }
+    }
+}
+
+// Exclusive scan over the E (<= 256) values held one per thread.
+__device__ int block_exclusive_scan_256(int v, int *tmp, int *total)
+{
+    const int tid = threadIdx.x;
+    tmp[tid] = v;
+    __syncthreads();
+    for (int off = 1; off < 256; off <<= 1) {
+        const int add = (tid >= off) ? tmp[tid - off] : 0;
+        __syncthreads();
+        tmp[tid] += add;
+        __syncthreads();
+    }
+    const int incl = tmp[tid];
+    *total = tmp[255];
+    __syncthreads();
+    return incl - v;
+}
+
+// One CTA of 256 threads, thread e owns expert e.
+__global__ void __launch_bounds__(256)
+scan_kernel(const int32_t *__restrict__ cta_counts, int n_cta, int E, int chunk_rows,
+            int32_t *__restrict__ cta_base, int32_t *__restrict__ counts,
+            int32_t *__restrict__ offsets, int32_t *__restrict__ chunk_start)
+{
+    __shared__ int tmp[256];
+    const int e = threadIdx.x;
+    int run = 0;
+    if (e < E) {
+        for (int c = 0; c < n_cta; ++c) {
+            const int v = cta_counts[(size_t)c * E + e];
+            cta_base[(size_t)c * E + e] = run;
+            run += v;
+        }
+        counts[e] = run;
+    }
+    int total = 0;
+    const int off = block_exclusive_scan_256(e < E ? run : 0, tmp, &total);
+    if (e < E)
+        offsets[e] = off;
+    if (e == 0)
+        offsets[E] = total;
+    const int nchunk = (e < E) ? (run + chunk_rows - 1) / chunk_rows : 0;
+    int total_chunks = 0;
+    const int cs = block_exclusive_scan_256(nchunk, tmp, &total_chunks);
+    if (e < E)
+        chunk_start[e] = cs;
+    if (e == 0)
+        chunk_start[E] = total_chunks;
+}
+
+// CTA per token, warp per slot: place the pair's row, copy the token's
+// activations into the expert-grouped buffer with 16-byte accesses.
+__global__ void __launch_bounds__(256)
+permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
+               const int32_t *__restrict__ local_rank, const int32_t *__restrict__ cta_base,
+               const int32_t *__restrict__ offsets, int T, int K, int E, int H,
+               int32_t *__restrict__ row_of, int32_t *__restrict__ row_src,
+               uint16_t *__restrict__ x_perm)
+{
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = t / kHistTokens;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+    const int nvec = H / 8;
+    for (int k = warp; k < K; k += 8) {
+        int e = ids[(size_t)t * K + k];
+        e = (e < 0 || e >= E) ? 0 : e;
+        const int row = offsets[e] + cta_base[(size_t)cta * E + e] + local_rank[(size_t)t * K + k];
+        if (lane == 0) {
+            row_of[(size_t)t * K + k] = row;
+            row_src[row] = t;
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)row * H);
+        for (int i = lane; i < nvec; i += 32)
+            dst[i] = src[i];
+    }
+}
+
+__global__ void __launch_bounds__(256)
+rows_kernel(const int32_t *__restrict__ ids, const int32_t *__restrict__ local_rank,
+            const int32_t *__restrict__ cta_base, const int32_t *__restrict__ offsets, int T, int K,
+            int E, int32_t *__restrict__ row_of)
+{
+    const size_t i = (size_t)blockIdx.x * 256 + threadIdx.x;
+    if (i >= (size_t)T * K)
+        return;
+    const int t = (int)(i / K);
+    int e = ids[i];
+    e = (e < 0 || e >= E) ? 0 : e;
+    row_of[i] = offsets[e] + cta_base[(size_t)(t / kHistTokens) * E + e] + local_rank[i];
+}
+
+// out[t,:] = bf16( sum_{k=0..K-1} w[t,k] * y[row_of[t,k], :] ), FP32 FMA chain
+// in ascending k.
+__global__ void __launch_bounds__(256)
+combine_kernel(const float *__restrict__ y, const float *__restrict__ w,
+               const int32_t *__restrict__ row_of, int T, int K, int H, uint16_t *__restrict__ out)
+{
+    __shared__ float ws[32];
+    __shared__ int rs[32];
+    const int t = blockIdx.x;
+    if (threadIdx.x < K) {
+        ws[threadIdx.x] = w[(size_t)t * K + threadIdx.x];
+        rs[threadIdx.x] = row_of[(size_t)t * K + threadIdx.x];
+    }
+    __syncthreads();
+    const int nvec = H / 4;
+    for (int i = threadIdx.x; i < nvec; i += 256) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < K; ++k) {
+            const float4 q = reinterpret_cast<const float4 *>(y + (size_t)rs[k] * H)[i];
+            const float wk = ws[k];
+            acc.x = __fmaf_rn(wk, q.x, acc.x);
+            acc.y = __fmaf_rn(wk, q.y, acc.y);
+            acc.z = __fmaf_rn(wk, q.z, acc.z);
+            acc.w = __fmaf_rn(wk, q.w, acc.w);
+        }
+        uint2 o;
+        o.x = pack_bf16x2(acc.x, acc.y);
+        o.y = pack_bf16x2(acc.z, acc.w);
+        reinterpret_cast<uint2 *>(out + (size_t)t * H)[i] = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_hist(const int32_t *ids, int T, int K, int E, int32_t *local_rank,
+                        int32_t *cta_counts, int *status, cudaStream_t s)
+{
+    stage_begin(kStHist, s);
+    hist_kernel<<<(T + kHistTokens - 1) / kHistTokens, 256, 0, s>>>(ids, T, K, E, local_rank,
+                                                                    cta_counts, status);
+    stage_end(kStHist, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int32_t *cta_counts, int n_cta, int E, int chunk_rows,
+                        int32_t *cta_base, int32_t *counts, int32_t *offsets,
+                        int32_t *chunk_start, cudaStream_t s)
+{
+    stage_begin(kStScan, s);
+    scan_kernel<<<1, 256, 0, s>>>(cta_counts, n_cta, E, chunk_rows, cta_base, counts, offsets,
+                                  chunk_start);
+    stage_end(kStScan, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
+                           const int32_t *cta_base, const int32_t *offsets, int T, int K, int E,
+                           int H, int32_t *row_of, int32_t *row_src, uint16_t *x_perm,
+                           cudaStream_t s)
+{
+    stage_begin(kStPermute, s);
+    permute_kernel<<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, T, K, E, H, row_of,
+                                     row_src, x_perm);
+    stage_end(kStPermute, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int32_t *cta_base,
+                        const int32_t *offsets, int T, int K, int E, int32_t *row_of,
+                        cudaStream_t s)
+{
+    const size_t n = (size_t)T * K;
+    stage_begin(kStPermute, s);
+    rows_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ids, local_rank, cta_base, offsets, T,
+                                                             K, E, row_of);
+    stage_end(kStPermute, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float *y, const float *w, const int32_t *row_of, int T, int K,
+                           int H, uint16_t *out, cudaStream_t s)
+{
+    stage_begin(kStCombine, s);
+    combine_kernel<<<T, 256, 0, s>>>(y, w, row_of, T, K, H, out);
+    stage_end(kStCombine, s);
+    return cudaGetLastError();
+}
+
+}  // namespace beam

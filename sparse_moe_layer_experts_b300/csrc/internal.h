@@ -1,0 +1,82 @@
+// Internal launchers shared by the translation units of libbeam_moe.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace beam {
+
+// Kernel stages, in launch order; the index of the optional timing events.
+enum Stage {
+    kStRouter = 0,
+    kStSelect,
+    kStHist,
+    kStScan,
+    kStPermute,
+    kStGateUp,
+    kStDown,
+    kStCombine,
+    kNumStages
+};
+// Bracket one kernel launch: records the calling thread's timing events for
+// the stage (if any are set) and counts the launch.
+void stage_begin(int stage, cudaStream_t s);
+void stage_end(int stage, cudaStream_t s);
+
+// ---- router.cu
+// scores[t,e] = sigmoid(sum_h x[t,h] * wr[h,e]) with an FP32 FMA chain in
+// ascending h per output.
+// Also resets *status (the call's device status word) to 0.
+cudaError_t launch_router_scores(const uint16_t *x, const float *wr, int T, int H, int E,
+                                 float *scores, int *status, cudaStream_t s);
+// Group-limited top-k over scores -> ids [T,K], w [T,K].
+cudaError_t launch_select(const float *scores, int T, int E, int G, int TG, int K, float scale,
+                          int32_t *ids, float *w, int *status, cudaStream_t s);
+
+// ---- dispatch.cu
+constexpr int kHistTokens = 256;  // tokens per histogram CTA
+cudaError_t launch_hist(const int32_t *ids, int T, int K, int E, int32_t *local_rank,
+                        int32_t *cta_counts, int *status, cudaStream_t s);
+cudaError_t launch_scan(const int32_t *cta_counts, int n_cta, int E, int chunk_rows,
+                        int32_t *cta_base, int32_t *counts, int32_t *offsets,
+                        int32_t *chunk_start, cudaStream_t s);
+cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
+                           const int32_t *cta_base, const int32_t *offsets, int T, int K, int E,
+                           int H, int32_t *row_of, int32_t *row_src, uint16_t *x_perm,
+                           cudaStream_t s);
+// route-only variant: row_of without moving activations
+cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int32_t *cta_base,
+                        const int32_t *offsets, int T, int K, int E, int32_t *row_of,
+                        cudaStream_t s);
+cudaError_t launch_combine(const float *y, const float *w, const int32_t *row_of, int T, int K,
+                           int H, uint16_t *out, cudaStream_t s);
+
+// ---- grouped_gemm.cu
+struct GemmArgs {
+    const int32_t *offsets;      // [E+1] rows of each expert in the permuted order
+    const int32_t *chunk_start;  // [E+1] prefix of per-expert row chunks
+    int E;
+    int m_tiles;    // weight rows per expert / 128
+    int ksteps;     // reduction length / 64
+    void *out;      // gate/up: h bf16 [R, ld]; down: y fp32 [R, ld]
+    int out_ld;
+    int *status;
+    unsigned long long timeout_ns;
+    unsigned debug_flags;
+};
+
+enum class GemmVariant { kDecode, kPrefill };
+
+// chunk height (rows of one expert handled by one tile) of a variant
+int gemm_chunk_rows(GemmVariant v);
+
+// h = silu(x_perm . Wg^T) * (x_perm . Wu^T) per expert segment (bf16 out)
+cudaError_t launch_gateup(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
+                          const CUtensorMap &xp, const GemmArgs &a, int grid, cudaStream_t s);
+// y = h . Wd^T per expert segment (fp32 out)
+cudaError_t launch_down(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
+                        const GemmArgs &a, int grid, cudaStream_t s);
+
+}  // namespace beam

@@ -1,0 +1,101 @@
+"""torch-facing wrapper of the C ABI: one Beam MoE layer with resident weights.
+
+Marshalling only (shapes, dtypes, device pointers, the workspace tensor); all
+arithmetic runs in libbeam_moe.so.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+def _stream_handle(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class BeamMoE:
+    """Resident-weight layer.  Weights: w_gate/w_up [E,I,H] bf16, w_down [E,H,I]
+    bf16, router_w [H,E] fp32, all contiguous on one CUDA device."""
+
+    def __init__(self, router_w, w_gate, w_up, w_down, n_groups=8, topk_groups=4, top_k=8,
+                 routed_scale=2.5, wait_timeout_ns=0, debug_flags=0):
+        E, I, H = w_gate.shape
+        for t, shape, dt in ((router_w, (H, E), torch.float32), (w_gate, (E, I, H), torch.bfloat16),
+                             (w_up, (E, I, H), torch.bfloat16), (w_down, (E, H, I), torch.bfloat16)):
+            if tuple(t.shape) != shape or t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"expected contiguous CUDA {dt} of shape {shape}")
+        self.router_w, self.w_gate, self.w_up, self.w_down = router_w, w_gate, w_up, w_down
+        self.H, self.I, self.E = H, I, E
+        self.cfg = B.make_cfg(H, I, E, n_groups, topk_groups, top_k, routed_scale)
+        self.cfg.wait_timeout_ns = wait_timeout_ns
+        self.cfg.debug_flags = debug_flags
+        self.device = w_gate.device
+        self._ws = None
+
+    @property
+    def top_k(self):
+        return self.cfg.top_k
+
+    def workspace(self, T: int, extra: int = 0) -> torch.Tensor:
+        need = B.beam_moe_workspace_size(T, self.cfg)
+        if need == 0:
+            raise ValueError("invalid layer configuration")
+        need += extra
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        self.cfg.workspace = self._ws.data_ptr()
+        self.cfg.workspace_bytes = self._ws.numel()
+        return self._ws
+
+    def _check_x(self, x):
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != self.H or not x.is_contiguous():
+            raise ValueError("x must be contiguous bf16 [T, H]")
+
+    def route(self, x, want_scores=True, stream=None):
+        self._check_x(x)
+        T, K, E = x.shape[0], self.top_k, self.E
+        dev = x.device
+        out = dict(
+            ids=torch.empty((T, K), dtype=torch.int32, device=dev),
+            w=torch.empty((T, K), dtype=torch.float32, device=dev),
+            scores=torch.empty((T, E), dtype=torch.float32, device=dev) if want_scores else None,
+            counts=torch.empty(E, dtype=torch.int32, device=dev),
+            offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            row_of=torch.empty((T, K), dtype=torch.int32, device=dev),
+        )
+        self.workspace(T)
+        p = lambda t: t.data_ptr() if t is not None else None
+        B.check(B.beam_moe_route(x.data_ptr(), self.router_w.data_ptr(), T, self.cfg,
+                                 p(out["ids"]), p(out["w"]), p(out["scores"]), p(out["counts"]),
+                                 p(out["offsets"]), p(out["row_of"]), _stream_handle(stream)),
+                "beam_moe_route")
+        return out
+
+    def forward(self, x, out=None, stream=None):
+        self._check_x(x)
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty_like(x)
+        self.workspace(T)
+        B.check(B.beam_moe_forward(x.data_ptr(), self.router_w.data_ptr(), self.w_gate.data_ptr(),
+                                   self.w_up.data_ptr(), self.w_down.data_ptr(), T, self.cfg,
+                                   out.data_ptr(), _stream_handle(stream)), "beam_moe_forward")
+        return out
+
+    def forward_host(self, x_host, out_host, stream=None):
+        """x_host/out_host: CPU bf16 [T,H] tensors (pinned for speed)."""
+        if x_host.is_cuda or out_host.is_cuda:
+            raise ValueError("host tensors expected")
+        self._check_x(x_host)
+        T = x_host.shape[0]
+        self.workspace(T, B.beam_moe_hostio_extra_bytes(T, self.cfg))
+        B.check(B.beam_moe_forward_hostio(x_host.data_ptr(), self.router_w.data_ptr(),
+                                          self.w_gate.data_ptr(), self.w_up.data_ptr(),
+                                          self.w_down.data_ptr(), T, self.cfg, out_host.data_ptr(),
+                                          _stream_handle(stream)), "beam_moe_forward_hostio")
+        return out_host
+
+    def status(self, stream=None) -> int:
+        return B.beam_moe_read_status(self.cfg, _stream_handle(stream))

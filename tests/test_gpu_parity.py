@@ -1,0 +1,150 @@
+"""GPU parity: the CUDA library against the CPU oracle on the same seeded
+inputs.  Routing (ids, weights, scores, counts, offsets, permuted rows) must
+match bit for bit; the layer output within a per-token relative L2 of 1e-2."""
+import numpy as np
+import pytest
+import torch
+
+from sparse_moe_layer_experts_b300 import synth
+from sparse_moe_layer_experts_b300.layer import BeamMoE
+from tests._gpu_util import REL_L2_TOL, host_inputs, out_bits, rel_l2_per_token, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+# small shapes that still span several tiles, chunks and ragged tails
+SMALL = {
+    "tiny": synth.shape("tiny"),
+    "tiny_T1": synth.shape("tiny", T=1),
+    "tiny_T7": synth.shape("tiny", T=7),
+    "tiny_T200": synth.shape("tiny", T=200),
+    "tiny_T1000": synth.shape("tiny", T=1000),
+    "medium": synth.LayerShape(T=3001, H=512, I=384, E=64, G=8, topk_groups=4, top_k=8),
+    "wide_groups": synth.LayerShape(T=777, H=256, I=256, E=96, G=4, topk_groups=2, top_k=6,
+                                    scale=1.5),
+}
+
+
+def _layer(sh, d, **kw):
+    return BeamMoE(d["router_w"], d["w_gate"], d["w_up"], d["w_down"], n_groups=sh.G,
+                   topk_groups=sh.topk_groups, top_k=sh.top_k, routed_scale=sh.scale, **kw)
+
+
+def _oracle_route(oracle_mod, sh, hx):
+    _, scores = oracle_mod.router_scores(hx["x"], hx["router_w"])
+    ids, w = oracle_mod.select(scores, sh.G, sh.topk_groups, sh.top_k, sh.scale)
+    return scores, ids, w
+
+
+def _check_route(oracle_mod, sh, layer, d, hx):
+    r = layer.route(d["x"])
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    scores, ids, w = _oracle_route(oracle_mod, sh, hx)
+    g_scores = r["scores"].cpu().numpy()
+    n_diff = int((g_scores.view(np.uint32) != scores.view(np.uint32)).sum())
+    assert n_diff == 0, f"{n_diff} scores differ from the oracle's"
+    assert np.array_equal(r["ids"].cpu().numpy(), ids)
+    assert np.array_equal(r["w"].cpu().numpy().view(np.uint32), w.view(np.uint32))
+    counts, offsets, row_of, row_src = oracle_mod.dispatch(ids, sh.E)
+    assert np.array_equal(r["counts"].cpu().numpy(), counts)
+    assert np.array_equal(r["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(r["row_of"].cpu().numpy(), row_of)
+    return ids, w, counts, offsets, row_src
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_route_small_bitexact(oracle_mod, name):
+    sh = SMALL[name]
+    d = synth.make_inputs(sh, seed=0, device="cuda")
+    hx = host_inputs(d)
+    _check_route(oracle_mod, sh, _layer(sh, d), d, hx)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_small_all_tokens(oracle_mod, name):
+    sh = SMALL[name]
+    d = synth.make_inputs(sh, seed=1, device="cuda")
+    hx = host_inputs(d)
+    layer = _layer(sh, d)
+    out = layer.forward(d["x"])
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    ref, _, _ = oracle_mod.forward(hx["x"], hx["router_w"], hx["w_gate"], hx["w_up"],
+                                   hx["w_down"], sh.G, sh.topk_groups, sh.top_k, sh.scale)
+    rel = rel_l2_per_token(out_bits(out), ref)
+    assert rel.max() <= REL_L2_TOL, (rel.max(), int(rel.argmax()))
+
+
+def test_forward_deterministic_and_hostio(oracle_mod):
+    sh = SMALL["medium"]
+    d = synth.make_inputs(sh, seed=2, device="cuda")
+    layer = _layer(sh, d)
+    a = layer.forward(d["x"]).clone()
+    b = layer.forward(d["x"]).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # a second stream, and host buffers through the host-I/O entry point
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c = layer.forward(d["x"], stream=s)
+    s.synchronize()
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+    xh = d["x"].cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    layer.forward_host(xh, oh)
+    assert torch.equal(a.cpu().view(torch.int16), oh.view(torch.int16))
+
+
+def test_timeout_reports_status_and_gpu_recovers(oracle_mod):
+    sh = SMALL["tiny"]
+    d = synth.make_inputs(sh, seed=3, device="cuda")
+    bad = _layer(sh, d, wait_timeout_ns=50_000_000, debug_flags=1)
+    bad.forward(d["x"])
+    torch.cuda.synchronize()
+    assert bad.status() == -5  # BEAM_MOE_ERR_TIMEOUT
+    good = _layer(sh, d)
+    out = good.forward(d["x"])
+    torch.cuda.synchronize()
+    assert good.status() == 0
+    hx = host_inputs(d)
+    ref, _, _ = oracle_mod.forward(hx["x"], hx["router_w"], hx["w_gate"], hx["w_up"],
+                                   hx["w_down"], sh.G, sh.topk_groups, sh.top_k, sh.scale)
+    assert rel_l2_per_token(out_bits(out), ref).max() <= REL_L2_TOL
+
+
+# ------------------------------------------------------------- full sizes
+
+@pytest.fixture(scope="module")
+def beam_weights():
+    sh = synth.shape("decode")
+    w = synth.make_inputs(sh, seed=0, device="cuda", weights=True)
+    yield {k: w[k] for k in ("w_gate", "w_up", "w_down")}
+    del w
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["decode", "prefill", "skewed", "nvfp4"])
+def test_full_size_route_and_sampled_forward(oracle_mod, beam_weights, name):
+    """Full-size workloads in the configuration the benchmark times: every
+    token's routing bit-exact, layer outputs for sampled tokens (first, last,
+    random, and the first/last row of expert segments)."""
+    sh = synth.shape(name)
+    d = synth.make_inputs(sh, seed=0, device="cuda", weights=False)
+    d.update(beam_weights)
+    layer = _layer(sh, d)
+    hx_route = dict(x=synth.to_bits(d["x"]), router_w=synth.to_f32(d["router_w"]))
+    ids, w, counts, offsets, row_src = _check_route(oracle_mod, sh, layer, d, hx_route)
+    out = layer.forward(d["x"])
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    toks = sample_tokens(sh.T, row_src, offsets, n_random=16)
+    hx = host_inputs(d, experts=np.unique(ids[toks]))
+    ref, ref_ids, _ = oracle_mod.forward(hx["x"], hx["router_w"], hx["w_gate"], hx["w_up"],
+                                         hx["w_down"], sh.G, sh.topk_groups, sh.top_k, sh.scale,
+                                         tokens=toks)
+    assert np.array_equal(ref_ids, ids[toks])
+    rel = rel_l2_per_token(out_bits(out)[toks], ref)
+    assert rel.max() <= REL_L2_TOL, (rel.max(), toks[int(rel.argmax())])
+    if name == "skewed":
+        # the synthetic Zipf bias makes one expert hot
+        assert counts.max() > 4 * counts.mean()
