@@ -53,9 +53,19 @@ def parse_args():
                     choices=["tiny", "decode", "prefill", "skewed", "nvfp4"])
     ap.add_argument("--cpu-tokens", type=int, default=16,
                     help="tokens of the batch the CPU oracle baseline computes")
+    ap.add_argument("--override", default="",
+                    help="shape overrides for profiling runs, e.g. T=512,E=32 (not a bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
+
+
+def parse_override(text):
+    out = {}
+    for item in filter(None, text.split(",")):
+        k, v = item.split("=")
+        out[k.strip()] = int(v)
+    return out
 
 
 # ------------------------------------------------------------- distributed
@@ -283,7 +293,7 @@ def run_ours(args, world, rank, local):
     build_mod.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    sh = synth.shape(args.config)
+    sh = synth.shape(args.config, **parse_override(args.override))
     d = synth.make_inputs(sh, seed=0, device=dev, weights=True)
     if rank > 0:  # each replica routes its own batch
         d["x"] = synth.make_inputs(sh, seed=rank, device=dev, weights=False)["x"]
@@ -306,6 +316,10 @@ def run_ours(args, world, rank, local):
     nst = len(B.KERNEL_STAGES)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(nst)] for _ in range(args.steps)]
+    for pair in ev:  # torch creates the CUDA event on its first record
+        for e0, e1 in pair:
+            e0.record(stream)
+            e1.record(stream)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = B.beam_moe_launch_count()
     torch.cuda.synchronize()
@@ -388,7 +402,7 @@ def run_ours(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) activations, N(0,0.02) bf16 weights)",
-            "config": {"workload": f"{args.config}: T={sh.T} tokens, hidden {sh.H}, "
+            "config": {"workload": f"{args.config}{'(' + args.override + ')' if args.override else ''}: T={sh.T} tokens, hidden {sh.H}, "
                                    f"intermediate {sh.I}, {sh.E} experts in {sh.G} groups, "
                                    f"top-{sh.topk_groups} groups, top-{sh.top_k}",
                        "tokens_per_step_per_gpu": sh.T, "active_experts": n_active,

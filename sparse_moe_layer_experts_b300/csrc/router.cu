@@ -19,98 +19,222 @@ namespace beam {
 
 namespace {
 
-// Register-tiled FP32 GEMM with a fixed per-output accumulation order:
-// every accumulator walks h = 0..H-1 in order, so the result does not depend
-// on the tiling.  CTA tile TM tokens x TE experts, thread tile RT x RE,
-// K chunk KC staged in shared memory.
-template <int TM, int TE, int RT, int RE, int KC>
-__global__ void __launch_bounds__(256)
-router_scores_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H,
-                     int E, float *__restrict__ scores, int *status)
+__device__ __forceinline__ float router_sigmoid(float l)
 {
-    // first kernel of every call: reset the call's device status word
+    const float ex = static_cast<float>(exp(-static_cast<double>(l)));
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, ex));
+}
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, bool valid)
+{
+    const uint32_t d = smem_u32(smem_dst);
+    const int n = valid ? 16 : 0;  // 0 source bytes: the 16 bytes are zero-filled
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gsrc), "r"(n)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Large batches: register-tiled FP32 GEMM, 16x16 threads, R x R outputs per
+// thread (CTA tile 16R tokens x 16R experts), K chunks of 16 double-buffered
+// in shared memory with the next chunk prefetched into registers.  Every
+// accumulator walks h = 0..H-1 in order, so the tiling does not change any
+// result.
+constexpr int kLKC = 16;
+
+template <int R>
+__global__ void __launch_bounds__(256, 2)
+router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H,
+                    int E, float *__restrict__ scores, int *status)
+{
+    constexpr int TM = 16 * R, TE = 16 * R, HALF = TM / 2, Q = R / 2;
+    static_assert(R == 4 || R == 8, "thread tile");
     if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
         *status = 0;
-    constexpr int NTX = TE / RE;
-    constexpr int NTY = TM / RT;
-    static_assert(NTX * NTY == 256, "256 threads");
-    static_assert(KC % 8 == 0 && TE % 4 == 0 && RE % 4 == 0, "vector widths");
-    __shared__ __align__(16) float xs[KC][TM + 4];
-    __shared__ __align__(16) float ws[KC][TE];
-
+    __shared__ __align__(16) float xs[2][kLKC][TM + 4];
+    __shared__ __align__(16) float ws[2][kLKC][TE];
     const int tid = threadIdx.x;
-    const int tx = tid % NTX, ty = tid / NTX;
+    const int tx = tid & 15, ty = tid >> 4;
     const int t0 = blockIdx.x * TM, e0 = blockIdx.y * TE;
 
-    float acc[RT][RE];
+    // loaders: x: TM rows x 16 bf16 (TM*2 16-byte vectors); w: 16 rows x TE fp32
+    constexpr int XV = TM * 2;          // x vectors per chunk
+    constexpr int WV = kLKC * TE / 4;   // w float4 per chunk
+    constexpr int XPT = XV / 256 > 0 ? XV / 256 : 1;
+    constexpr int WPT = WV / 256;
+    static_assert(WV % 256 == 0, "w loader");
+    uint4 xq[XPT];
+    float4 wq[WPT];
+    auto gload = [&](int k0) {
 #pragma unroll
-    for (int i = 0; i < RT; ++i)
+        for (int v = 0; v < XPT; ++v) {
+            const int c = tid + v * 256;
+            const int r = c >> 1, col = (c & 1) * 8;
+            const bool ok = c < XV && t0 + r < T;
+            xq[v] = ok ? *reinterpret_cast<const uint4 *>(x + (size_t)(t0 + r) * H + k0 + col)
+                       : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int j = 0; j < RE; ++j)
+        for (int v = 0; v < WPT; ++v) {
+            const int c = tid + v * 256;
+            const int r = c / (TE / 4), col = (c % (TE / 4)) * 4;
+            wq[v] = (e0 + col < E)
+                        ? *reinterpret_cast<const float4 *>(wr + (size_t)(k0 + r) * E + e0 + col)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    auto sstore = [&](int b) {
+#pragma unroll
+        for (int v = 0; v < XPT; ++v) {
+            const int c = tid + v * 256;
+            if (c < XV) {
+                const int r = c >> 1, col = (c & 1) * 8;
+                const uint32_t q[4] = {xq[v].x, xq[v].y, xq[v].z, xq[v].w};
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    xs[b][col + 2 * p][r] = bf16_bits_to_f32(q[p] & 0xFFFFu);
+                    xs[b][col + 2 * p + 1][r] = bf16_bits_to_f32(q[p] >> 16);
+                }
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < WPT; ++v) {
+            const int c = tid + v * 256;
+            const int r = c / (TE / 4), col = (c % (TE / 4)) * 4;
+            *reinterpret_cast<float4 *>(&ws[b][r][col]) = wq[v];
+        }
+    };
+
+    float acc[R][R];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int j = 0; j < R; ++j)
             acc[i][j] = 0.0f;
 
-    for (int k0 = 0; k0 < H; k0 += KC) {
-        // x chunk: TM rows x KC bf16, 8 per 16-byte vector, stored transposed
-        for (int v = tid; v < TM * (KC / 8); v += 256) {
-            const int r = v / (KC / 8), c8 = (v % (KC / 8)) * 8;
-            const int t = t0 + r;
-            uint4 q = make_uint4(0, 0, 0, 0);
-            if (t < T)
-                q = *reinterpret_cast<const uint4 *>(x + (size_t)t * H + k0 + c8);
-            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+    const int nk = H / kLKC;
+    gload(0);
+    sstore(0);
+    __syncthreads();
+    for (int kc = 0; kc < nk; ++kc) {
+        const int b = kc & 1;
+        if (kc + 1 < nk)
+            gload((kc + 1) * kLKC);
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                xs[c8 + 2 * p][r] = bf16_bits_to_f32(w4[p] & 0xFFFFu);
-                xs[c8 + 2 * p + 1][r] = bf16_bits_to_f32(w4[p] >> 16);
-            }
-        }
-        // router weight chunk: KC rows x TE fp32
-        for (int v = tid; v < KC * (TE / 4); v += 256) {
-            const int r = v / (TE / 4), c4 = (v % (TE / 4)) * 4;
-            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e0 + c4 < E)
-                q = *reinterpret_cast<const float4 *>(wr + (size_t)(k0 + r) * E + e0 + c4);
-            *reinterpret_cast<float4 *>(&ws[r][c4]) = q;
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (int k = 0; k < KC; ++k) {
-            float a[RT], b[RE];
+        for (int k = 0; k < kLKC; ++k) {
+            float a[R], bb[R];
 #pragma unroll
-            for (int i = 0; i < RT; ++i)
-                a[i] = xs[k][ty * RT + i];
-#pragma unroll
-            for (int j = 0; j < RE; j += 4) {
-                const float4 q = *reinterpret_cast<const float4 *>(&ws[k][tx * RE + j]);
-                b[j] = q.x;
-                b[j + 1] = q.y;
-                b[j + 2] = q.z;
-                b[j + 3] = q.w;
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const float *ap = &xs[b][k][h2 * HALF + ty * Q];
+                const float *bp = &ws[b][k][h2 * HALF + tx * Q];
+                if constexpr (Q == 4) {
+                    const float4 av = *reinterpret_cast<const float4 *>(ap);
+                    const float4 bv = *reinterpret_cast<const float4 *>(bp);
+                    a[h2 * 4] = av.x;
+                    a[h2 * 4 + 1] = av.y;
+                    a[h2 * 4 + 2] = av.z;
+                    a[h2 * 4 + 3] = av.w;
+                    bb[h2 * 4] = bv.x;
+                    bb[h2 * 4 + 1] = bv.y;
+                    bb[h2 * 4 + 2] = bv.z;
+                    bb[h2 * 4 + 3] = bv.w;
+                } else {
+                    const float2 av = *reinterpret_cast<const float2 *>(ap);
+                    const float2 bv = *reinterpret_cast<const float2 *>(bp);
+                    a[h2 * 2] = av.x;
+                    a[h2 * 2 + 1] = av.y;
+                    bb[h2 * 2] = bv.x;
+                    bb[h2 * 2 + 1] = bv.y;
+                }
             }
 #pragma unroll
-            for (int i = 0; i < RT; ++i)
+            for (int i = 0; i < R; ++i)
 #pragma unroll
-                for (int j = 0; j < RE; ++j)
-                    acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < R; ++j)
+                    acc[i][j] = __fmaf_rn(a[i], bb[j], acc[i][j]);
         }
+        if (kc + 1 < nk)
+            sstore(b ^ 1);
         __syncthreads();
     }
 
+    // thread (ty, tx) owns tokens {h*HALF + ty*Q + i} x experts {h*HALF + tx*Q + j}
 #pragma unroll
-    for (int i = 0; i < RT; ++i) {
-        const int t = t0 + ty * RT + i;
+    for (int i = 0; i < R; ++i) {
+        const int t = t0 + (i / Q) * HALF + ty * Q + (i % Q);
         if (t >= T)
             continue;
 #pragma unroll
-        for (int j = 0; j < RE; ++j) {
-            const int e = e0 + tx * RE + j;
-            if (e >= E)
-                continue;
-            const float ex = static_cast<float>(exp(-static_cast<double>(acc[i][j])));
-            const float den = __fadd_rn(1.0f, ex);
-            scores[(size_t)t * E + e] = __fdiv_rn(1.0f, den);
+        for (int j = 0; j < R; ++j) {
+            const int e = e0 + (j / Q) * HALF + tx * Q + (j % Q);
+            if (e < E)
+                scores[(size_t)t * E + e] = router_sigmoid(acc[i][j]);
         }
     }
+}
+
+// Small batches (decode): the FMA chain of each output is the critical
+// path, so one thread owns one output and the CTAs spread over the experts.
+// CTA = 32 tokens x 4 experts (128 threads); K chunks of 64 flow through a
+// 4-stage cp.async ring.
+constexpr int kSTM = 32, kSTE = 4, kSKC = 64, kSNS = 4, kSXP = kSKC + 8;
+
+__global__ void __launch_bounds__(128)
+router_scores_small(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H,
+                    int E, float *__restrict__ scores, int *status)
+{
+    if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        *status = 0;
+    __shared__ __align__(16) uint16_t xs[kSNS][kSTM][kSXP];
+    __shared__ __align__(16) float ws[kSNS][kSKC][kSTE];
+    const int tid = threadIdx.x;
+    const int te = tid & 3, tt = tid >> 2;
+    const int t0 = blockIdx.x * kSTM, e0 = blockIdx.y * kSTE;
+    const int nk = H / kSKC;
+
+    auto load = [&](int st, int k0) {
+        // x: 32 rows x 8 chunks of 16 B; w: 64 rows x one 16-B chunk
+        for (int c = tid; c < kSTM * (kSKC / 8); c += 128) {
+            const int r = c >> 3, q = c & 7;
+            const bool ok = t0 + r < T;
+            cp_async16(&xs[st][r][q * 8], x + (size_t)(ok ? t0 + r : 0) * H + k0 + q * 8, ok);
+        }
+        if (tid < kSKC) {
+            const bool ok = e0 < E;
+            cp_async16(&ws[st][tid][0], wr + (size_t)(k0 + tid) * E + (ok ? e0 : 0), ok);
+        }
+    };
+
+#pragma unroll
+    for (int s = 0; s < kSNS - 1; ++s) {
+        if (s < nk)
+            load(s, s * kSKC);
+        cp_async_commit();
+    }
+    float acc = 0.0f;
+    for (int kc = 0; kc < nk; ++kc) {
+        cp_async_wait<kSNS - 2>();
+        __syncthreads();
+        if (kc + kSNS - 1 < nk)
+            load((kc + kSNS - 1) % kSNS, (kc + kSNS - 1) * kSKC);
+        cp_async_commit();
+        const int st = kc % kSNS;
+#pragma unroll 16
+        for (int k = 0; k < kSKC; ++k)
+            acc = __fmaf_rn(bf16_bits_to_f32(xs[st][tt][k]), ws[st][k][te], acc);
+    }
+    const int t = t0 + tt, e = e0 + te;
+    if (t < T && e < E)
+        scores[(size_t)t * E + e] = router_sigmoid(acc);
 }
 
 // One warp per token.  Lane l holds the scores of experts l, l+32, ...
@@ -214,14 +338,15 @@ cudaError_t launch_router_scores(const uint16_t *x, const float *wr, int T, int 
                                  float *scores, int *status, cudaStream_t s)
 {
     stage_begin(kStRouter, s);
-    if (T >= 512) {
-        constexpr int TM = 64, TE = 128;
-        dim3 grid((T + TM - 1) / TM, (E + TE - 1) / TE);
-        router_scores_kernel<TM, TE, 4, 8, 32><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
+    if (T >= 8192) {
+        dim3 grid((T + 127) / 128, (E + 127) / 128);
+        router_scores_large<8><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
+    } else if (T >= 128) {
+        dim3 grid((T + 63) / 64, (E + 63) / 64);
+        router_scores_large<4><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
     } else {
-        constexpr int TM = 16, TE = 64;
-        dim3 grid((T + TM - 1) / TM, (E + TE - 1) / TE);
-        router_scores_kernel<TM, TE, 1, 4, 32><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
+        dim3 grid((T + kSTM - 1) / kSTM, (E + kSTE - 1) / kSTE);
+        router_scores_small<<<grid, 128, 0, s>>>(x, wr, T, H, E, scores, status);
     }
     stage_end(kStRouter, s);
     return cudaGetLastError();
