@@ -166,6 +166,39 @@ int beam_moe_forward_hostio(const void *x_host, const float *router_w,
 size_t beam_moe_hostio_extra_bytes(int64_t T, const beam_moe_cfg *cfg);
 
 /*
+ * beam_moe_forward for callers that cannot allocate device memory.  The
+ * pages have no counterpart: this is a library convenience, not part of the
+ * method.
+ *
+ * Who needs it: callers whose device memory is owned by someone else and who
+ * cannot call cudaMalloc (a host application that forbids allocations after
+ * start-up, a fixed inference arena, a plug-in without access to the
+ * process's allocator).  They pass inputs and outputs only; the scratch
+ * lives in a 24 MiB array compiled into the library, and this call makes no
+ * allocation of any kind.
+ *
+ * Arguments are those of beam_moe_forward; cfg->workspace and
+ * cfg->workspace_bytes are ignored.
+ *  - Limit: beam_moe_workspace_size(T, cfg) must not exceed 24 MiB (at the
+ *    Beam sizes: T <= 87 tokens); larger calls return BEAM_MOE_ERR_WORKSPACE
+ *    with nothing enqueued.  Invalid configurations return
+ *    BEAM_MOE_ERR_INVALID_ARG; T = 0 returns BEAM_MOE_OK.
+ *  - Memory: every GPU on which this entry point runs keeps the 24 MiB array
+ *    until the process exits.
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress) with that device current; make that
+ *    first call before any stream capture.
+ *  - Sharing: all calls share the one array and each call overwrites it, so
+ *    calls that overlap on the GPU race; serialise them.  The device status
+ *    word lives in the shared array and is not readable through
+ *    beam_moe_read_status.
+ */
+int beam_moe_forward_noalloc(const void *x, const float *router_w,
+                             const void *w_gate, const void *w_up,
+                             const void *w_down, int64_t T,
+                             const beam_moe_cfg *cfg, void *out, void *stream);
+
+/*
  * NVFP4 weight quantisation (E2M1 values, one E4M3 scale per 16 consecutive
  * elements of a row, one FP32 global scale per matrix).
  *   w        [n_mat, rows, cols] bf16, device; cols % 16 == 0

@@ -171,3 +171,14 @@ def make_cfg(H, I, E, G, topk_groups, top_k, scale=2.5, wtype=BEAM_MOE_W_BF16) -
     c.hidden, c.inter, c.n_experts, c.n_groups = H, I, E, G
     c.topk_groups, c.top_k, c.routed_scale, c.wtype = topk_groups, top_k, scale, wtype
     return c
+
+
+def beam_moe_forward_noalloc(x, router_w, w_gate, w_up, w_down, T, cfg, out, stream) -> int:
+    """The layer forward with the library's built-in scratch (no workspace,
+    no allocation); for callers that cannot allocate device memory."""
+    f = lib().beam_moe_forward_noalloc
+    if f.argtypes is None:
+        vp = ctypes.c_void_p
+        f.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int64, ctypes.POINTER(beam_moe_cfg), vp, vp]
+        f.restype = ctypes.c_int
+    return f(x, router_w, w_gate, w_up, w_down, T, ctypes.byref(cfg), out, stream)
