@@ -156,26 +156,39 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def kernel_source_sha():
+KERNEL_SOURCES = {
+    "router_scores": ("router.cu", "common.cuh"),
+    "select": ("router.cu", "common.cuh"),
+    "hist": ("dispatch.cu", "common.cuh"),
+    "scan": ("dispatch.cu", "common.cuh"),
+    "permute": ("dispatch.cu", "common.cuh"),
+    "combine": ("dispatch.cu", "common.cuh"),
+    "gateup_gemm": ("grouped_gemm.cu", "common.cuh"),
+    "down_gemm": ("grouped_gemm.cu", "common.cuh"),
+}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    """Hash of the source files a kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_moe_layer_experts_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    """DRAM bytes per launch from the committed ncu summary
+    (profiles/dram_traffic.json), if it was taken on the kernel's current
+    sources; else None."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_sha") != kernel_source_sha():
+    if not e or e.get("source_sha") != kernel_source_sha(kernel):
         return None
     return e.get("bytes_per_launch")
 
