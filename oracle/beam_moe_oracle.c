@@ -39,6 +39,18 @@
  *  - permuted order: rows grouped by expert (ascending), tokens ascending
  *    inside an expert.
  *
+ * NVFP4 variant (the pages: "most parameters in 4 bits, some kept in BF16",
+ * [P1-HW] = "Reflection Beam 1.0", section "Hardware requirements: NVFP4 is
+ * the most practical serving path", and [P5-MoE]; they give no recipe, so the
+ * whole recipe is a reading): E2M1 values with one E4M3 scale per 16
+ * consecutive elements of a row and one FP32 scale per matrix,
+ *   gs = amax|W| / (6*448)                     (1 if the matrix is all zero)
+ *   sf = e4m3( (amax16 / 6) / gs )             round to nearest even, saturate
+ *   q  = e2m1( v / (sf*gs) )                   0 when sf == 0
+ *   dequantised value = q * sf * gs.
+ * Activations (x before the gate/up GEMM, h before the down GEMM) use the
+ * same block recipe with gs = 1.  The router stays FP32 on the bf16 x.
+ *
  * Everything here is written for clarity, not speed: no blocking, no fusion.
  */
 #include <math.h>
@@ -340,6 +352,217 @@ int oracle_forward(const uint16_t *x, const float *wr, const uint16_t *wg,
         free(w);
         free(hbuf);
         free(y);
+        free(acc);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ NVFP4 */
+
+/* magnitudes of the E2M1 codes 0..7 (bit 3 is the sign) */
+static const float kE2M1[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+
+float oracle_e2m1_value(int code)
+{
+    const float m = kE2M1[code & 7];
+    return (code & 8) ? -m : m;
+}
+
+/* Nearest E2M1 code; a tie goes to the code whose mantissa bit (bit 0) is 0;
+   magnitudes beyond 6 take 6; the sign is kept (so -0.1 gives -0). */
+int oracle_e2m1_code(float v)
+{
+    const double a = fabs((double)v);
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c < 8; ++c) {
+        const double d = fabs(a - (double)kE2M1[c]);
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            bd = d;
+            best = c;
+        }
+    }
+    return best | (signbit(v) ? 8 : 0);
+}
+
+/* value of an E4M3 code (4 exponent bits, bias 7, 3 mantissa bits; no
+   infinities; 0x7F / 0xFF are NaN and never produced here) */
+float oracle_e4m3_value(int code)
+{
+    const int e = (code >> 3) & 15, m = code & 7;
+    const float mag = (e == 0) ? ldexpf((float)m, -9) : ldexpf(1.0f + (float)m / 8.0f, e - 7);
+    return (code & 0x80) ? -mag : mag;
+}
+
+/* Nearest non-negative finite E4M3 code for v >= 0 (ties to an even
+   mantissa; values beyond 448 take 448). */
+int oracle_e4m3_code(float v)
+{
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double d = fabs((double)v - (double)oracle_e4m3_value(c));
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            bd = d;
+            best = c;
+        }
+    }
+    return best;
+}
+
+/* Quantise one row of n (multiple of 16) floats with global scale g:
+   codes[n] (one E2M1 code per byte), sf[n/16] (E4M3 codes). */
+static void quantize_row(const float *v, int64_t n, float g, uint8_t *codes, uint8_t *sf)
+{
+    for (int64_t b = 0; b < n / 16; ++b) {
+        const float *blk = v + b * 16;
+        float bmax = 0.0f;
+        for (int i = 0; i < 16; ++i)
+            if (fabsf(blk[i]) > bmax)
+                bmax = fabsf(blk[i]);
+        const float want = (bmax / 6.0f) / g;
+        const int sc = oracle_e4m3_code(want);
+        sf[b] = (uint8_t)sc;
+        const float sfv = oracle_e4m3_value(sc);
+        const float den = sfv * g;
+        for (int i = 0; i < 16; ++i)
+            codes[b * 16 + i] = (sfv == 0.0f) ? 0 : (uint8_t)oracle_e2m1_code(blk[i] / den);
+    }
+}
+
+/*
+ * NVFP4 quantisation of n_mat bf16 matrices [rows, cols] (cols % 16 == 0):
+ *   codes [n_mat, rows, cols] one E2M1 code per byte
+ *   sf    [n_mat, rows, cols/16] E4M3 codes
+ *   gs    [n_mat] FP32 global scales
+ */
+int oracle_quantize_nvfp4(const uint16_t *w, int64_t n_mat, int64_t rows, int64_t cols,
+                          uint8_t *codes, uint8_t *sf, float *gs)
+{
+    if (cols % 16 != 0)
+        return -1;
+    for (int64_t mat = 0; mat < n_mat; ++mat) {
+        const uint16_t *wm = w + mat * rows * cols;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < rows * cols; ++i) {
+            const float a = fabsf(bf16_bits_to_float(wm[i]));
+            if (a > amax)
+                amax = a;
+        }
+        const float g = (amax > 0.0f) ? amax / (6.0f * 448.0f) : 1.0f;
+        gs[mat] = g;
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < rows; ++r) {
+            float *row = (float *)malloc(sizeof(float) * (size_t)cols);
+            for (int64_t c = 0; c < cols; ++c)
+                row[c] = bf16_bits_to_float(wm[r * cols + c]);
+            quantize_row(row, cols, g, codes + (mat * rows + r) * cols,
+                         sf + (mat * rows + r) * (cols / 16));
+            free(row);
+        }
+    }
+    return 0;
+}
+
+/* Quantise-then-dequantise a row in place with global scale 1 (activations). */
+static void fake_quant_row(float *v, int64_t n)
+{
+    uint8_t *codes = (uint8_t *)malloc((size_t)n);
+    uint8_t *sf = (uint8_t *)malloc((size_t)(n / 16));
+    quantize_row(v, n, 1.0f, codes, sf);
+    for (int64_t i = 0; i < n; ++i)
+        v[i] = oracle_e2m1_value(codes[i]) * oracle_e4m3_value(sf[i / 16]);
+    free(codes);
+    free(sf);
+}
+
+/* exported for the pins: quantise-dequantise rows [n_rows, n] with gs = 1 */
+void oracle_fake_quant_rows(float *v, int64_t n_rows, int64_t n)
+{
+    for (int64_t r = 0; r < n_rows; ++r)
+        fake_quant_row(v + r * n, n);
+}
+
+static double deq(const uint8_t *codes, const uint8_t *sf, float g, int64_t row, int64_t cols,
+                  int64_t c)
+{
+    return (double)oracle_e2m1_value(codes[row * cols + c]) *
+           (double)oracle_e4m3_value(sf[row * (cols / 16) + c / 16]) * (double)g;
+}
+
+/*
+ * The layer with NVFP4 experts and NVFP4 activations (see the header note):
+ * router and selection exactly as oracle_forward; per selected expert,
+ *   g, u = xq . deq(Wg)^T, xq . deq(Wu)^T   (FP64 sums, rounded to FP32)
+ *   h    = fakequant( silu(g) * u )          (FP32 product, then gs = 1 blocks)
+ *   y    = h . deq(Wd)^T                     (FP64)
+ * where xq = fakequant(x).  Weight arrays are the outputs of
+ * oracle_quantize_nvfp4: codes [E,I,H] / [E,H,I], sf [.., /16], gs [E].
+ */
+int oracle_forward_nvfp4(const uint16_t *x, const float *wr, const uint8_t *gc, const uint8_t *gsf,
+                         const float *ggs, const uint8_t *uc, const uint8_t *usf,
+                         const float *ugs, const uint8_t *dc, const uint8_t *dsf,
+                         const float *dgs, int64_t T, int H, int I, int E, int G,
+                         int topk_groups, int top_k, float scale, const int64_t *tokens,
+                         int64_t n_tokens, uint16_t *out, int32_t *ids_out, float *w_out)
+{
+    if (E % G != 0 || top_k > topk_groups * (E / G) || H % 16 || I % 16)
+        return -1;
+    const int64_t n = tokens ? n_tokens : T;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t t = tokens ? tokens[r] : r;
+        if (t < 0 || t >= T) {
+            bad = 1;
+            continue;
+        }
+        const uint16_t *xrow = x + t * H;
+        float *scores = (float *)malloc(sizeof(float) * (size_t)E);
+        int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)top_k);
+        float *w = (float *)malloc(sizeof(float) * (size_t)top_k);
+        float *xq = (float *)malloc(sizeof(float) * (size_t)H);
+        float *hq = (float *)malloc(sizeof(float) * (size_t)I);
+        double *acc = (double *)calloc((size_t)H, sizeof(double));
+
+        oracle_router_scores(xrow, wr, 1, H, E, NULL, scores);
+        if (oracle_select(scores, 1, E, G, topk_groups, top_k, scale, ids, w) != 0)
+            bad = 1;
+        for (int h = 0; h < H; ++h)
+            xq[h] = bf16_bits_to_float(xrow[h]);
+        fake_quant_row(xq, H);
+        for (int k = 0; k < top_k && !bad; ++k) {
+            const int64_t e = ids[k];
+            for (int i = 0; i < I; ++i) {
+                double gd = 0.0, ud = 0.0;
+                const int64_t row = e * I + i;
+                for (int h = 0; h < H; ++h) {
+                    gd += (double)xq[h] * deq(gc, gsf, ggs[e], row, H, h);
+                    ud += (double)xq[h] * deq(uc, usf, ugs[e], row, H, h);
+                }
+                const float g = (float)gd, u = (float)ud;
+                hq[i] = (g * sigmoid_f32(g)) * u;
+            }
+            fake_quant_row(hq, I);
+            for (int j = 0; j < H; ++j) {
+                double yd = 0.0;
+                const int64_t row = e * H + j;
+                for (int i = 0; i < I; ++i)
+                    yd += (double)hq[i] * deq(dc, dsf, dgs[e], row, I, i);
+                acc[j] += (double)w[k] * yd;
+            }
+        }
+        for (int j = 0; j < H; ++j)
+            out[r * H + j] = float_to_bf16_bits_rne((float)acc[j]);
+        if (ids_out)
+            memcpy(ids_out + r * top_k, ids, sizeof(int32_t) * (size_t)top_k);
+        if (w_out)
+            memcpy(w_out + r * top_k, w, sizeof(float) * (size_t)top_k);
+        free(scores);
+        free(ids);
+        free(w);
+        free(xq);
+        free(hq);
         free(acc);
     }
     return bad ? -1 : 0;

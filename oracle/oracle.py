@@ -58,6 +58,21 @@ def lib():
         L.oracle_forward.argtypes = [p, p, p, p, p, i64, i32, i32, i32, i32, i32, i32,
                                      f32, p, i64, p, p, p]
         L.oracle_forward.restype = i32
+        L.oracle_e2m1_value.argtypes = [i32]
+        L.oracle_e2m1_value.restype = f32
+        L.oracle_e2m1_code.argtypes = [f32]
+        L.oracle_e2m1_code.restype = i32
+        L.oracle_e4m3_value.argtypes = [i32]
+        L.oracle_e4m3_value.restype = f32
+        L.oracle_e4m3_code.argtypes = [f32]
+        L.oracle_e4m3_code.restype = i32
+        L.oracle_quantize_nvfp4.argtypes = [p, i64, i64, i64, p, p, p]
+        L.oracle_quantize_nvfp4.restype = i32
+        L.oracle_fake_quant_rows.argtypes = [p, i64, i64]
+        L.oracle_fake_quant_rows.restype = None
+        L.oracle_forward_nvfp4.argtypes = [p, p, p, p, p, p, p, p, p, p, p, i64, i32, i32, i32, i32,
+                                           i32, i32, f32, p, i64, p, p, p]
+        L.oracle_forward_nvfp4.restype = i32
         _lib = L
     return _lib
 
@@ -161,3 +176,75 @@ def forward(x_bits, router_w, wg_bits, wu_bits, wd_bits, n_groups, topk_groups, 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------------- NVFP4
+
+def e2m1_value(code: int) -> float:
+    return float(lib().oracle_e2m1_value(int(code)))
+
+
+def e2m1_code(v: float) -> int:
+    return int(lib().oracle_e2m1_code(float(v)))
+
+
+def e4m3_value(code: int) -> float:
+    return float(lib().oracle_e4m3_value(int(code)))
+
+
+def e4m3_code(v: float) -> int:
+    return int(lib().oracle_e4m3_code(float(v)))
+
+
+def quantize_nvfp4(w_bits: np.ndarray):
+    """bf16 bits [n_mat, rows, cols] -> (codes [n_mat,rows,cols] u8 one per byte,
+    sf [n_mat,rows,cols/16] u8 E4M3, gs [n_mat] f32)."""
+    w_bits = _c(w_bits, np.uint16)
+    n_mat, rows, cols = w_bits.shape
+    codes = np.empty((n_mat, rows, cols), np.uint8)
+    sf = np.empty((n_mat, rows, cols // 16), np.uint8)
+    gs = np.empty(n_mat, np.float32)
+    if lib().oracle_quantize_nvfp4(_ptr(w_bits), n_mat, rows, cols, _ptr(codes), _ptr(sf),
+                                   _ptr(gs)) != 0:
+        raise ValueError("cols must be a multiple of 16")
+    return codes, sf, gs
+
+
+def fake_quant_rows(v: np.ndarray) -> np.ndarray:
+    """Quantise-dequantise fp32 rows [n, k] with global scale 1 (activations)."""
+    v = np.array(v, np.float32, copy=True, order="C")
+    lib().oracle_fake_quant_rows(_ptr(v), v.shape[0], v.shape[1])
+    return v
+
+
+def dequantize_nvfp4(codes, sf, gs) -> np.ndarray:
+    """float64 values q * sf * gs of oracle-layout NVFP4 tensors."""
+    e2 = np.array([e2m1_value(c) for c in range(16)], np.float64)
+    e4 = np.array([e4m3_value(c) for c in range(256)], np.float64)
+    v = e2[codes] * np.repeat(e4[sf], 16, axis=-1)
+    return v * np.asarray(gs, np.float64).reshape((-1,) + (1,) * (codes.ndim - 1))
+
+
+def forward_nvfp4(x_bits, router_w, q_gate, q_up, q_down, n_groups, topk_groups, top_k,
+                  scale, tokens=None):
+    """NVFP4 layer for `tokens`; q_* = (codes, sf, gs) from quantize_nvfp4."""
+    x_bits = _c(x_bits, np.uint16)
+    router_w = _c(router_w, np.float32)
+    (gc, gsf, ggs), (uc, usf, ugs), (dc, dsf, dgs) = [
+        (_c(c, np.uint8), _c(f, np.uint8), _c(g, np.float32)) for c, f, g in
+        (q_gate, q_up, q_down)]
+    T, H = x_bits.shape
+    E, I, H2 = gc.shape
+    assert H2 == H and dc.shape == (E, H, I)
+    tok = None if tokens is None else _c(np.asarray(tokens, np.int64), np.int64)
+    n = T if tok is None else tok.shape[0]
+    out = np.empty((n, H), np.uint16)
+    ids = np.empty((n, top_k), np.int32)
+    w = np.empty((n, top_k), np.float32)
+    rc = lib().oracle_forward_nvfp4(_ptr(x_bits), _ptr(router_w), _ptr(gc), _ptr(gsf), _ptr(ggs),
+                                    _ptr(uc), _ptr(usf), _ptr(ugs), _ptr(dc), _ptr(dsf),
+                                    _ptr(dgs), T, H, I, E, n_groups, topk_groups, top_k,
+                                    float(scale), _ptr(tok), n, _ptr(out), _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise ValueError("oracle_forward_nvfp4 failed")
+    return out, ids, w
