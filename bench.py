@@ -24,6 +24,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -161,18 +163,20 @@ KERNEL_SOURCES = {
     "select": ("router.cu", "common.cuh"),
     "hist": ("dispatch.cu", "common.cuh"),
     "scan": ("dispatch.cu", "common.cuh"),
-    "permute": ("dispatch.cu", "common.cuh"),
+    "permute": ("dispatch.cu", "common.cuh", "nvfp4.cuh"),
     "combine": ("dispatch.cu", "common.cuh"),
-    "gateup_gemm": ("grouped_gemm.cu", "common.cuh"),
-    "down_gemm": ("grouped_gemm.cu", "common.cuh"),
+    "gateup_gemm": ("grouped_gemm.cu", "gemm_common.cuh", "common.cuh"),
+    "down_gemm": ("grouped_gemm.cu", "gemm_common.cuh", "common.cuh"),
 }
+FP4_GEMM_SOURCES = ("grouped_gemm_fp4.cu", "gemm_common.cuh", "common.cuh", "nvfp4.cuh")
 
 
-def kernel_source_sha(kernel: str) -> str:
+def kernel_source_sha(kernel: str, nvfp4: bool = False) -> str:
     """Hash of the source files a kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_moe_layer_experts_b300", "csrc")
-    for name in KERNEL_SOURCES[kernel]:
+    files = FP4_GEMM_SOURCES if (nvfp4 and kernel.endswith("_gemm")) else KERNEL_SOURCES[kernel]
+    for name in files:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -188,19 +192,20 @@ def ncu_traffic(kernel: str, workload: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_sha") != kernel_source_sha(kernel):
+    if not e or e.get("source_sha") != kernel_source_sha(kernel, workload == "nvfp4"):
         return None
     return e.get("bytes_per_launch")
 
 
-def workload_algorithmic(sh, n_active: int):
+def workload_algorithmic(sh, n_active: int, nvfp4: bool = False):
     """Algorithmic bytes / FLOPs per launch of each kernel (compulsory traffic
     of the kernel's own inputs and outputs; expert weights of active experts
-    only)."""
+    only).  NVFP4 weights: 0.5 B per code + 1/16 B of block scale."""
     T, H, I, E, K = sh.T, sh.H, sh.I, sh.E, sh.top_k
     R = T * K
-    w_gu = n_active * 2 * I * H * 2
-    w_d = n_active * H * I * 2
+    wb = 0.5625 if nvfp4 else 2
+    w_gu = int(n_active * 2 * I * H * wb)
+    w_d = int(n_active * H * I * wb)
     return {
         "router_scores": dict(bytes=T * H * 2 + H * E * 4 + T * E * 4, flops=2 * T * H * E),
         "select": dict(bytes=T * E * 4 + R * 8, flops=0),
@@ -227,7 +232,7 @@ def host_sample(sh, d, toks):
     rw = synth.to_f32(d["router_w"])
     _, s = oracle.router_scores(xh[toks], rw)
     ids, _ = oracle.select(s, sh.G, sh.topk_groups, sh.top_k, sh.scale)
-    host = dict(x=xh, router_w=rw)
+    host = dict(x=xh, router_w=rw, experts=sorted(set(ids.reshape(-1).tolist())))
     for k in ("w_gate", "w_up", "w_down"):
         a = np.zeros(tuple(d[k].shape), np.uint16)
         for e in sorted(set(ids.reshape(-1).tolist())):
@@ -236,22 +241,37 @@ def host_sample(sh, d, toks):
     return host
 
 
-def oracle_step(sh, host, toks):
+def oracle_step(sh, host, toks, nvfp4=False):
     from oracle import oracle
     t0 = time.perf_counter()
-    oracle.forward(host["x"], host["router_w"], host["w_gate"], host["w_up"], host["w_down"],
-                   sh.G, sh.topk_groups, sh.top_k, sh.scale, tokens=toks)
+    if nvfp4:
+        # the oracle quantises the experts the sample uses, then runs the layer
+        q = []
+        for k in ("w_gate", "w_up", "w_down"):
+            w = host[k]
+            codes = np.zeros(w.shape, np.uint8)
+            sf = np.zeros(w.shape[:-1] + (w.shape[-1] // 16,), np.uint8)
+            gs = np.ones(w.shape[0], np.float32)
+            for e in host["experts"]:
+                c1, s1, g1 = oracle.quantize_nvfp4(w[e:e + 1])
+                codes[e], sf[e], gs[e] = c1[0], s1[0], g1[0]
+            q.append((codes, sf, gs))
+        oracle.forward_nvfp4(host["x"], host["router_w"], *q, sh.G, sh.topk_groups, sh.top_k,
+                             sh.scale, tokens=toks)
+    else:
+        oracle.forward(host["x"], host["router_w"], host["w_gate"], host["w_up"],
+                       host["w_down"], sh.G, sh.topk_groups, sh.top_k, sh.scale, tokens=toks)
     return time.perf_counter() - t0
 
 
-def cpu_oracle_run(sh, d, n_tokens, seed=0):
+def cpu_oracle_run(sh, d, n_tokens, seed=0, nvfp4=False):
     """Time the CPU oracle on `n_tokens` seeded tokens of the batch."""
     import numpy as np
     from oracle import oracle
     rng = np.random.default_rng(seed)
     toks = sorted(rng.choice(sh.T, size=min(n_tokens, sh.T), replace=False).tolist())
     host = host_sample(sh, d, toks)
-    dt = oracle_step(sh, host, toks)
+    dt = oracle_step(sh, host, toks, nvfp4)
     return len(toks) / dt, min(oracle.num_threads(), len(toks)), len(toks), dt
 
 
@@ -274,7 +294,8 @@ def run_reference(args, world, rank):
     toks = sorted(np.random.default_rng(0).choice(sh.T, size=ntok, replace=False).tolist())
     host = host_sample(sh, d, toks)
     del d
-    times = [oracle_step(sh, host, toks) for _ in range(args.warmup + args.steps)]
+    nvfp4 = args.config == "nvfp4"
+    times = [oracle_step(sh, host, toks, nvfp4) for _ in range(args.warmup + args.steps)]
     total = sum(times[args.warmup:])
     value = ntok * args.steps / total
     cores = min(oracle.num_threads(), ntok)
@@ -299,7 +320,7 @@ def run_ours(args, world, rank, local):
     from sparse_moe_layer_experts_b300 import binding as B
     from sparse_moe_layer_experts_b300 import build as build_mod
     from sparse_moe_layer_experts_b300 import synth
-    from sparse_moe_layer_experts_b300.layer import BeamMoE
+    from sparse_moe_layer_experts_b300.layer import BeamMoE, quantize_nvfp4
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
@@ -307,11 +328,17 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sh = synth.shape(args.config, **parse_override(args.override))
+    nvfp4 = args.config == "nvfp4"
     d = synth.make_inputs(sh, seed=0, device=dev, weights=True)
     if rank > 0:  # each replica routes its own batch
         d["x"] = synth.make_inputs(sh, seed=rank, device=dev, weights=False)["x"]
-    layer = BeamMoE(d["router_w"], d["w_gate"], d["w_up"], d["w_down"], n_groups=sh.G,
-                    topk_groups=sh.topk_groups, top_k=sh.top_k, routed_scale=sh.scale)
+    if nvfp4:
+        q = [quantize_nvfp4(d[k]) for k in ("w_gate", "w_up", "w_down")]
+        layer = BeamMoE.nvfp4(d["router_w"], *q, n_groups=sh.G, topk_groups=sh.topk_groups,
+                              top_k=sh.top_k, routed_scale=sh.scale)
+    else:
+        layer = BeamMoE(d["router_w"], d["w_gate"], d["w_up"], d["w_down"], n_groups=sh.G,
+                        topk_groups=sh.topk_groups, top_k=sh.top_k, routed_scale=sh.scale)
     x = d["x"]
     out = torch.empty_like(x)
     r = layer.route(x, want_scores=False)
@@ -374,7 +401,7 @@ def run_ours(args, world, rank, local):
 
     value = world * sh.T * args.steps / (ms_max / 1e3)
     peaks, peak_src = load_peaks()
-    alg = workload_algorithmic(sh, n_active)
+    alg = workload_algorithmic(sh, n_active, nvfp4)
     dom = max(per_kernel_ms, key=per_kernel_ms.get)
     a = alg[dom]
     t_dom = per_kernel_ms[dom] / 1e3
@@ -405,7 +432,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, n, dt = cpu_oracle_run(sh, d, args.cpu_tokens)
+        v, cores, n, dt = cpu_oracle_run(sh, d, args.cpu_tokens, nvfp4=nvfp4)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{n} seeded tokens of the {args.config} batch ({dt:.1f} s)"}
 
@@ -413,7 +440,8 @@ def run_ours(args, world, rank, local):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 weights+activations, f16 MMA, f32 accumulate" if nvfp4 else "bf16",
             "data": "synthetic (seeded N(0,1) activations, N(0,0.02) bf16 weights)",
             "config": {"workload": f"{args.config}{'(' + args.override + ')' if args.override else ''}: T={sh.T} tokens, hidden {sh.H}, "
                                    f"intermediate {sh.I}, {sh.E} experts in {sh.G} groups, "

@@ -141,7 +141,12 @@ int beam_moe_route(const void *x, const float *router_w, int64_t T,
  *   w_down   [E,H,I] bf16, device (per expert: [out=H, in=I])
  *   out      [T,H] bf16, device, written
  * With cfg->wtype == BEAM_MOE_W_NVFP4 the three weight pointers are packed
- * E2M1 codes as produced by beam_moe_quantize_nvfp4.
+ * E2M1 codes as produced by beam_moe_quantize_nvfp4 (w_gate/w_up: n_mat = E,
+ * rows = I, cols = H; w_down: n_mat = E, rows = H, cols = I), and
+ * cfg->w_*_sf / cfg->w_*_gs point at the matching block and global scales
+ * (16-byte aligned).  The activations are then quantised to NVFP4 as well
+ * (16-element blocks, global scale 1): x before the gate/up GEMM, h before
+ * the down GEMM.  The router stays FP32 on the bf16 x.
  * Deterministic: the same inputs give bitwise the same output.
  */
 int beam_moe_forward(const void *x, const float *router_w, const void *w_gate,
@@ -201,14 +206,19 @@ int beam_moe_forward_noalloc(const void *x, const float *router_w,
 /*
  * NVFP4 weight quantisation (E2M1 values, one E4M3 scale per 16 consecutive
  * elements of a row, one FP32 global scale per matrix).
- *   w        [n_mat, rows, cols] bf16, device; cols % 16 == 0
+ *   w        [n_mat, rows, cols] bf16, device; rows % 128 == 0, cols % 64 == 0
  *   packed   [n_mat, rows, cols/2] uint8, device, out (two codes per byte,
- *            element 2j in the low nibble)
- *   block_sf [n_mat, rows, cols/16] uint8, device, out (E4M3 bits)
- *   global_sf[n_mat] fp32, device, out: amax(|w|)/(6*448) per matrix
- * The pages name the format only ("most parameters in 4 bits"); the exact
- * recipe is a reading: sf = e4m3(amax16 / 6 / gs), q = e2m1(v / (sf * gs)),
- * round to nearest even, saturating.
+ *            element 2j in the low nibble, bit 3 of a code = sign)
+ *   block_sf [n_mat, rows/128, cols/64, 128, 4] uint8, device, out (E4M3
+ *            bits): the scale of elements [16b, 16b+16) of row r is entry
+ *            (r % 128, b % 4) of tile (r / 128, b / 4), so the 512 scales of
+ *            one 128 x 64 weight tile are contiguous
+ *   global_sf[n_mat] fp32, device, out
+ * Recipe (the pages name the format only: "most parameters in 4 bits"; the
+ * recipe is a reading): gs = amax|W| / (6*448) per matrix (1 if all zero);
+ * per block sf = e4m3((amax16 / 6) / gs); q = e2m1(v / (sf * gs)), 0 when
+ * sf = 0; round to nearest even, saturating.  Dequantised value: q * sf * gs.
+ * All pointers 16-byte aligned.  Two kernel launches on `stream`.
  */
 int beam_moe_quantize_nvfp4(const void *w, int64_t n_mat, int64_t rows,
                             int64_t cols, void *packed, void *block_sf,

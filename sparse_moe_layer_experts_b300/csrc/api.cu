@@ -136,21 +136,38 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 2-D bf16 tensor [outer, inner] (inner contiguous), box [box_outer, 64],
-// 128-byte swizzle, zero fill outside.
-bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer)
+// 2-D tensor [outer, inner] (inner contiguous), box [box_outer, box_inner],
+// zero fill outside.
+bool make_map_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                 uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swizzle)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {64, box_outer};
+    cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(m, dtype, 2, const_cast<void *>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// 16-bit operand [outer, inner], box [box_outer, 64] with the 128-byte swizzle
+// the MMA descriptors name.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
+{
+    return make_map_2d(m, base, dtype, 2, inner, outer, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Packed E2M1 codes [outer rows, inner/2 bytes], box [128 rows, 32 bytes].
+bool make_code_map(CUtensorMap *m, const void *base, uint64_t inner_elems, uint64_t outer)
+{
+    return make_map_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, inner_elems / 2, outer, 32, 128,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int device_sms()
@@ -208,17 +225,27 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
         return rc;
     const int K = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
     const int64_t R = T * K;
+    const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4;
     BEAM_CUDA(launch_permute(static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids),
                              at<int32_t>(ws, L.local_rank), at<int32_t>(ws, L.cta_base),
                              at<int32_t>(ws, L.offsets), (int)T, K, E, H, at<int32_t>(ws, L.row_of),
-                             at<int32_t>(ws, L.row_src), at<uint16_t>(ws, L.x_perm), s));
+                             at<int32_t>(ws, L.row_src), at<uint16_t>(ws, L.x_perm), fp4, s));
 
+    // activations: bf16, or the exact FP16 values of their NVFP4 quantisation
+    const CUtensorMapDataType act =
+        fp4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap m_wg, m_wu, m_wd, m_xp, m_h;
-    if (!make_map(&m_wg, w_gate, H, (uint64_t)E * I, 128) ||
-        !make_map(&m_wu, w_up, H, (uint64_t)E * I, 128) ||
-        !make_map(&m_wd, w_down, I, (uint64_t)E * H, 128) ||
-        !make_map(&m_xp, at<void>(ws, L.x_perm), H, (uint64_t)R, 16) ||
-        !make_map(&m_h, at<void>(ws, L.h), I, (uint64_t)R, 16))
+    bool maps_ok;
+    if (fp4)
+        maps_ok = make_code_map(&m_wg, w_gate, H, (uint64_t)E * I) &&
+                  make_code_map(&m_wu, w_up, H, (uint64_t)E * I) &&
+                  make_code_map(&m_wd, w_down, I, (uint64_t)E * H);
+    else
+        maps_ok = make_map(&m_wg, w_gate, H, (uint64_t)E * I, 128) &&
+                  make_map(&m_wu, w_up, H, (uint64_t)E * I, 128) &&
+                  make_map(&m_wd, w_down, I, (uint64_t)E * H, 128);
+    if (!maps_ok || !make_map(&m_xp, at<void>(ws, L.x_perm), H, (uint64_t)R, 16, act) ||
+        !make_map(&m_h, at<void>(ws, L.h), I, (uint64_t)R, 16, act))
         return BEAM_MOE_ERR_CUDA;
 
     const int sms = device_sms();
@@ -236,14 +263,25 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     a.ksteps = H / 64;
     a.out = at<void>(ws, L.h);
     a.out_ld = I;
-    BEAM_CUDA(launch_gateup(v, m_wg, m_wu, m_xp, a, sms, s));
+    if (fp4) {
+        Fp4Weights f{static_cast<const uint8_t *>(c.w_gate_sf),
+                     static_cast<const uint8_t *>(c.w_up_sf), c.w_gate_gs, c.w_up_gs};
+        BEAM_CUDA(launch_gateup_fp4(v, m_wg, m_wu, m_xp, a, f, sms, s));
+    } else {
+        BEAM_CUDA(launch_gateup(v, m_wg, m_wu, m_xp, a, sms, s));
+    }
 
     a.m_tiles = H / 128;
     a.ksteps = I / 64;
     a.out = at<void>(ws, L.y);
     a.out_ld = H;
     a.debug_flags = 0;
-    BEAM_CUDA(launch_down(v, m_wd, m_h, a, sms, s));
+    if (fp4) {
+        Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, c.w_down_gs, nullptr};
+        BEAM_CUDA(launch_down_fp4(v, m_wd, m_h, a, f, sms, s));
+    } else {
+        BEAM_CUDA(launch_down(v, m_wd, m_h, a, sms, s));
+    }
 
     BEAM_CUDA(launch_combine(at<float>(ws, L.y), at<float>(ws, L.wts), at<int32_t>(ws, L.row_of),
                              (int)T, K, H, static_cast<uint16_t *>(out), s));
@@ -334,10 +372,15 @@ int beam_moe_forward(const void *x, const float *router_w, const void *w_gate, c
         return rc;
     if (T == 0)
         return BEAM_MOE_OK;
-    if (cfg->wtype != BEAM_MOE_W_BF16)
-        return BEAM_MOE_ERR_UNSUPPORTED;
     if (!x || !router_w || !w_gate || !w_up || !w_down || !out)
         return BEAM_MOE_ERR_INVALID_ARG;
+    if (cfg->wtype == BEAM_MOE_W_NVFP4) {
+        const void *p[6] = {cfg->w_gate_sf, cfg->w_up_sf, cfg->w_down_sf,
+                            cfg->w_gate_gs, cfg->w_up_gs, cfg->w_down_gs};
+        for (const void *q : p)
+            if (!q || !aligned16(q))
+                return BEAM_MOE_ERR_INVALID_ARG;
+    }
     if (!aligned16(x) || !aligned16(router_w) || !aligned16(w_gate) || !aligned16(w_up) ||
         !aligned16(w_down) || !aligned16(out))
         return BEAM_MOE_ERR_INVALID_ARG;
@@ -380,15 +423,19 @@ int beam_moe_forward_hostio(const void *x_host, const float *router_w, const voi
 int beam_moe_quantize_nvfp4(const void *w, int64_t n_mat, int64_t rows, int64_t cols,
                             void *packed, void *block_sf, float *global_sf, void *stream)
 {
-    (void)w;
-    (void)n_mat;
-    (void)rows;
-    (void)cols;
-    (void)packed;
-    (void)block_sf;
-    (void)global_sf;
-    (void)stream;
-    return BEAM_MOE_ERR_UNSUPPORTED;
+    if (n_mat == 0 || rows == 0)
+        return BEAM_MOE_OK;
+    if (n_mat < 0 || rows < 0 || cols <= 0 || rows % 128 || cols % 64 || rows > (1 << 24) ||
+        cols > (1 << 24) || n_mat > (1 << 20))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (!w || !packed || !block_sf || !global_sf || !aligned16(w) || !aligned16(packed) ||
+        !aligned16(block_sf) || !aligned16(global_sf))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    BEAM_CUDA(launch_quantize_nvfp4(static_cast<const uint16_t *>(w), n_mat, (int)rows, (int)cols,
+                                    static_cast<uint8_t *>(packed),
+                                    static_cast<uint8_t *>(block_sf), global_sf,
+                                    static_cast<cudaStream_t>(stream)));
+    return BEAM_MOE_OK;
 }
 
 int beam_moe_read_status(const beam_moe_cfg *cfg, void *stream)

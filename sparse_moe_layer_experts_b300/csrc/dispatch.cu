@@ -9,6 +9,7 @@
 // expert outputs are combined with the normalised router weights).
 #include "common.cuh"
 #include "internal.h"
+#include "nvfp4.cuh"
 
 namespace beam {
 
@@ -112,7 +113,10 @@ scan_kernel(const int32_t *__restrict__ cta_counts, int n_cta, int E, int chunk_
 }
 
 // CTA per token, warp per slot: place the pair's row, copy the token's
-// activations into the expert-grouped buffer with 16-byte accesses.
+// activations into the expert-grouped buffer with 16-byte accesses.  With
+// QUANT (NVFP4 layers) each 16-element block is quantised to NVFP4 (scale 1)
+// on the way and stored as the exact FP16 values q * sf.
+template <bool QUANT>
 __global__ void __launch_bounds__(256)
 permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
                const int32_t *__restrict__ local_rank, const int32_t *__restrict__ cta_base,
@@ -134,8 +138,34 @@ permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
             row_src[row] = t;
         }
         uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)row * H);
-        for (int i = lane; i < nvec; i += 32)
-            dst[i] = src[i];
+        if constexpr (!QUANT) {
+            for (int i = lane; i < nvec; i += 32)
+                dst[i] = src[i];
+        } else {
+            for (int blk = lane; blk < H / 16; blk += 32) {
+                const uint4 q0 = src[2 * blk], q1 = src[2 * blk + 1];
+                const uint32_t raw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                float v[16];
+                float bmax = 0.0f;
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    v[2 * p] = bf16_bits_to_f32(raw[p] & 0xFFFFu);
+                    v[2 * p + 1] = bf16_bits_to_f32(raw[p] >> 16);
+                    bmax = fmaxf(bmax, fmaxf(fabsf(v[2 * p]), fabsf(v[2 * p + 1])));
+                }
+                float sfv;
+                nvfp4_block_scale(bmax, 1.0f, &sfv);
+                uint32_t o[8];
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    const __half2 hv = __floats2half2_rn(nvfp4_fake_quant(v[2 * p], sfv),
+                                                         nvfp4_fake_quant(v[2 * p + 1], sfv));
+                    o[p] = *reinterpret_cast<const uint32_t *>(&hv);
+                }
+                dst[2 * blk] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[2 * blk + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+        }
     }
 }
 
@@ -211,11 +241,15 @@ cudaError_t launch_scan(const int32_t *cta_counts, int n_cta, int E, int chunk_r
 cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
                            const int32_t *cta_base, const int32_t *offsets, int T, int K, int E,
                            int H, int32_t *row_of, int32_t *row_src, uint16_t *x_perm,
-                           cudaStream_t s)
+                           bool quant_nvfp4, cudaStream_t s)
 {
     stage_begin(kStPermute, s);
-    permute_kernel<<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, T, K, E, H, row_of,
-                                     row_src, x_perm);
+    if (quant_nvfp4)
+        permute_kernel<true><<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, T, K, E, H,
+                                               row_of, row_src, x_perm);
+    else
+        permute_kernel<false><<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, T, K, E,
+                                                H, row_of, row_src, x_perm);
     stage_end(kStPermute, s);
     return cudaGetLastError();
 }

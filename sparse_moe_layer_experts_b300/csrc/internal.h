@@ -45,7 +45,7 @@ cudaError_t launch_scan(const int32_t *cta_counts, int n_cta, int E, int chunk_r
 cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
                            const int32_t *cta_base, const int32_t *offsets, int T, int K, int E,
                            int H, int32_t *row_of, int32_t *row_src, uint16_t *x_perm,
-                           cudaStream_t s);
+                           bool quant_nvfp4, cudaStream_t s);
 // route-only variant: row_of without moving activations
 cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int32_t *cta_base,
                         const int32_t *offsets, int T, int K, int E, int32_t *row_of,
@@ -69,6 +69,17 @@ struct GemmArgs {
 
 enum class GemmVariant { kDecode, kPrefill };
 
+// NVFP4 weights: E2M1 codes, tiled E4M3 block scales, FP32 global scales.
+struct Fp4Weights {
+    const uint8_t *sf0, *sf1;  // block scales of A0 / A1 (A1: up projection)
+    const float *gs0, *gs1;    // global scales [E]
+};
+
+// ---- nvfp4.cu
+cudaError_t launch_quantize_nvfp4(const uint16_t *w, int64_t n_mat, int rows, int cols,
+                                  uint8_t *packed, uint8_t *block_sf, float *global_sf,
+                                  cudaStream_t s);
+
 // chunk height (rows of one expert handled by one tile) of a variant
 int gemm_chunk_rows(GemmVariant v);
 
@@ -78,5 +89,13 @@ cudaError_t launch_gateup(GemmVariant v, const CUtensorMap &wg, const CUtensorMa
 // y = h . Wd^T per expert segment (fp32 out)
 cudaError_t launch_down(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
                         const GemmArgs &a, int grid, cudaStream_t s);
+
+// ---- grouped_gemm_fp4.cu: the same GEMMs with NVFP4 weights (codes via
+// TMA maps of the packed bytes) and FP16 activations; gate/up quantises h.
+cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
+                              const CUtensorMap &xp, const GemmArgs &a, const Fp4Weights &f,
+                              int grid, cudaStream_t s);
+cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
+                            const GemmArgs &a, const Fp4Weights &f, int grid, cudaStream_t s);
 
 }  // namespace beam

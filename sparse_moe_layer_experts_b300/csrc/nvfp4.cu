@@ -1,0 +1,115 @@
+// NVFP4 weight quantisation (offline preparation of the expert weights).
+//
+// Layouts written (see beam_moe_quantize_nvfp4 in the header):
+//   packed   [n_mat, rows, cols/2]  two E2M1 codes per byte, even element in
+//                                   the low nibble
+//   block_sf [n_mat, rows/128, cols/64, 128, 4]  the E4M3 scale of elements
+//            [16b, 16b+16) of row r sits at tile (r/128, b/4), entry
+//            (r%128, b%4): the 512 scales one 128x64 GEMM tile needs are
+//            contiguous
+//   global   [n_mat] FP32
+#include "common.cuh"
+#include "internal.h"
+#include "nvfp4.cuh"
+
+namespace beam {
+
+namespace {
+
+// One CTA per matrix: amax over rows*cols bf16 values, then the global scale.
+__global__ void __launch_bounds__(1024)
+nvfp4_global_scale_kernel(const uint16_t *__restrict__ w, int64_t per_mat, float *__restrict__ gs)
+{
+    __shared__ float red[32];
+    const uint16_t *wm = w + (size_t)blockIdx.x * per_mat;
+    float m = 0.0f;
+    for (int64_t i = (int64_t)threadIdx.x * 8; i < per_mat; i += 1024 * 8) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(wm + i);
+        const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            m = fmaxf(m, fabsf(bf16_bits_to_f32(v[p] & 0xFFFFu)));
+            m = fmaxf(m, fabsf(bf16_bits_to_f32(v[p] >> 16)));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = red[threadIdx.x];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+        if (threadIdx.x == 0)
+            gs[blockIdx.x] = (m > 0.0f) ? __fdiv_rn(m, 6.0f * 448.0f) : 1.0f;
+    }
+}
+
+// One thread per 16-element block.
+__global__ void __launch_bounds__(256)
+nvfp4_quantize_kernel(const uint16_t *__restrict__ w, int64_t n_blocks, int rows, int cols,
+                      const float *__restrict__ gs, uint8_t *__restrict__ packed,
+                      uint8_t *__restrict__ block_sf)
+{
+    const int64_t b = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (b >= n_blocks)
+        return;
+    const int bpr = cols / 16;
+    const int64_t per_mat = (int64_t)rows * bpr;
+    const int64_t mat = b / per_mat;
+    const int64_t rem = b - mat * per_mat;
+    const int r = (int)(rem / bpr), cb = (int)(rem % bpr);
+    const int64_t elem = (mat * rows + r) * (int64_t)cols + (int64_t)cb * 16;
+
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(w + elem);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(w + elem + 8);
+    const uint32_t raw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    float v[16];
+    float bmax = 0.0f;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        v[2 * p] = bf16_bits_to_f32(raw[p] & 0xFFFFu);
+        v[2 * p + 1] = bf16_bits_to_f32(raw[p] >> 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        bmax = fmaxf(bmax, fabsf(v[i]));
+    const float g = gs[mat];
+    float sfv;
+    const uint32_t sc = nvfp4_block_scale(bmax, g, &sfv);
+    const float den = __fmul_rn(sfv, g);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t c = (sfv == 0.0f) ? 0u : e2m1_code(__fdiv_rn(v[i], den));
+        if (i < 8)
+            lo |= c << (4 * i);
+        else
+            hi |= c << (4 * (i - 8));
+    }
+    *reinterpret_cast<uint2 *>(packed + elem / 2) = make_uint2(lo, hi);
+    const int64_t tile = (mat * (rows / 128) + r / 128) * (cols / 64) + cb / 4;
+    block_sf[tile * 512 + (r % 128) * 4 + (cb % 4)] = (uint8_t)sc;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_nvfp4(const uint16_t *w, int64_t n_mat, int rows, int cols,
+                                  uint8_t *packed, uint8_t *block_sf, float *global_sf,
+                                  cudaStream_t s)
+{
+    stage_begin(kNumStages, s);
+    nvfp4_global_scale_kernel<<<(unsigned)n_mat, 1024, 0, s>>>(w, (int64_t)rows * cols, global_sf);
+    stage_end(kNumStages, s);
+    const int64_t n_blocks = n_mat * rows * (int64_t)(cols / 16);
+    stage_begin(kNumStages, s);
+    nvfp4_quantize_kernel<<<(unsigned)((n_blocks + 255) / 256), 256, 0, s>>>(
+        w, n_blocks, rows, cols, global_sf, packed, block_sf);
+    stage_end(kNumStages, s);
+    return cudaGetLastError();
+}
+
+}  // namespace beam

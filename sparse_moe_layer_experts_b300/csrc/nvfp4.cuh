@@ -1,0 +1,82 @@
+// NVFP4 numerics: E2M1 values with one E4M3 scale per 16 elements and an
+// FP32 scale per matrix.  The Beam pages name the format only ("most
+// parameters in 4 bits" for Blackwell: "Reflection Beam 1.0", section on
+// hardware requirements); the recipe below is a reading:
+//   gs = amax|W| / (6*448) per matrix (1 for an all-zero matrix)
+//   sf = e4m3_rn_satfinite((amax16 / 6) / gs)
+//   q  = e2m1_rn_satfinite(v / (sf * gs)),   0 when sf == 0
+// Activations use the same blocks with gs = 1.  q * sf always fits an FP16
+// exactly (at most 6 significant bits, magnitude in [2^-10, 2688]).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace beam {
+
+// Nearest E2M1 code (ties to the even mantissa bit, saturating at 6, sign
+// kept in bit 3).  Thresholds are the midpoints of 0, .5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ uint32_t e2m1_code(float v)
+{
+    const float a = fabsf(v);
+    uint32_t c;
+    if (a <= 0.25f)
+        c = 0;
+    else if (a < 0.75f)
+        c = 1;
+    else if (a <= 1.25f)
+        c = 2;
+    else if (a < 1.75f)
+        c = 3;
+    else if (a <= 2.5f)
+        c = 4;
+    else if (a < 3.5f)
+        c = 5;
+    else if (a <= 5.0f)
+        c = 6;
+    else
+        c = 7;
+    return c | (signbit(v) ? 8u : 0u);
+}
+
+__device__ __forceinline__ float e2m1_value(uint32_t c)
+{
+    // magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 built as FP32 bit patterns:
+    // exponent 126 + (m >> 1), mantissa bit (m & 1) for m >= 2
+    const uint32_t m = c & 7u;
+    const uint32_t bits =
+        (m == 0u) ? 0u : ((126u + (m >> 1)) << 23) | ((m >= 2u ? (m & 1u) : 0u) << 22);
+    return __uint_as_float(bits | ((c & 8u) << 28));
+}
+
+__device__ __forceinline__ uint32_t e4m3_code(float v)
+{
+    return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t c)
+{
+    __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+// Block scale of 16 values whose largest magnitude is bmax, for global
+// scale gs: returns the E4M3 code; *sfv its value.
+__device__ __forceinline__ uint32_t nvfp4_block_scale(float bmax, float gs, float *sfv)
+{
+    const uint32_t c = e4m3_code(__fdiv_rn(__fdiv_rn(bmax, 6.0f), gs));
+    *sfv = e4m3_value(c);
+    return c;
+}
+
+// Quantise-dequantise one value of a block with scale sfv (gs = 1): the
+// exact value q * sfv.
+__device__ __forceinline__ float nvfp4_fake_quant(float v, float sfv)
+{
+    if (sfv == 0.0f)
+        return 0.0f;
+    return e2m1_value(e2m1_code(__fdiv_rn(v, sfv))) * sfv;
+}
+
+}  // namespace beam

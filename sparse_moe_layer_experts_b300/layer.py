@@ -15,9 +15,27 @@ def _stream_handle(stream) -> int:
     return s.cuda_stream
 
 
+def quantize_nvfp4(w: torch.Tensor, stream=None):
+    """NVFP4-quantise bf16 matrices [n_mat, rows, cols] on the GPU.
+
+    Returns (packed [n_mat, rows, cols/2] uint8, block scales (flat uint8, the
+    tiled layout of beam_moe_quantize_nvfp4), global scales [n_mat] fp32)."""
+    if w.dtype != torch.bfloat16 or w.dim() != 3 or not w.is_cuda or not w.is_contiguous():
+        raise ValueError("w must be a contiguous CUDA bf16 [n_mat, rows, cols] tensor")
+    n_mat, rows, cols = w.shape
+    packed = torch.empty((n_mat, rows, cols // 2), dtype=torch.uint8, device=w.device)
+    sf = torch.empty(n_mat * rows * (cols // 16), dtype=torch.uint8, device=w.device)
+    gs = torch.empty(n_mat, dtype=torch.float32, device=w.device)
+    B.check(B.beam_moe_quantize_nvfp4(w.data_ptr(), n_mat, rows, cols, packed.data_ptr(),
+                                      sf.data_ptr(), gs.data_ptr(), _stream_handle(stream)),
+            "beam_moe_quantize_nvfp4")
+    return packed, sf, gs
+
+
 class BeamMoE:
     """Resident-weight layer.  Weights: w_gate/w_up [E,I,H] bf16, w_down [E,H,I]
-    bf16, router_w [H,E] fp32, all contiguous on one CUDA device."""
+    bf16, router_w [H,E] fp32, all contiguous on one CUDA device.  For NVFP4
+    weights use BeamMoE.nvfp4()."""
 
     def __init__(self, router_w, w_gate, w_up, w_down, n_groups=8, topk_groups=4, top_k=8,
                  routed_scale=2.5, wait_timeout_ns=0, debug_flags=0):
@@ -26,13 +44,34 @@ class BeamMoE:
                              (w_up, (E, I, H), torch.bfloat16), (w_down, (E, H, I), torch.bfloat16)):
             if tuple(t.shape) != shape or t.dtype != dt or not t.is_cuda or not t.is_contiguous():
                 raise ValueError(f"expected contiguous CUDA {dt} of shape {shape}")
+        self._setup(router_w, w_gate, w_up, w_down, E, I, H, n_groups, topk_groups, top_k,
+                    routed_scale, wait_timeout_ns, debug_flags)
+
+    def _setup(self, router_w, w_gate, w_up, w_down, E, I, H, n_groups, topk_groups, top_k,
+               routed_scale, wait_timeout_ns, debug_flags, wtype=B.BEAM_MOE_W_BF16):
         self.router_w, self.w_gate, self.w_up, self.w_down = router_w, w_gate, w_up, w_down
         self.H, self.I, self.E = H, I, E
-        self.cfg = B.make_cfg(H, I, E, n_groups, topk_groups, top_k, routed_scale)
+        self.cfg = B.make_cfg(H, I, E, n_groups, topk_groups, top_k, routed_scale, wtype)
         self.cfg.wait_timeout_ns = wait_timeout_ns
         self.cfg.debug_flags = debug_flags
         self.device = w_gate.device
         self._ws = None
+
+    @classmethod
+    def nvfp4(cls, router_w, q_gate, q_up, q_down, n_groups=8, topk_groups=4, top_k=8,
+              routed_scale=2.5, wait_timeout_ns=0):
+        """Layer with NVFP4 experts; q_* = quantize_nvfp4(w_*)."""
+        self = cls.__new__(cls)
+        E, I, H2 = q_gate[0].shape
+        H = H2 * 2
+        self._setup(router_w, q_gate[0], q_up[0], q_down[0], E, I, H, n_groups, topk_groups,
+                    top_k, routed_scale, wait_timeout_ns, 0, B.BEAM_MOE_W_NVFP4)
+        self._scales = (q_gate, q_up, q_down)  # keep them alive
+        self.cfg.w_gate_sf, self.cfg.w_up_sf, self.cfg.w_down_sf = (
+            q[1].data_ptr() for q in (q_gate, q_up, q_down))
+        self.cfg.w_gate_gs, self.cfg.w_up_gs, self.cfg.w_down_gs = (
+            q[2].data_ptr() for q in (q_gate, q_up, q_down))
+        return self
 
     @property
     def top_k(self):
