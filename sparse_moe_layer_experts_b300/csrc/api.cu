@@ -244,8 +244,9 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
         maps_ok = make_map(&m_wg, w_gate, H, (uint64_t)E * I, 128) &&
                   make_map(&m_wu, w_up, H, (uint64_t)E * I, 128) &&
                   make_map(&m_wd, w_down, I, (uint64_t)E * H, 128);
-    if (!maps_ok || !make_map(&m_xp, at<void>(ws, L.x_perm), H, (uint64_t)R, 16, act) ||
-        !make_map(&m_h, at<void>(ws, L.h), I, (uint64_t)R, 16, act))
+    const uint32_t box = (uint32_t)gemm_box_rows(v);
+    if (!maps_ok || !make_map(&m_xp, at<void>(ws, L.x_perm), H, (uint64_t)R, box, act) ||
+        !make_map(&m_h, at<void>(ws, L.h), I, (uint64_t)R, box, act))
         return BEAM_MOE_ERR_CUDA;
 
     const int sms = device_sms();

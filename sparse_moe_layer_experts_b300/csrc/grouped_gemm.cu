@@ -21,7 +21,9 @@
 // Persistent kernel, one CTA per SM, warp-specialised:
 //   warp 0      TMA producer (one thread)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2..5  epilogue: tcgen05.ld from TMEM, SwiGLU, global stores
+//   warps 2..   epilogue warpgroup(s): tcgen05.ld from TMEM, SwiGLU, global
+//               stores; with two warpgroups each takes every other 16-column
+//               chunk of the tile
 // Tiles are enumerated expert by expert, weight tile by weight tile, token
 // chunk fastest, so CTAs that run at the same time share weight tiles in L2.
 #include "common.cuh"
@@ -34,17 +36,19 @@ namespace beam {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kNonEpiThreads = 64;  // producer warp + MMA warp
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 64;  // 64 bf16 = one 128-byte swizzle row
 constexpr int kABytes = kBlockM * kBlockK * 2;
-constexpr int kBoxRows = 16;  // token rows per TMA box
-constexpr int kBoxBytes = kBoxRows * kBlockK * 2;
 constexpr int kMaxExperts = 256;
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS>
+// BOX: token rows per TMA box of the B operand (bigger boxes, fewer TMA
+// operations); EPI_WG: epilogue warpgroups, which split a tile's columns.
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG>
 struct Cfg {
     static constexpr int NA = GATEUP ? 2 : 1;
+    static constexpr int THREADS = kNonEpiThreads + 128 * EPI_WG;
+    static constexpr int BOX_BYTES = BOX * kBlockK * 2;
     static constexpr int B_BYTES = BN * kBlockK * 2;
     static constexpr int STAGE_BYTES = NA * kABytes + B_BYTES;
     static constexpr int ACC_COLS = NA * BN;
@@ -59,6 +63,7 @@ struct Cfg {
     static constexpr int AUX_BYTES = N_BARS * 8 + 16 + 2 * (kMaxExperts + 1) * 4;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + ((AUX_BYTES + 127) / 128) * 128;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+    static_assert(BN % BOX == 0 && BOX % 16 == 0, "token boxes tile the B operand");
     static_assert(COLS_RAW <= 512, "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -68,13 +73,13 @@ __device__ __forceinline__ float silu_mul(float g, float u)
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG>
+__global__ void __launch_bounds__(kNonEpiThreads + 128 * EPI_WG, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB, const GemmArgs p)
 {
-    using C = Cfg<GATEUP, BN, STAGES, ACC_BUFS>;
+    using C = Cfg<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
@@ -103,7 +108,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         }
         for (int a = 0; a < ACC_BUFS; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 128);
+            mbar_init(tempty_bar(a), 128 * EPI_WG);
         }
         mbar_init(drain_bar, 1);
         *s_abort = 0;
@@ -119,7 +124,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
-    for (int i = threadIdx.x; i <= E; i += kThreads) {
+    for (int i = threadIdx.x; i <= E; i += C::THREADS) {
         s_off[i] = p.offsets[i];
         s_cs[i] = p.chunk_start[i];
     }
@@ -140,8 +145,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const Tile tl = decode_tile(t, s_off, s_cs, E, p.m_tiles);
                 const int arow = tl.e * p.m_tiles * kBlockM + tl.m * kBlockM;
-                const int nb = (tl.nrows + kBoxRows - 1) / kBoxRows;
-                const uint32_t bytes = C::NA * kABytes + nb * kBoxBytes;
+                const int nb = (tl.nrows + BOX - 1) / BOX;
+                const uint32_t bytes = C::NA * kABytes + nb * C::BOX_BYTES;
                 for (int k = 0; k < p.ksteps; ++k) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, tmo, s_abort, p.status)) {
                         ok = false;
@@ -159,8 +164,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                             tma_load_2d(sa + kABytes, &tmA1, k * kBlockK, arow, full_bar(stage));
                         const uint32_t sb = sa + C::NA * kABytes;
                         for (int b = 0; b < nb; ++b)
-                            tma_load_2d(sb + b * kBoxBytes, &tmB, k * kBlockK,
-                                        tl.row0 + b * kBoxRows, full_bar(stage));
+                            tma_load_2d(sb + b * C::BOX_BYTES, &tmB, k * kBlockK,
+                                        tl.row0 + b * BOX, full_bar(stage));
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -232,6 +237,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int i = q * 32 + lane;
+        const int wg = (warp - 2) >> 2;  // this warpgroup takes column chunks wg, wg+EPI_WG, ...
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
@@ -241,7 +247,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             tc_fence_after();
             const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::ACC_COLS;
             const int col = tl.m * kBlockM + i;
-            for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
+            for (int c0 = wg * 16; c0 < tl.nrows; c0 += 16 * EPI_WG) {
                 uint32_t g[16];
                 tmem_ld16(ta + c0, g);
                 if (GATEUP) {
@@ -281,12 +287,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
     }
 }
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG>
 cudaError_t launch_variant(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                            const GemmArgs &args, int grid, int stage, cudaStream_t s)
 {
-    using C = Cfg<GATEUP, BN, STAGES, ACC_BUFS>;
-    auto kern = grouped_gemm_kernel<GATEUP, BN, STAGES, ACC_BUFS>;
+    using C = Cfg<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG>;
+    auto kern = grouped_gemm_kernel<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -296,7 +302,7 @@ cudaError_t launch_variant(const CUtensorMap &a0, const CUtensorMap &a1, const C
     if (attr_err != cudaSuccess)
         return attr_err;
     stage_begin(stage, s);
-    kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, args);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a0, a1, b, args);
     stage_end(stage, s);
     return cudaGetLastError();
 }
@@ -308,20 +314,25 @@ int gemm_chunk_rows(GemmVariant v)
     return v == GemmVariant::kDecode ? 32 : 256;
 }
 
+int gemm_box_rows(GemmVariant v)
+{
+    return v == GemmVariant::kDecode ? 16 : 64;
+}
+
 cudaError_t launch_gateup(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
                           const CUtensorMap &xp, const GemmArgs &a, int grid, cudaStream_t s)
 {
     if (v == GemmVariant::kDecode)
-        return launch_variant<true, 32, 6, 2>(wg, wu, xp, a, grid, kStGateUp, s);
-    return launch_variant<true, 256, 3, 1>(wg, wu, xp, a, grid, kStGateUp, s);
+        return launch_variant<true, 32, 6, 2, 16, 1>(wg, wu, xp, a, grid, kStGateUp, s);
+    return launch_variant<true, 256, 3, 1, 64, 2>(wg, wu, xp, a, grid, kStGateUp, s);
 }
 
 cudaError_t launch_down(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
                         const GemmArgs &a, int grid, cudaStream_t s)
 {
     if (v == GemmVariant::kDecode)
-        return launch_variant<false, 32, 10, 2>(wd, wd, hp, a, grid, kStDown, s);
-    return launch_variant<false, 256, 4, 2>(wd, wd, hp, a, grid, kStDown, s);
+        return launch_variant<false, 32, 10, 2, 16, 1>(wd, wd, hp, a, grid, kStDown, s);
+    return launch_variant<false, 256, 4, 2, 64, 2>(wd, wd, hp, a, grid, kStDown, s);
 }
 
 }  // namespace beam

@@ -14,13 +14,13 @@
 // the permute kernel) and of h (quantised here, in the gate/up epilogue).  The
 // global scale multiplies the FP32 accumulator in the epilogue.
 //
-// Warp roles (320 threads):
+// Warp roles:
 //   warp 0      producer: TMA of the code tile + bulk copy of its 512 scale
 //               bytes into a deep "raw" ring, and TMA of the token tile into
 //               the B ring
 //   warp 1      TMEM allocator and MMA issuer
-//   warps 2..5  epilogue
-//   warps 6..9  converters, one weight row per thread: raw ring -> FP16 A
+//   next 4*EPI_WG warps: epilogue warpgroup(s), splitting a tile's columns
+//   last 4 warps converters, one weight row per thread: raw ring -> FP16 A
 //               tiles (128-byte swizzled, K-major) of the A ring
 #include "common.cuh"
 #include "gemm_common.cuh"
@@ -33,19 +33,19 @@ namespace beam {
 
 namespace {
 
-constexpr int kThreads = 320;
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 64;
 constexpr int kCodeBytes = kBlockM * kBlockK / 2;  // 4096
 constexpr int kSfBytes = kBlockM * kBlockK / 16;   // 512
 constexpr int kAF16Bytes = kBlockM * kBlockK * 2;  // 16384
-constexpr int kBoxRows = 16;
-constexpr int kBoxBytes = kBoxRows * kBlockK * 2;
 constexpr int kMaxExperts = 256;
 
-template <bool GATEUP, int BN, int RS, int AS, int BS, int ACC_BUFS>
+template <bool GATEUP, int BN, int RS, int AS, int BS, int ACC_BUFS, int BOX, int EPI_WG>
 struct CfgF {
     static constexpr int NA = GATEUP ? 2 : 1;
+    static constexpr int THREADS = 64 + 128 * EPI_WG + 128;
+    static constexpr int CONV_WARP0 = 2 + 4 * EPI_WG;
+    static constexpr int BOX_BYTES = BOX * kBlockK * 2;
     static constexpr int RAW_BYTES = NA * (kCodeBytes + kSfBytes);
     static constexpr int A_BYTES = NA * kAF16Bytes;     // converted weight tiles
     static constexpr int B_BYTES = BN * kBlockK * 2;    // token tile
@@ -61,6 +61,7 @@ struct CfgF {
     static constexpr int SMEM_BYTES = 1024 + AS * A_BYTES + BS * B_BYTES + RS * RAW_BYTES +
                                       ((AUX_BYTES + 127) / 128) * 128;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+    static_assert(BN % BOX == 0 && BOX % 16 == 0, "token boxes tile the B operand");
     static_assert(COLS_RAW <= 512, "TMEM columns");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && RAW_BYTES % 128 == 0,
                   "alignment");
@@ -120,13 +121,13 @@ __device__ __forceinline__ float silu_mul_f(float g, float u)
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <bool GATEUP, int BN, int RS, int AS, int BS, int ACC_BUFS>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool GATEUP, int BN, int RS, int AS, int BS, int ACC_BUFS, int BOX, int EPI_WG>
+__global__ void __launch_bounds__(64 + 128 * EPI_WG + 128, 1)
 grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB, const Fp4Params P)
 {
-    using C = CfgF<GATEUP, BN, RS, AS, BS, ACC_BUFS>;
+    using C = CfgF<GATEUP, BN, RS, AS, BS, ACC_BUFS, BOX, EPI_WG>;
     const GemmArgs &p = P.a;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -173,7 +174,7 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
         }
         for (int a = 0; a < ACC_BUFS; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 128);
+            mbar_init(tempty_bar(a), 128 * EPI_WG);
         }
         mbar_init(drain_bar, 1);
         *s_abort = 0;
@@ -189,7 +190,7 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
-    for (int i = threadIdx.x; i <= E; i += kThreads) {
+    for (int i = threadIdx.x; i <= E; i += C::THREADS) {
         s_off[i] = p.offsets[i];
         s_cs[i] = p.chunk_start[i];
     }
@@ -210,7 +211,7 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
                 const Tile tl = decode_tile(t, s_off, s_cs, E, p.m_tiles);
                 const int arow = tl.e * p.m_tiles * kBlockM + tl.m * kBlockM;
                 const size_t sf_tile = ((size_t)tl.e * p.m_tiles + tl.m) * P.ksteps_total;
-                const int nb = (tl.nrows + kBoxRows - 1) / kBoxRows;
+                const int nb = (tl.nrows + BOX - 1) / BOX;
                 for (int k = 0; k < p.ksteps; ++k) {
                     if (!mbar_wait_bounded(raw_empty(rs), rph ^ 1u, tmo, s_abort, p.status)) {
                         ok = false;
@@ -237,12 +238,12 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(b_full(bs), nb * kBoxBytes);
+                    mbar_arrive_expect_tx(b_full(bs), nb * C::BOX_BYTES);
                     barmed |= 1u << bs;
                     barmed_par = (barmed_par & ~(1u << bs)) | (bph << bs);
                     const uint32_t sb = b_u32 + bs * C::B_BYTES;
                     for (int bb = 0; bb < nb; ++bb)
-                        tma_load_2d(sb + bb * kBoxBytes, &tmB, k * kBlockK, tl.row0 + bb * kBoxRows,
+                        tma_load_2d(sb + bb * C::BOX_BYTES, &tmB, k * kBlockK, tl.row0 + bb * BOX,
                                     b_full(bs));
                     if (++bs == BS) {
                         bs = 0;
@@ -320,10 +321,11 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < C::CONV_WARP0) {
         // ------------------------------------------------- epilogue
         const int q = warp & 3;
         const int i = q * 32 + lane;
+        const int wg = (warp - 2) >> 2;  // column chunks wg, wg+EPI_WG, ...
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
@@ -335,7 +337,7 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
             tc_fence_after();
             const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::ACC_COLS;
             const int col = tl.m * kBlockM + i;
-            for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
+            for (int c0 = wg * 16; c0 < tl.nrows; c0 += 16 * EPI_WG) {
                 uint32_t g[16];
                 tmem_ld16(ta + c0, g);
                 if constexpr (GATEUP) {
@@ -352,11 +354,9 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
 #pragma unroll
                         for (int off = 8; off > 0; off >>= 1)
                             bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, off));
-                        float sfv;
-                        nvfp4_block_scale(bmax, 1.0f, &sfv);
                         if (c0 + j < tl.nrows)
                             out[(size_t)(tl.row0 + c0 + j) * p.out_ld + col] =
-                                __float2half_rn(nvfp4_fake_quant(h, sfv));
+                                __float2half_rn(nvfp4_fake_quant_fast(h, bmax));
                     }
                 } else {
                     tmem_ld_wait();
@@ -377,7 +377,7 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
         }
     } else {
         // ------------------------------------------------ converters
-        const int r = (warp - 6) * 32 + lane;  // weight row of the tile
+        const int r = (warp - C::CONV_WARP0) * 32 + lane;  // weight row of the tile
         int rs = 0, as = 0;
         uint32_t rph = 0, aph = 0;
         bool ok = true;
@@ -439,13 +439,13 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
     }
 }
 
-template <bool GATEUP, int BN, int RS, int AS, int BS, int ACC_BUFS>
+template <bool GATEUP, int BN, int RS, int AS, int BS, int ACC_BUFS, int BOX, int EPI_WG>
 cudaError_t launch_fp4_variant(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                                const GemmArgs &args, const Fp4Weights &f, int grid, int stage,
                                cudaStream_t s)
 {
-    using C = CfgF<GATEUP, BN, RS, AS, BS, ACC_BUFS>;
-    auto kern = grouped_gemm_fp4_kernel<GATEUP, BN, RS, AS, BS, ACC_BUFS>;
+    using C = CfgF<GATEUP, BN, RS, AS, BS, ACC_BUFS, BOX, EPI_WG>;
+    auto kern = grouped_gemm_fp4_kernel<GATEUP, BN, RS, AS, BS, ACC_BUFS, BOX, EPI_WG>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -459,7 +459,7 @@ cudaError_t launch_fp4_variant(const CUtensorMap &a0, const CUtensorMap &a1, con
     P.f = f;
     P.ksteps_total = args.ksteps;
     stage_begin(stage, s);
-    kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, P);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a0, a1, b, P);
     stage_end(stage, s);
     return cudaGetLastError();
 }
@@ -471,16 +471,16 @@ cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtens
                               int grid, cudaStream_t s)
 {
     if (v == GemmVariant::kDecode)
-        return launch_fp4_variant<true, 32, 12, 3, 4, 2>(wg, wu, xp, a, f, grid, kStGateUp, s);
-    return launch_fp4_variant<true, 256, 6, 2, 3, 1>(wg, wu, xp, a, f, grid, kStGateUp, s);
+        return launch_fp4_variant<true, 32, 12, 3, 4, 2, 16, 1>(wg, wu, xp, a, f, grid, kStGateUp, s);
+    return launch_fp4_variant<true, 256, 6, 2, 3, 1, 64, 2>(wg, wu, xp, a, f, grid, kStGateUp, s);
 }
 
 cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
                             const GemmArgs &a, const Fp4Weights &f, int grid, cudaStream_t s)
 {
     if (v == GemmVariant::kDecode)
-        return launch_fp4_variant<false, 32, 16, 4, 6, 2>(wd, wd, hp, a, f, grid, kStDown, s);
-    return launch_fp4_variant<false, 256, 10, 2, 4, 2>(wd, wd, hp, a, f, grid, kStDown, s);
+        return launch_fp4_variant<false, 32, 16, 4, 6, 2, 16, 1>(wd, wd, hp, a, f, grid, kStDown, s);
+    return launch_fp4_variant<false, 256, 10, 2, 4, 2, 64, 2>(wd, wd, hp, a, f, grid, kStDown, s);
 }
 
 }  // namespace beam

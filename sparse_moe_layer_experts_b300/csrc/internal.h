@@ -82,6 +82,8 @@ cudaError_t launch_quantize_nvfp4(const uint16_t *w, int64_t n_mat, int rows, in
 
 // chunk height (rows of one expert handled by one tile) of a variant
 int gemm_chunk_rows(GemmVariant v);
+// token rows per TMA box of the B operand (the B tensor maps' box height)
+int gemm_box_rows(GemmVariant v);
 
 // h = silu(x_perm . Wg^T) * (x_perm . Wu^T) per expert segment (bf16 out)
 cudaError_t launch_gateup(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
