@@ -213,8 +213,8 @@ def workload_algorithmic(sh, n_active: int, nvfp4: bool = False):
         "scan": dict(bytes=((T + 255) // 256) * E * 8, flops=0),
         "permute": dict(bytes=T * H * 2 + R * H * 2, flops=0),
         "gateup_gemm": dict(bytes=w_gu + R * H * 2 + R * I * 2, flops=2 * R * H * 2 * I),
-        "down_gemm": dict(bytes=w_d + R * I * 2 + R * H * 4, flops=2 * R * I * H),
-        "combine": dict(bytes=R * H * 4 + T * H * 2 + R * 8, flops=2 * R * H),
+        "down_gemm": dict(bytes=w_d + R * I * 2 + R * H * 2, flops=2 * R * I * H),
+        "combine": dict(bytes=R * H * 2 + T * H * 2 + R * 8, flops=2 * R * H),
         "layer": dict(bytes=w_gu + w_d + H * E * 4 + 2 * T * H * 2,
                       flops=2 * T * H * E + 6 * R * H * I),
     }

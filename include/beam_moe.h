@@ -185,7 +185,7 @@ size_t beam_moe_hostio_extra_bytes(int64_t T, const beam_moe_cfg *cfg);
  * Arguments are those of beam_moe_forward; cfg->workspace and
  * cfg->workspace_bytes are ignored.
  *  - Limit: beam_moe_workspace_size(T, cfg) must not exceed 24 MiB (at the
- *    Beam sizes: T <= 87 tokens); larger calls return BEAM_MOE_ERR_WORKSPACE
+ *    Beam sizes: T <= 122 tokens); larger calls return BEAM_MOE_ERR_WORKSPACE
  *    with nothing enqueued.  Invalid configurations return
  *    BEAM_MOE_ERR_INVALID_ARG; T = 0 returns BEAM_MOE_OK.
  *  - Memory: every GPU on which this entry point runs keeps the 24 MiB array

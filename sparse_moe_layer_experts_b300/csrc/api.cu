@@ -69,7 +69,7 @@ Layout make_layout(int64_t T, const beam_moe_cfg &c)
     L.row_src = take(sizeof(int32_t) * R);
     L.x_perm = take(2 * R * H);
     L.h = take(2 * R * I);
-    L.y = take(4 * R * H);
+    L.y = take(2 * R * H);
     L.total = o;
     return L;
 }
@@ -284,7 +284,7 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
         BEAM_CUDA(launch_down(v, m_wd, m_h, a, sms, s));
     }
 
-    BEAM_CUDA(launch_combine(at<float>(ws, L.y), at<float>(ws, L.wts), at<int32_t>(ws, L.row_of),
+    BEAM_CUDA(launch_combine(at<uint16_t>(ws, L.y), at<float>(ws, L.wts), at<int32_t>(ws, L.row_of),
                              (int)T, K, H, static_cast<uint16_t *>(out), s));
     return BEAM_MOE_OK;
 }

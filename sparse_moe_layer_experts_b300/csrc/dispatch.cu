@@ -112,10 +112,10 @@ scan_kernel(const int32_t *__restrict__ cta_counts, int n_cta, int E, int chunk_
         chunk_start[E] = total_chunks;
 }
 
-// CTA per token, warp per slot: place the pair's row, copy the token's
-// activations into the expert-grouped buffer with 16-byte accesses.  With
-// QUANT (NVFP4 layers) each 16-element block is quantised to NVFP4 (scale 1)
-// on the way and stored as the exact FP16 values q * sf.
+// CTA per token: place the token's K rows, then read the token's activations
+// once (16-byte vectors) and write them to all K rows.  With QUANT (NVFP4
+// layers) each 16-element block is quantised to NVFP4 (scale 1) once and the
+// exact FP16 values q * sf are written.
 template <bool QUANT>
 __global__ void __launch_bounds__(256)
 permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
@@ -124,46 +124,53 @@ permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
                int32_t *__restrict__ row_of, int32_t *__restrict__ row_src,
                uint16_t *__restrict__ x_perm)
 {
+    __shared__ int rows[32];
     const int t = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = t / kHistTokens;
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
-    const int nvec = H / 8;
-    for (int k = warp; k < K; k += 8) {
+    if (threadIdx.x < K) {
+        const int k = threadIdx.x;
         int e = ids[(size_t)t * K + k];
         e = (e < 0 || e >= E) ? 0 : e;
         const int row = offsets[e] + cta_base[(size_t)cta * E + e] + local_rank[(size_t)t * K + k];
-        if (lane == 0) {
-            row_of[(size_t)t * K + k] = row;
-            row_src[row] = t;
+        rows[k] = row;
+        row_of[(size_t)t * K + k] = row;
+        row_src[row] = t;
+    }
+    __syncthreads();
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+    if constexpr (!QUANT) {
+        for (int i = threadIdx.x; i < H / 8; i += 256) {
+            const uint4 v = src[i];
+            for (int k = 0; k < K; ++k)
+                reinterpret_cast<uint4 *>(x_perm + (size_t)rows[k] * H)[i] = v;
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)row * H);
-        if constexpr (!QUANT) {
-            for (int i = lane; i < nvec; i += 32)
-                dst[i] = src[i];
-        } else {
-            for (int blk = lane; blk < H / 16; blk += 32) {
-                const uint4 q0 = src[2 * blk], q1 = src[2 * blk + 1];
-                const uint32_t raw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                float v[16];
-                float bmax = 0.0f;
+    } else {
+        for (int blk = threadIdx.x; blk < H / 16; blk += 256) {
+            const uint4 q0 = src[2 * blk], q1 = src[2 * blk + 1];
+            const uint32_t raw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            float v[16];
+            float bmax = 0.0f;
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    v[2 * p] = bf16_bits_to_f32(raw[p] & 0xFFFFu);
-                    v[2 * p + 1] = bf16_bits_to_f32(raw[p] >> 16);
-                    bmax = fmaxf(bmax, fmaxf(fabsf(v[2 * p]), fabsf(v[2 * p + 1])));
-                }
-                float sfv;
-                nvfp4_block_scale(bmax, 1.0f, &sfv);
-                uint32_t o[8];
+            for (int p = 0; p < 8; ++p) {
+                v[2 * p] = bf16_bits_to_f32(raw[p] & 0xFFFFu);
+                v[2 * p + 1] = bf16_bits_to_f32(raw[p] >> 16);
+                bmax = fmaxf(bmax, fmaxf(fabsf(v[2 * p]), fabsf(v[2 * p + 1])));
+            }
+            float sfv;
+            nvfp4_block_scale(bmax, 1.0f, &sfv);
+            uint32_t o[8];
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    const __half2 hv = __floats2half2_rn(nvfp4_fake_quant(v[2 * p], sfv),
-                                                         nvfp4_fake_quant(v[2 * p + 1], sfv));
-                    o[p] = *reinterpret_cast<const uint32_t *>(&hv);
-                }
-                dst[2 * blk] = make_uint4(o[0], o[1], o[2], o[3]);
-                dst[2 * blk + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+            for (int p = 0; p < 8; ++p) {
+                const __half2 hv = __floats2half2_rn(nvfp4_fake_quant(v[2 * p], sfv),
+                                                     nvfp4_fake_quant(v[2 * p + 1], sfv));
+                o[p] = *reinterpret_cast<const uint32_t *>(&hv);
+            }
+            const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]);
+            const uint4 o1 = make_uint4(o[4], o[5], o[6], o[7]);
+            for (int k = 0; k < K; ++k) {
+                uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)rows[k] * H);
+                dst[2 * blk] = o0;
+                dst[2 * blk + 1] = o1;
             }
         }
     }
@@ -184,9 +191,9 @@ rows_kernel(const int32_t *__restrict__ ids, const int32_t *__restrict__ local_r
 }
 
 // out[t,:] = bf16( sum_{k=0..K-1} w[t,k] * y[row_of[t,k], :] ), FP32 FMA chain
-// in ascending k.
+// in ascending k over the bf16 expert outputs y.
 __global__ void __launch_bounds__(256)
-combine_kernel(const float *__restrict__ y, const float *__restrict__ w,
+combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ w,
                const int32_t *__restrict__ row_of, int T, int K, int H, uint16_t *__restrict__ out)
 {
     __shared__ float ws[32];
@@ -197,21 +204,28 @@ combine_kernel(const float *__restrict__ y, const float *__restrict__ w,
         rs[threadIdx.x] = row_of[(size_t)t * K + threadIdx.x];
     }
     __syncthreads();
-    const int nvec = H / 4;
+    const int nvec = H / 8;
     for (int i = threadIdx.x; i < nvec; i += 256) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            acc[j] = 0.0f;
         for (int k = 0; k < K; ++k) {
-            const float4 q = reinterpret_cast<const float4 *>(y + (size_t)rs[k] * H)[i];
+            const uint4 q = reinterpret_cast<const uint4 *>(y + (size_t)rs[k] * H)[i];
+            const uint32_t v[4] = {q.x, q.y, q.z, q.w};
             const float wk = ws[k];
-            acc.x = __fmaf_rn(wk, q.x, acc.x);
-            acc.y = __fmaf_rn(wk, q.y, acc.y);
-            acc.z = __fmaf_rn(wk, q.z, acc.z);
-            acc.w = __fmaf_rn(wk, q.w, acc.w);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[2 * j] = __fmaf_rn(wk, bf16_bits_to_f32(v[j] & 0xFFFFu), acc[2 * j]);
+                acc[2 * j + 1] = __fmaf_rn(wk, bf16_bits_to_f32(v[j] >> 16), acc[2 * j + 1]);
+            }
         }
-        uint2 o;
-        o.x = pack_bf16x2(acc.x, acc.y);
-        o.y = pack_bf16x2(acc.z, acc.w);
-        reinterpret_cast<uint2 *>(out + (size_t)t * H)[i] = o;
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        reinterpret_cast<uint4 *>(out + (size_t)t * H)[i] = o;
     }
 }
 
@@ -266,7 +280,7 @@ cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const float *y, const float *w, const int32_t *row_of, int T, int K,
+cudaError_t launch_combine(const uint16_t *y, const float *w, const int32_t *row_of, int T, int K,
                            int H, uint16_t *out, cudaStream_t s)
 {
     stage_begin(kStCombine, s);

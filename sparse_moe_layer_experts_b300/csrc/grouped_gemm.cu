@@ -16,7 +16,7 @@
 //            D_u[i, n] = sum_h Wu[e, m0+i, h] * Xp[row0+n, h]  (cols BN..2BN)
 //            h[row0+n, m0+i] = bf16( silu(D_g) * D_u )   in FP32
 //   down:    D[i, n]   = sum_j Wd[e, m0+i, j] * Hp[row0+n, j]
-//            y[row0+n, m0+i] = D                         (FP32)
+//            y[row0+n, m0+i] = bf16(D)   (the combine sums the K rows in FP32)
 //
 // Persistent kernel, one CTA per SM, warp-specialised:
 //   warp 0      TMA producer (one thread)
@@ -262,12 +262,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                                 silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j])));
                 } else {
                     tmem_ld_wait();
-                    float *out = static_cast<float *>(p.out);
+                    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         if (c0 + j < tl.nrows)
                             out[(size_t)(tl.row0 + c0 + j) * p.out_ld + col] =
-                                __uint_as_float(g[j]);
+                                __float2bfloat16_rn(__uint_as_float(g[j]));
                 }
             }
             tc_fence_before();
@@ -316,7 +316,7 @@ int gemm_chunk_rows(GemmVariant v)
 
 int gemm_box_rows(GemmVariant v)
 {
-    return v == GemmVariant::kDecode ? 16 : 64;
+    return v == GemmVariant::kDecode ? 16 : 128;
 }
 
 cudaError_t launch_gateup(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
@@ -324,7 +324,7 @@ cudaError_t launch_gateup(GemmVariant v, const CUtensorMap &wg, const CUtensorMa
 {
     if (v == GemmVariant::kDecode)
         return launch_variant<true, 32, 6, 2, 16, 1>(wg, wu, xp, a, grid, kStGateUp, s);
-    return launch_variant<true, 256, 3, 1, 64, 2>(wg, wu, xp, a, grid, kStGateUp, s);
+    return launch_variant<true, 256, 3, 1, 128, 2>(wg, wu, xp, a, grid, kStGateUp, s);
 }
 
 cudaError_t launch_down(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
@@ -332,7 +332,7 @@ cudaError_t launch_down(GemmVariant v, const CUtensorMap &wd, const CUtensorMap 
 {
     if (v == GemmVariant::kDecode)
         return launch_variant<false, 32, 10, 2, 16, 1>(wd, wd, hp, a, grid, kStDown, s);
-    return launch_variant<false, 256, 4, 2, 64, 2>(wd, wd, hp, a, grid, kStDown, s);
+    return launch_variant<false, 256, 4, 2, 128, 2>(wd, wd, hp, a, grid, kStDown, s);
 }
 
 }  // namespace beam

@@ -360,12 +360,12 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
                     }
                 } else {
                     tmem_ld_wait();
-                    float *out = static_cast<float *>(p.out);
+                    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         if (c0 + j < tl.nrows)
                             out[(size_t)(tl.row0 + c0 + j) * p.out_ld + col] =
-                                __fmul_rn(__uint_as_float(g[j]), g0);
+                                __float2bfloat16_rn(__fmul_rn(__uint_as_float(g[j]), g0));
                 }
             }
             tc_fence_before();
@@ -472,7 +472,7 @@ cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtens
 {
     if (v == GemmVariant::kDecode)
         return launch_fp4_variant<true, 32, 12, 3, 4, 2, 16, 1>(wg, wu, xp, a, f, grid, kStGateUp, s);
-    return launch_fp4_variant<true, 256, 6, 2, 3, 1, 64, 2>(wg, wu, xp, a, f, grid, kStGateUp, s);
+    return launch_fp4_variant<true, 256, 6, 2, 3, 1, 128, 2>(wg, wu, xp, a, f, grid, kStGateUp, s);
 }
 
 cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
@@ -480,7 +480,7 @@ cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensor
 {
     if (v == GemmVariant::kDecode)
         return launch_fp4_variant<false, 32, 16, 4, 6, 2, 16, 1>(wd, wd, hp, a, f, grid, kStDown, s);
-    return launch_fp4_variant<false, 256, 10, 2, 4, 2, 64, 2>(wd, wd, hp, a, f, grid, kStDown, s);
+    return launch_fp4_variant<false, 256, 10, 2, 4, 2, 128, 2>(wd, wd, hp, a, f, grid, kStDown, s);
 }
 
 }  // namespace beam

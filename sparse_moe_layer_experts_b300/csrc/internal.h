@@ -50,7 +50,7 @@ cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t 
 cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int32_t *cta_base,
                         const int32_t *offsets, int T, int K, int E, int32_t *row_of,
                         cudaStream_t s);
-cudaError_t launch_combine(const float *y, const float *w, const int32_t *row_of, int T, int K,
+cudaError_t launch_combine(const uint16_t *y, const float *w, const int32_t *row_of, int T, int K,
                            int H, uint16_t *out, cudaStream_t s);
 
 // ---- grouped_gemm.cu
@@ -60,7 +60,7 @@ struct GemmArgs {
     int E;
     int m_tiles;    // weight rows per expert / 128
     int ksteps;     // reduction length / 64
-    void *out;      // gate/up: h bf16 [R, ld]; down: y fp32 [R, ld]
+    void *out;      // gate/up: h [R, ld] (bf16, or fp16 for NVFP4); down: y bf16 [R, ld]
     int out_ld;
     int *status;
     unsigned long long timeout_ns;
@@ -88,7 +88,7 @@ int gemm_box_rows(GemmVariant v);
 // h = silu(x_perm . Wg^T) * (x_perm . Wu^T) per expert segment (bf16 out)
 cudaError_t launch_gateup(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
                           const CUtensorMap &xp, const GemmArgs &a, int grid, cudaStream_t s);
-// y = h . Wd^T per expert segment (fp32 out)
+// y = h . Wd^T per expert segment (bf16 out)
 cudaError_t launch_down(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
                         const GemmArgs &a, int grid, cudaStream_t s);
 

@@ -64,8 +64,8 @@ def test_beam_defaults_and_workspace_size(L):
     s32 = B.beam_moe_workspace_size(32, c)
     s64 = B.beam_moe_workspace_size(64, c)
     assert 0 < s32 < s64
-    # x_perm (bf16) + h (bf16) + y (fp32) dominate: 8 rows per token
-    assert s64 - s32 >= 32 * 8 * (5120 * 2 + 2560 * 2 + 5120 * 4)
+    # x_perm (bf16) + h (bf16) + y (bf16) dominate: 8 rows per token
+    assert s64 - s32 >= 32 * 8 * (5120 * 2 + 2560 * 2 + 5120 * 2)
     assert B.beam_moe_hostio_extra_bytes(32, c) >= 2 * 32 * 5120 * 2
 
 

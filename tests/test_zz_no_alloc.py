@@ -59,7 +59,7 @@ def test_noalloc_rejects_batches_beyond_its_scratch():
     c = B.beam_moe_cfg()
     B.beam_moe_cfg_init_beam(c)
     before = B.beam_moe_launch_count()
-    # 128 Beam tokens need ~35 MiB of scratch, above the 24 MiB array
+    # 128 Beam tokens need ~25 MiB of scratch, above the 24 MiB array
     rc = B.beam_moe_forward_noalloc(16, 16, 16, 16, 16, 128, c, 16, None)
     assert rc == B.BEAM_MOE_ERR_WORKSPACE
     c.top_k = 0
