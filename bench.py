@@ -57,6 +57,9 @@ def parse_args():
                     help="tokens of the batch the CPU oracle baseline computes")
     ap.add_argument("--override", default="",
                     help="shape overrides for profiling runs, e.g. T=512,E=32 (not a bench line)")
+    ap.add_argument("--route-only", action="store_true",
+                    help="profiling mode: time only the routing kernels (no expert weights "
+                         "are allocated); prints a diagnostic line, not a bench line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -461,8 +464,49 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_route_only(args):
+    """Diagnostic: the routing kernels alone on the configured batch."""
+    import torch
+    from sparse_moe_layer_experts_b300 import binding as B
+    from sparse_moe_layer_experts_b300 import build as build_mod
+    from sparse_moe_layer_experts_b300 import synth
+    from sparse_moe_layer_experts_b300.layer import BeamMoE
+    build_mod.build()
+    sh = synth.shape(args.config, **parse_override(args.override))
+    d = synth.make_inputs(sh, seed=0, device="cuda", weights=False)
+    w = torch.zeros(1, dtype=torch.bfloat16, device="cuda")
+    layer = BeamMoE.__new__(BeamMoE)
+    layer._setup(d["router_w"], w, w, w, sh.E, sh.I, sh.H, sh.G, sh.topk_groups, sh.top_k,
+                 sh.scale, 0, 0)
+    for _ in range(args.warmup):
+        layer.route(d["x"], want_scores=False)
+    torch.cuda.synchronize()
+    names = B.KERNEL_STAGES[:4]
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in names] for _ in range(args.steps)]
+    for pair in ev:
+        for e0, e1 in pair:
+            e0.record()
+            e1.record()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        B.check(B.beam_moe_set_kernel_events([e[0].cuda_event for e in ev[i]],
+                                             [e[1].cuda_event for e in ev[i]]), "events")
+        layer.route(d["x"], want_scores=False)
+    torch.cuda.synchronize()
+    B.beam_moe_set_kernel_events([], [])
+    ms = {n: sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps)) / args.steps
+          for j, n in enumerate(names)}
+    gflop = 2 * sh.T * sh.H * sh.E / 1e9
+    print(json.dumps({"route_only": True, "config": args.config, "T": sh.T, "kernels_ms": ms,
+                      "router_tflops": gflop / ms["router_scores"]}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.route_only:
+        run_route_only(args)
+        return
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -129,7 +129,8 @@ router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr
         const int b = kc & 1;
         if (kc + 1 < nk)
             gload((kc + 1) * kLKC);
-#pragma unroll
+        // a partial unroll keeps the 8x8 tile free of register spills
+#pragma unroll 4
         for (int k = 0; k < kLKC; ++k) {
             float a[R], bb[R];
 #pragma unroll
