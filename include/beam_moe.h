@@ -242,10 +242,11 @@ int64_t beam_moe_launch_count(void);
  * library launches from the calling host thread is bracketed by
  * cudaEventRecord(start[i]) and cudaEventRecord(stop[i]) on its stream, i
  * being the kernel's stage: 0 router scores, 1 selection, 2 histogram,
- * 3 scan, 4 permute, 5 gate/up GEMM, 6 down GEMM, 7 combine.  Events are
- * cudaEvent_t handles passed as void*, owned by the caller and alive while
- * set; n = 0 turns the hook off.  Returns BEAM_MOE_ERR_INVALID_ARG for
- * n < 0, n > 8 or NULL arrays.
+ * 3 scan, 4 permute, 5 gate/up GEMM, 6 down GEMM, 7 combine, 8 NVFP4
+ * quantisation of h (NVFP4 layers only).  Events are cudaEvent_t handles
+ * passed as void*, owned by the caller and alive while set; n = 0 turns the
+ * hook off.  Returns BEAM_MOE_ERR_INVALID_ARG for n < 0, n > 9 or NULL
+ * arrays.
  */
 int beam_moe_set_kernel_events(void *const *start, void *const *stop, int n);
 

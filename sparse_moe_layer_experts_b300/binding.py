@@ -154,7 +154,7 @@ def beam_moe_set_kernel_events(starts, stops) -> int:
 
 
 KERNEL_STAGES = ("router_scores", "select", "hist", "scan", "permute", "gateup_gemm",
-                 "down_gemm", "combine")
+                 "down_gemm", "combine", "quantize_h")
 
 
 def beam_moe_device_sms() -> int:

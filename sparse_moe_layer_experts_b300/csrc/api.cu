@@ -40,7 +40,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
     size_t status, scores, ids, wts, local_rank, cta_counts, cta_base, counts, offsets,
-        chunk_start, row_of, row_src, x_perm, h, y, total;
+        chunk_start, row_of, row_src, x_perm, h, h_raw, y, total;
 };
 
 Layout make_layout(int64_t T, const beam_moe_cfg &c)
@@ -69,6 +69,7 @@ Layout make_layout(int64_t T, const beam_moe_cfg &c)
     L.row_src = take(sizeof(int32_t) * R);
     L.x_perm = take(2 * R * H);
     L.h = take(2 * R * I);
+    L.h_raw = take(c.wtype == BEAM_MOE_W_NVFP4 ? 4 * R * I : 0);  // FP32 h before quantisation
     L.y = take(2 * R * H);
     L.total = o;
     return L;
@@ -267,7 +268,9 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     if (fp4) {
         Fp4Weights f{static_cast<const uint8_t *>(c.w_gate_sf),
                      static_cast<const uint8_t *>(c.w_up_sf), c.w_gate_gs, c.w_up_gs};
+        a.out = at<void>(ws, L.h_raw);
         BEAM_CUDA(launch_gateup_fp4(v, m_wg, m_wu, m_xp, a, f, sms, s));
+        BEAM_CUDA(launch_quantize_rows(at<float>(ws, L.h_raw), R, I, at<uint16_t>(ws, L.h), s));
     } else {
         BEAM_CUDA(launch_gateup(v, m_wg, m_wu, m_xp, a, sms, s));
     }

@@ -176,6 +176,42 @@ permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
     }
 }
 
+// NVFP4 activation quantisation of an FP32 matrix [rows, cols] (scale 1 per
+// 16-element block): writes the exact FP16 values q * sf.  One thread per block.
+__global__ void __launch_bounds__(256)
+quantize_rows_kernel(const float *__restrict__ in, int64_t n_blocks, uint16_t *__restrict__ out)
+{
+    const int64_t b = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (b >= n_blocks)
+        return;
+    const float4 *src = reinterpret_cast<const float4 *>(in) + 4 * b;
+    float v[16];
+    float bmax = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 f = src[q];
+        v[4 * q] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        bmax = fmaxf(bmax, fabsf(v[i]));
+    float sfv;
+    nvfp4_block_scale(bmax, 1.0f, &sfv);
+    uint32_t o[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const __half2 hv = __floats2half2_rn(nvfp4_fake_quant(v[2 * p], sfv),
+                                             nvfp4_fake_quant(v[2 * p + 1], sfv));
+        o[p] = *reinterpret_cast<const uint32_t *>(&hv);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(out) + 2 * b;
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 __global__ void __launch_bounds__(256)
 rows_kernel(const int32_t *__restrict__ ids, const int32_t *__restrict__ local_rank,
             const int32_t *__restrict__ cta_base, const int32_t *__restrict__ offsets, int T, int K,
@@ -277,6 +313,16 @@ cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int
     rows_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ids, local_rank, cta_base, offsets, T,
                                                              K, E, row_of);
     stage_end(kStPermute, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows(const float *in, int64_t rows, int cols, uint16_t *out,
+                                 cudaStream_t s)
+{
+    const int64_t n_blocks = rows * (int64_t)(cols / 16);
+    stage_begin(kStQuantH, s);
+    quantize_rows_kernel<<<(unsigned)((n_blocks + 255) / 256), 256, 0, s>>>(in, n_blocks, out);
+    stage_end(kStQuantH, s);
     return cudaGetLastError();
 }
 

@@ -11,8 +11,9 @@
 // FP16 values q*sf, which are exact because they need at most 6 significant
 // bits.  The tensor cores then run the same kind::f16 MMA as the bf16 path:
 // activations are FP16 too, holding the exact NVFP4 values of x (quantised in
-// the permute kernel) and of h (quantised here, in the gate/up epilogue).  The
-// global scale multiplies the FP32 accumulator in the epilogue.
+// the permute kernel) and of h (the gate/up epilogue writes h in FP32 and a
+// streaming pass quantises it).  The global scale multiplies the FP32
+// accumulator in the epilogue.
 //
 // Warp roles:
 //   warp 0      producer: TMA of the code tile + bulk copy of its 512 scale
@@ -344,20 +345,15 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
                     uint32_t u[16];
                     tmem_ld16(ta + BN + c0, u);
                     tmem_ld_wait();
-                    __half *out = static_cast<__half *>(p.out);
+                    // h = silu(g) * u, kept in FP32 for a separate pass that
+                    // quantises it to NVFP4 before the down GEMM
+                    float *out = static_cast<float *>(p.out);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float h = silu_mul_f(__fmul_rn(__uint_as_float(g[j]), g0),
-                                                   __fmul_rn(__uint_as_float(u[j]), g1));
-                        // NVFP4 block of 16 consecutive rows = 16 lanes
-                        float bmax = fabsf(h);
-#pragma unroll
-                        for (int off = 8; off > 0; off >>= 1)
-                            bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, off));
+                    for (int j = 0; j < 16; ++j)
                         if (c0 + j < tl.nrows)
                             out[(size_t)(tl.row0 + c0 + j) * p.out_ld + col] =
-                                __float2half_rn(nvfp4_fake_quant_fast(h, bmax));
-                    }
+                                silu_mul_f(__fmul_rn(__uint_as_float(g[j]), g0),
+                                           __fmul_rn(__uint_as_float(u[j]), g1));
                 } else {
                     tmem_ld_wait();
                     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);

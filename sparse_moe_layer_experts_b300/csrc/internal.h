@@ -18,6 +18,7 @@ enum Stage {
     kStGateUp,
     kStDown,
     kStCombine,
+    kStQuantH,  // NVFP4 layers only: quantise h before the down GEMM
     kNumStages
 };
 // Bracket one kernel launch: records the calling thread's timing events for
@@ -50,6 +51,9 @@ cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t 
 cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int32_t *cta_base,
                         const int32_t *offsets, int T, int K, int E, int32_t *row_of,
                         cudaStream_t s);
+// NVFP4 activations: FP32 [rows, cols] -> FP16 holding q * sf (16-blocks, scale 1)
+cudaError_t launch_quantize_rows(const float *in, int64_t rows, int cols, uint16_t *out,
+                                 cudaStream_t s);
 cudaError_t launch_combine(const uint16_t *y, const float *w, const int32_t *row_of, int T, int K,
                            int H, uint16_t *out, cudaStream_t s);
 
@@ -60,7 +64,7 @@ struct GemmArgs {
     int E;
     int m_tiles;    // weight rows per expert / 128
     int ksteps;     // reduction length / 64
-    void *out;      // gate/up: h [R, ld] (bf16, or fp16 for NVFP4); down: y bf16 [R, ld]
+    void *out;      // gate/up: h bf16 [R, ld] (NVFP4: FP32); down: y bf16 [R, ld]
     int out_ld;
     int *status;
     unsigned long long timeout_ns;

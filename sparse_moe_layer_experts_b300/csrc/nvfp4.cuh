@@ -79,15 +79,4 @@ __device__ __forceinline__ float nvfp4_fake_quant(float v, float sfv)
     return e2m1_value(e2m1_code(__fdiv_rn(v, sfv))) * sfv;
 }
 
-// The same quantise-dequantise with reciprocal multiplies in place of the
-// two IEEE divisions (for h, an intermediate the oracle computes in its own
-// rounding anyway): bmax is the block's largest magnitude.
-__device__ __forceinline__ float nvfp4_fake_quant_fast(float v, float bmax)
-{
-    const float sfv = e4m3_value(e4m3_code(bmax * (1.0f / 6.0f)));
-    if (sfv == 0.0f)
-        return 0.0f;
-    return e2m1_value(e2m1_code(v * __frcp_rn(sfv))) * sfv;
-}
-
 }  // namespace beam
