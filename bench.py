@@ -169,7 +169,7 @@ KERNEL_SOURCES = {
     "permute": ("dispatch.cu", "common.cuh", "nvfp4.cuh"),
     "combine": ("dispatch.cu", "common.cuh"),
     "gateup_gemm": ("grouped_gemm.cu", "gemm_common.cuh", "common.cuh"),
-    "down_gemm": ("grouped_gemm.cu", "gemm_common.cuh", "common.cuh"),
+    "down_gemm": ("grouped_gemm.cu", "grouped_gemm_pair.cu", "gemm_common.cuh", "common.cuh"),
 }
 FP4_GEMM_SOURCES = ("grouped_gemm_fp4.cu", "gemm_common.cuh", "common.cuh", "nvfp4.cuh")
 

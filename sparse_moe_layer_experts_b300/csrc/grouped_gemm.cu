@@ -332,6 +332,8 @@ cudaError_t launch_down(GemmVariant v, const CUtensorMap &wd, const CUtensorMap 
 {
     if (v == GemmVariant::kDecode)
         return launch_variant<false, 32, 10, 2, 16, 1>(wd, wd, hp, a, grid, kStDown, s);
+    if (a.m_tiles % 2 == 0)
+        return launch_down_pair(wd, hp, a, grid, s);
     return launch_variant<false, 256, 4, 2, 128, 2>(wd, wd, hp, a, grid, kStDown, s);
 }
 

@@ -96,6 +96,12 @@ cudaError_t launch_gateup(GemmVariant v, const CUtensorMap &wg, const CUtensorMa
 cudaError_t launch_down(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
                         const GemmArgs &a, int grid, cudaStream_t s);
 
+// ---- grouped_gemm_pair.cu: the prefill-size down GEMM on CTA pairs with the
+// 2-SM MMA (weight tiles of 256 rows; needs an even a.m_tiles and 128-row
+// token boxes in the B map)
+cudaError_t launch_down_pair(const CUtensorMap &wd, const CUtensorMap &hp, const GemmArgs &a,
+                             int grid, cudaStream_t s);
+
 // ---- grouped_gemm_fp4.cu: the same GEMMs with NVFP4 weights (codes via
 // TMA maps of the packed bytes) and FP16 activations; gate/up quantises h.
 cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
