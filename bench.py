@@ -203,10 +203,13 @@ def ncu_traffic(kernel: str, workload: str):
 def workload_algorithmic(sh, n_active: int, nvfp4: bool = False):
     """Algorithmic bytes / FLOPs per launch of each kernel (compulsory traffic
     of the kernel's own inputs and outputs; expert weights of active experts
-    only).  NVFP4 weights: 0.5 B per code + 1/16 B of block scale."""
+    only).  NVFP4 weights and activations: 0.5 B per code + 1/16 B of block
+    scale; NVFP4 h leaves gate/up in FP32 for the quantize_h pass."""
     T, H, I, E, K = sh.T, sh.H, sh.I, sh.E, sh.top_k
     R = T * K
     wb = 0.5625 if nvfp4 else 2
+    ab = 0.5625 if nvfp4 else 2  # activation operand bytes per element
+    hb = 4 if nvfp4 else 2       # h as written by gate/up
     w_gu = int(n_active * 2 * I * H * wb)
     w_d = int(n_active * H * I * wb)
     return {
@@ -214,11 +217,11 @@ def workload_algorithmic(sh, n_active: int, nvfp4: bool = False):
         "select": dict(bytes=T * E * 4 + R * 8, flops=0),
         "hist": dict(bytes=R * 8 + ((T + 255) // 256) * E * 4, flops=0),
         "scan": dict(bytes=((T + 255) // 256) * E * 8, flops=0),
-        "permute": dict(bytes=T * H * 2 + R * H * 2, flops=0),
-        "gateup_gemm": dict(bytes=w_gu + R * H * 2 + R * I * 2, flops=2 * R * H * 2 * I),
-        "down_gemm": dict(bytes=w_d + R * I * 2 + R * H * 2, flops=2 * R * I * H),
+        "permute": dict(bytes=int(T * H * 2 + R * H * ab), flops=0),
+        "gateup_gemm": dict(bytes=int(w_gu + R * H * ab + R * I * hb), flops=2 * R * H * 2 * I),
+        "down_gemm": dict(bytes=int(w_d + R * I * ab + R * H * 2), flops=2 * R * I * H),
         "combine": dict(bytes=R * H * 2 + T * H * 2 + R * 8, flops=2 * R * H),
-        "quantize_h": dict(bytes=R * I * 6, flops=0),
+        "quantize_h": dict(bytes=int(R * I * (4 + 0.5625)), flops=0),
         "layer": dict(bytes=w_gu + w_d + H * E * 4 + 2 * T * H * 2,
                       flops=2 * T * H * E + 6 * R * H * I),
     }
@@ -406,16 +409,19 @@ def run_ours(args, world, rank, local):
 
     value = world * sh.T * args.steps / (ms_max / 1e3)
     peaks, peak_src = load_peaks()
+    # tensor peak of the path's MMA type: bf16, or FP4 (measured bf16 x the
+    # nominal fp4/bf16 ratio)
+    t_peak = peaks["bf16_tflops"] * (NVFP4_OVER_BF16 if nvfp4 else 1.0)
     alg = workload_algorithmic(sh, n_active, nvfp4)
     dom = max(per_kernel_ms, key=per_kernel_ms.get)
     a = alg[dom]
     t_dom = per_kernel_ms[dom] / 1e3
     t_bw = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_fl = a["flops"] / (peaks["bf16_tflops"] * 1e12) if a["flops"] else 0.0
+    t_fl = a["flops"] / (t_peak * 1e12) if a["flops"] else 0.0
     if t_fl > t_bw:
         achieved = a["flops"] / t_dom / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
+        roof = {"bound": "tensor", "achieved": achieved, "peak": t_peak,
+                "unit": "TFLOP/s", "frac": achieved / t_peak}
     else:
         achieved = a["bytes"] / t_dom / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -424,15 +430,17 @@ def run_ours(args, world, rank, local):
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else \
         "fallback"
+    if nvfp4 and roof["bound"] == "tensor":
+        roof["peak_source"] += ", bf16 x 13.5/2.25 (nominal dense fp4/bf16)"
     roof["algorithmic_bytes_per_launch"] = a["bytes"]
     roof["algorithmic_flops_per_launch"] = a["flops"]
     lay = alg["layer"]
     t_step = ms_max / args.steps / 1e3
     layer_roof = {
         "hbm_frac": lay["bytes"] / t_step / 1e9 / peaks["hbm_gbs"],
-        "tensor_frac": lay["flops"] / t_step / 1e12 / peaks["bf16_tflops"],
+        "tensor_frac": lay["flops"] / t_step / 1e12 / t_peak,
         "attainable_frac": max(lay["bytes"] / (peaks["hbm_gbs"] * 1e9),
-                               lay["flops"] / (peaks["bf16_tflops"] * 1e12)) / t_step,
+                               lay["flops"] / (t_peak * 1e12)) / t_step,
     }
 
     cpu = None
@@ -446,7 +454,7 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "nvfp4 weights+activations, f16 MMA, f32 accumulate" if nvfp4 else "bf16",
+            "dtype": "nvfp4 weights+activations, fp4 MMA (kind::mxf4nvf4), f32 accumulate" if nvfp4 else "bf16",
             "data": "synthetic (seeded N(0,1) activations, N(0,0.02) bf16 weights)",
             "config": {"workload": f"{args.config}{'(' + args.override + ')' if args.override else ''}: T={sh.T} tokens, hidden {sh.H}, "
                                    f"intermediate {sh.I}, {sh.E} experts in {sh.G} groups, "

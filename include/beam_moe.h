@@ -146,7 +146,8 @@ int beam_moe_route(const void *x, const float *router_w, int64_t T,
  * cfg->w_*_sf / cfg->w_*_gs point at the matching block and global scales
  * (16-byte aligned).  The activations are then quantised to NVFP4 as well
  * (16-element blocks, global scale 1): x before the gate/up GEMM, h before
- * the down GEMM.  The router stays FP32 on the bf16 x.
+ * the down GEMM, and both expert GEMMs run on the FP4 tensor cores with
+ * FP32 accumulation.  The router stays FP32 on the bf16 x.
  * Deterministic: the same inputs give bitwise the same output.
  */
 int beam_moe_forward(const void *x, const float *router_w, const void *w_gate,
@@ -209,10 +210,12 @@ int beam_moe_forward_noalloc(const void *x, const float *router_w,
  *   w        [n_mat, rows, cols] bf16, device; rows % 128 == 0, cols % 64 == 0
  *   packed   [n_mat, rows, cols/2] uint8, device, out (two codes per byte,
  *            element 2j in the low nibble, bit 3 of a code = sign)
- *   block_sf [n_mat, rows/128, cols/64, 128, 4] uint8, device, out (E4M3
- *            bits): the scale of elements [16b, 16b+16) of row r is entry
- *            (r % 128, b % 4) of tile (r / 128, b / 4), so the 512 scales of
- *            one 128 x 64 weight tile are contiguous
+ *   block_sf [n_mat, rows/128, cols/64, 512] uint8, device, out (E4M3
+ *            bits): the scale of elements [16b, 16b+16) of row r is byte
+ *            16*(r % 32) + 4*((r % 128) / 32) + b % 4 of tile
+ *            (r / 128, b / 4), so the 512 scales of one 128 x 64 weight tile
+ *            are contiguous, rows in the order the FP4 tensor cores' scale
+ *            copy takes them
  *   global_sf[n_mat] fp32, device, out
  * Recipe (the pages name the format only: "most parameters in 4 bits"; the
  * recipe is a reading): gs = amax|W| / (6*448) per matrix (1 if all zero);

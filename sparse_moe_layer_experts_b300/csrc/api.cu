@@ -40,8 +40,21 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
     size_t status, scores, ids, wts, local_rank, cta_counts, cta_base, counts, offsets,
-        chunk_start, row_of, row_src, x_perm, h, h_raw, y, total;
+        chunk_start, row_of, row_src, x_perm, h, h_raw, y, row_pos, x_sf, h_sf, total;
 };
+
+GemmVariant pick_variant(int64_t T, const beam_moe_cfg &c)
+{
+    // decode: a handful of tokens per active expert
+    return (T * c.top_k <= 16LL * c.n_experts) ? GemmVariant::kDecode : GemmVariant::kPrefill;
+}
+
+// Rows per token chunk (the N tile of the grouped GEMMs).
+int chunk_rows(int64_t T, const beam_moe_cfg &c)
+{
+    const GemmVariant v = pick_variant(T, c);
+    return c.wtype == BEAM_MOE_W_NVFP4 ? fp4_chunk_rows(v) : gemm_chunk_rows(v);
+}
 
 Layout make_layout(int64_t T, const beam_moe_cfg &c)
 {
@@ -67,10 +80,19 @@ Layout make_layout(int64_t T, const beam_moe_cfg &c)
     L.chunk_start = take(sizeof(int32_t) * (E + 1));
     L.row_of = take(sizeof(int32_t) * R);
     L.row_src = take(sizeof(int32_t) * R);
-    L.x_perm = take(2 * R * H);
-    L.h = take(2 * R * I);
-    L.h_raw = take(c.wtype == BEAM_MOE_W_NVFP4 ? 4 * R * I : 0);  // FP32 h before quantisation
+    const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4;
+    // activations: bf16 rows, or NVFP4 codes (2 per byte)
+    L.x_perm = take(fp4 ? R * H / 2 : 2 * R * H);
+    L.h = take(fp4 ? R * I / 2 : 2 * R * I);
+    L.h_raw = take(fp4 ? 4 * R * I : 0);  // FP32 h before quantisation
     L.y = take(2 * R * H);
+    // NVFP4: chunk*128 + position of each row, and the activations' scales
+    // in token-chunk atoms [chunk, K/64, 512]
+    const int64_t cr = chunk_rows(T, c);
+    const int64_t chunks = fp4 ? (R + cr - 1) / cr + E : 0;
+    L.row_pos = take(fp4 ? 4 * R : 0);
+    L.x_sf = take((size_t)chunks * (H / 64) * 512);
+    L.h_sf = take((size_t)chunks * (I / 64) * 512);
     L.total = o;
     return L;
 }
@@ -164,11 +186,13 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
     return make_map_2d(m, base, dtype, 2, inner, outer, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Packed E2M1 codes [outer rows, inner/2 bytes], box [128 rows, 32 bytes].
-bool make_code_map(CUtensorMap *m, const void *base, uint64_t inner_elems, uint64_t outer)
+// Packed E2M1 codes [outer rows, inner/2 bytes], box [box_outer rows, 128
+// bytes = 256 elements] with the 128-byte swizzle; zero fill past the row end.
+bool make_code_map(CUtensorMap *m, const void *base, uint64_t inner_elems, uint64_t outer,
+                   uint32_t box_outer)
 {
-    return make_map_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, inner_elems / 2, outer, 32, 128,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    return make_map_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, inner_elems / 2, outer, 128,
+                       box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int device_sms()
@@ -181,11 +205,6 @@ int device_sms()
     return n;
 }
 
-GemmVariant pick_variant(int64_t T, const beam_moe_cfg &c)
-{
-    // decode: a handful of tokens per active expert
-    return (T * c.top_k <= 16LL * c.n_experts) ? GemmVariant::kDecode : GemmVariant::kPrefill;
-}
 
 #define BEAM_CUDA(call)                          \
     do {                                         \
@@ -219,35 +238,44 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     const Layout L = make_layout(T, c);
     void *ws = c.workspace;
     const GemmVariant v = pick_variant(T, c);
-    const int chunk = gemm_chunk_rows(v);
     int rc = run_route(x, router_w, T, c, L, at<float>(ws, L.scores), at<int32_t>(ws, L.ids),
-                       at<float>(ws, L.wts), chunk, s);
+                       at<float>(ws, L.wts), chunk_rows(T, c), s);
     if (rc != BEAM_MOE_OK)
         return rc;
     const int K = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
     const int64_t R = T * K;
     const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4;
-    BEAM_CUDA(launch_permute(static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids),
-                             at<int32_t>(ws, L.local_rank), at<int32_t>(ws, L.cta_base),
-                             at<int32_t>(ws, L.offsets), (int)T, K, E, H, at<int32_t>(ws, L.row_of),
-                             at<int32_t>(ws, L.row_src), at<uint16_t>(ws, L.x_perm), fp4, s));
+    if (fp4)
+        BEAM_CUDA(launch_permute_nvfp4(
+            static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids), at<int32_t>(ws, L.local_rank),
+            at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start),
+            (int)T, K, E, H, at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.row_src),
+            at<int32_t>(ws, L.row_pos), at<uint8_t>(ws, L.x_perm), at<uint8_t>(ws, L.x_sf), s));
+    else
+        BEAM_CUDA(launch_permute(static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids),
+                                 at<int32_t>(ws, L.local_rank), at<int32_t>(ws, L.cta_base),
+                                 at<int32_t>(ws, L.offsets), (int)T, K, E, H,
+                                 at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.row_src),
+                                 at<void>(ws, L.x_perm), s));
 
-    // activations: bf16, or the exact FP16 values of their NVFP4 quantisation
-    const CUtensorMapDataType act =
-        fp4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap m_wg, m_wu, m_wd, m_xp, m_h;
     bool maps_ok;
-    if (fp4)
-        maps_ok = make_code_map(&m_wg, w_gate, H, (uint64_t)E * I) &&
-                  make_code_map(&m_wu, w_up, H, (uint64_t)E * I) &&
-                  make_code_map(&m_wd, w_down, I, (uint64_t)E * H);
-    else
+    if (fp4) {
+        const uint32_t box = (uint32_t)fp4_box_rows(v);
+        maps_ok = make_code_map(&m_wg, w_gate, H, (uint64_t)E * I, 128) &&
+                  make_code_map(&m_wu, w_up, H, (uint64_t)E * I, 128) &&
+                  make_code_map(&m_wd, w_down, I, (uint64_t)E * H, 128) &&
+                  make_code_map(&m_xp, at<void>(ws, L.x_perm), H, (uint64_t)R, box) &&
+                  make_code_map(&m_h, at<void>(ws, L.h), I, (uint64_t)R, box);
+    } else {
+        const uint32_t box = (uint32_t)gemm_box_rows(v);
         maps_ok = make_map(&m_wg, w_gate, H, (uint64_t)E * I, 128) &&
                   make_map(&m_wu, w_up, H, (uint64_t)E * I, 128) &&
-                  make_map(&m_wd, w_down, I, (uint64_t)E * H, 128);
-    const uint32_t box = (uint32_t)gemm_box_rows(v);
-    if (!maps_ok || !make_map(&m_xp, at<void>(ws, L.x_perm), H, (uint64_t)R, box, act) ||
-        !make_map(&m_h, at<void>(ws, L.h), I, (uint64_t)R, box, act))
+                  make_map(&m_wd, w_down, I, (uint64_t)E * H, 128) &&
+                  make_map(&m_xp, at<void>(ws, L.x_perm), H, (uint64_t)R, box) &&
+                  make_map(&m_h, at<void>(ws, L.h), I, (uint64_t)R, box);
+    }
+    if (!maps_ok)
         return BEAM_MOE_ERR_CUDA;
 
     const int sms = device_sms();
@@ -267,10 +295,12 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     a.out_ld = I;
     if (fp4) {
         Fp4Weights f{static_cast<const uint8_t *>(c.w_gate_sf),
-                     static_cast<const uint8_t *>(c.w_up_sf), c.w_gate_gs, c.w_up_gs};
+                     static_cast<const uint8_t *>(c.w_up_sf), c.w_gate_gs, c.w_up_gs,
+                     at<uint8_t>(ws, L.x_sf)};
         a.out = at<void>(ws, L.h_raw);
-        BEAM_CUDA(launch_gateup_fp4(v, m_wg, m_wu, m_xp, a, f, sms, s));
-        BEAM_CUDA(launch_quantize_rows(at<float>(ws, L.h_raw), R, I, at<uint16_t>(ws, L.h), s));
+        BEAM_CUDA(launch_gateup_fp4(v, m_wg, m_wu, m_xp, a, f, H / 64, sms, s));
+        BEAM_CUDA(launch_quantize_rows(at<float>(ws, L.h_raw), R, I, at<int32_t>(ws, L.row_pos),
+                                       at<uint8_t>(ws, L.h), at<uint8_t>(ws, L.h_sf), s));
     } else {
         BEAM_CUDA(launch_gateup(v, m_wg, m_wu, m_xp, a, sms, s));
     }
@@ -281,8 +311,9 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     a.out_ld = H;
     a.debug_flags = 0;
     if (fp4) {
-        Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, c.w_down_gs, nullptr};
-        BEAM_CUDA(launch_down_fp4(v, m_wd, m_h, a, f, sms, s));
+        Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, c.w_down_gs, nullptr,
+                     at<uint8_t>(ws, L.h_sf)};
+        BEAM_CUDA(launch_down_fp4(v, m_wd, m_h, a, f, I / 64, sms, s));
     } else {
         BEAM_CUDA(launch_down(v, m_wd, m_h, a, sms, s));
     }
@@ -348,7 +379,7 @@ int beam_moe_route(const void *x, const float *router_w, int64_t T, const beam_m
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *ws = c.workspace;
     float *sc = scores ? scores : at<float>(ws, L.scores);
-    rc = run_route(x, router_w, T, c, L, sc, topk_ids, topk_w, gemm_chunk_rows(pick_variant(T, c)),
+    rc = run_route(x, router_w, T, c, L, sc, topk_ids, topk_w, chunk_rows(T, c),
                    s);
     if (rc != BEAM_MOE_OK)
         return rc;

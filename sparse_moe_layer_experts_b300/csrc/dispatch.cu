@@ -114,79 +114,101 @@ scan_kernel(const int32_t *__restrict__ cta_counts, int n_cta, int E, int chunk_
 
 // CTA per token: place the token's K rows, then read the token's activations
 // once (16-byte vectors) and write them to all K rows.  With QUANT (NVFP4
-// layers) each 16-element block is quantised to NVFP4 (scale 1) once and the
-// exact FP16 values q * sf are written.
+// layers) each 16-element block is quantised to NVFP4 (global scale 1) once:
+// its 8 code bytes go to every row, its E4M3 scale into the row's token-chunk
+// scale atom, and row_pos records (chunk * 128 + position) for the pass that
+// quantises h.
 template <bool QUANT>
 __global__ void __launch_bounds__(256)
 permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
                const int32_t *__restrict__ local_rank, const int32_t *__restrict__ cta_base,
-               const int32_t *__restrict__ offsets, int T, int K, int E, int H,
-               int32_t *__restrict__ row_of, int32_t *__restrict__ row_src,
-               uint16_t *__restrict__ x_perm)
+               const int32_t *__restrict__ offsets, const int32_t *__restrict__ chunk_start,
+               int T, int K, int E, int H, int32_t *__restrict__ row_of,
+               int32_t *__restrict__ row_src, int32_t *__restrict__ row_pos,
+               void *__restrict__ x_perm, uint8_t *__restrict__ x_sf)
 {
     __shared__ int rows[32];
+    __shared__ int pos[32];
     const int t = blockIdx.x;
     const int cta = t / kHistTokens;
     if (threadIdx.x < K) {
         const int k = threadIdx.x;
         int e = ids[(size_t)t * K + k];
         e = (e < 0 || e >= E) ? 0 : e;
-        const int row = offsets[e] + cta_base[(size_t)cta * E + e] + local_rank[(size_t)t * K + k];
+        const int rank = cta_base[(size_t)cta * E + e] + local_rank[(size_t)t * K + k];
+        const int row = offsets[e] + rank;
         rows[k] = row;
         row_of[(size_t)t * K + k] = row;
         row_src[row] = t;
+        if constexpr (QUANT) {
+            int j;
+            const int c = nvfp4_chunk_of_row(rank, offsets[e + 1] - offsets[e],
+                                             chunk_start[e + 1] - chunk_start[e], &j);
+            pos[k] = (chunk_start[e] + c) * 128 + j;
+            row_pos[row] = pos[k];
+        }
     }
     __syncthreads();
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
     if constexpr (!QUANT) {
+        uint16_t *xp = static_cast<uint16_t *>(x_perm);
         for (int i = threadIdx.x; i < H / 8; i += 256) {
             const uint4 v = src[i];
             for (int k = 0; k < K; ++k)
-                reinterpret_cast<uint4 *>(x_perm + (size_t)rows[k] * H)[i] = v;
+                reinterpret_cast<uint4 *>(xp + (size_t)rows[k] * H)[i] = v;
         }
     } else {
-        for (int blk = threadIdx.x; blk < H / 16; blk += 256) {
+        // NVFP4: codes [rows, H/2] and the scales in token-chunk atoms
+        // [chunk, H/64, 512]; each 4 lanes (one 64-block) merge their scale
+        // bytes into one word
+        uint8_t *xq = static_cast<uint8_t *>(x_perm);
+        const int nblk = H / 16;
+        const int lane = threadIdx.x & 31;
+        for (int blk0 = threadIdx.x & ~31; blk0 < nblk; blk0 += 256) {
+            const int blk = blk0 + lane;
+            const unsigned live = __ballot_sync(0xFFFFFFFFu, blk < nblk);
+            if (blk >= nblk)
+                break;
             const uint4 q0 = src[2 * blk], q1 = src[2 * blk + 1];
             const uint32_t raw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
             float v[16];
-            float bmax = 0.0f;
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
                 v[2 * p] = bf16_bits_to_f32(raw[p] & 0xFFFFu);
                 v[2 * p + 1] = bf16_bits_to_f32(raw[p] >> 16);
-                bmax = fmaxf(bmax, fmaxf(fabsf(v[2 * p]), fabsf(v[2 * p + 1])));
             }
-            float sfv;
-            nvfp4_block_scale(bmax, 1.0f, &sfv);
-            uint32_t o[8];
-#pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                const __half2 hv = __floats2half2_rn(nvfp4_fake_quant(v[2 * p], sfv),
-                                                     nvfp4_fake_quant(v[2 * p + 1], sfv));
-                o[p] = *reinterpret_cast<const uint32_t *>(&hv);
-            }
-            const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]);
-            const uint4 o1 = make_uint4(o[4], o[5], o[6], o[7]);
+            uint32_t lo, hi;
+            uint32_t word = nvfp4_quant16(v, &lo, &hi) << (8 * (blk & 3));
+            word |= __shfl_xor_sync(live, word, 1);
+            word |= __shfl_xor_sync(live, word, 2);
             for (int k = 0; k < K; ++k) {
-                uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)rows[k] * H);
-                dst[2 * blk] = o0;
-                dst[2 * blk + 1] = o1;
+                *reinterpret_cast<uint2 *>(xq + (size_t)rows[k] * (H / 2) + 8 * blk) =
+                    make_uint2(lo, hi);
+                if ((blk & 3) == 0) {
+                    const int ps = pos[k];
+                    *reinterpret_cast<uint32_t *>(
+                        x_sf + ((size_t)(ps >> 7) * (H / 64) + (blk >> 2)) * 512 +
+                        nvfp4_atom_offset(ps & 127)) = word;
+                }
             }
         }
     }
 }
 
-// NVFP4 activation quantisation of an FP32 matrix [rows, cols] (scale 1 per
-// 16-element block): writes the exact FP16 values q * sf.  One thread per block.
+// NVFP4 activation quantisation of an FP32 matrix [rows, cols] (global scale
+// 1): codes [rows, cols/2] and the scales in token-chunk atoms
+// [chunk, cols/64, 512] at the row's row_pos.  One thread per 16-block.
 __global__ void __launch_bounds__(256)
-quantize_rows_kernel(const float *__restrict__ in, int64_t n_blocks, uint16_t *__restrict__ out)
+quantize_rows_kernel(const float *__restrict__ in, int64_t n_blocks, int cols,
+                     const int32_t *__restrict__ row_pos, uint8_t *__restrict__ codes,
+                     uint8_t *__restrict__ sf)
 {
     const int64_t b = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    const unsigned live = __ballot_sync(0xFFFFFFFFu, b < n_blocks);
     if (b >= n_blocks)
         return;
     const float4 *src = reinterpret_cast<const float4 *>(in) + 4 * b;
     float v[16];
-    float bmax = 0.0f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const float4 f = src[q];
@@ -195,21 +217,18 @@ quantize_rows_kernel(const float *__restrict__ in, int64_t n_blocks, uint16_t *_
         v[4 * q + 2] = f.z;
         v[4 * q + 3] = f.w;
     }
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        bmax = fmaxf(bmax, fabsf(v[i]));
-    float sfv;
-    nvfp4_block_scale(bmax, 1.0f, &sfv);
-    uint32_t o[8];
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const __half2 hv = __floats2half2_rn(nvfp4_fake_quant(v[2 * p], sfv),
-                                             nvfp4_fake_quant(v[2 * p + 1], sfv));
-        o[p] = *reinterpret_cast<const uint32_t *>(&hv);
+    uint32_t lo, hi;
+    const int bpr = cols / 16;
+    const int blk = (int)(b % bpr);
+    uint32_t word = nvfp4_quant16(v, &lo, &hi) << (8 * (blk & 3));
+    word |= __shfl_xor_sync(live, word, 1);
+    word |= __shfl_xor_sync(live, word, 2);
+    reinterpret_cast<uint2 *>(codes)[b] = make_uint2(lo, hi);
+    if ((blk & 3) == 0) {
+        const int ps = row_pos[b / bpr];
+        *reinterpret_cast<uint32_t *>(sf + ((size_t)(ps >> 7) * (cols / 64) + (blk >> 2)) * 512 +
+                                      nvfp4_atom_offset(ps & 127)) = word;
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(out) + 2 * b;
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 __global__ void __launch_bounds__(256)
@@ -290,16 +309,25 @@ cudaError_t launch_scan(const int32_t *cta_counts, int n_cta, int E, int chunk_r
 
 cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
                            const int32_t *cta_base, const int32_t *offsets, int T, int K, int E,
-                           int H, int32_t *row_of, int32_t *row_src, uint16_t *x_perm,
-                           bool quant_nvfp4, cudaStream_t s)
+                           int H, int32_t *row_of, int32_t *row_src, void *x_perm,
+                           cudaStream_t s)
 {
     stage_begin(kStPermute, s);
-    if (quant_nvfp4)
-        permute_kernel<true><<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, T, K, E, H,
-                                               row_of, row_src, x_perm);
-    else
-        permute_kernel<false><<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, T, K, E,
-                                                H, row_of, row_src, x_perm);
+    permute_kernel<false><<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, nullptr, T, K,
+                                            E, H, row_of, row_src, nullptr, x_perm, nullptr);
+    stage_end(kStPermute, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute_nvfp4(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
+                                 const int32_t *cta_base, const int32_t *offsets,
+                                 const int32_t *chunk_start, int T, int K, int E, int H,
+                                 int32_t *row_of, int32_t *row_src, int32_t *row_pos,
+                                 uint8_t *x_codes, uint8_t *x_sf, cudaStream_t s)
+{
+    stage_begin(kStPermute, s);
+    permute_kernel<true><<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, chunk_start, T,
+                                           K, E, H, row_of, row_src, row_pos, x_codes, x_sf);
     stage_end(kStPermute, s);
     return cudaGetLastError();
 }
@@ -316,12 +344,13 @@ cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int
     return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_rows(const float *in, int64_t rows, int cols, uint16_t *out,
-                                 cudaStream_t s)
+cudaError_t launch_quantize_rows(const float *in, int64_t rows, int cols, const int32_t *row_pos,
+                                 uint8_t *codes, uint8_t *sf, cudaStream_t s)
 {
     const int64_t n_blocks = rows * (int64_t)(cols / 16);
     stage_begin(kStQuantH, s);
-    quantize_rows_kernel<<<(unsigned)((n_blocks + 255) / 256), 256, 0, s>>>(in, n_blocks, out);
+    quantize_rows_kernel<<<(unsigned)((n_blocks + 255) / 256), 256, 0, s>>>(in, n_blocks, cols,
+                                                                            row_pos, codes, sf);
     stage_end(kStQuantH, s);
     return cudaGetLastError();
 }

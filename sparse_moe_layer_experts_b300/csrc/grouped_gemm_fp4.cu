@@ -1,28 +1,32 @@
-// Grouped expert GEMMs with NVFP4 expert weights (E2M1 codes, one E4M3
-// scale per 16 elements, an FP32 scale per expert and projection).
+// Grouped expert GEMMs in NVFP4 on the FP4 tensor cores: E2M1 weights and
+// activations, one E4M3 scale per 16 elements, an FP32 scale per expert and
+// projection.
 //
 // The pages name NVFP4 as the checkpoint for Blackwell ("Reflection Beam
 // 1.0", section on hardware requirements: most parameters in 4 bits); the
 // recipe is a reading (see nvfp4.cuh).  Each expert is still the SwiGLU MLP of
 // the "Mixture of Experts" section with the product in FP32.
 //
-// The weights stream from HBM as 4-bit codes plus scales (0.5625 B per
-// weight).  Converter warps expand each 128x64 tile in shared memory into the
-// FP16 values q*sf, which are exact because they need at most 6 significant
-// bits.  The tensor cores then run the same kind::f16 MMA as the bf16 path:
-// activations are FP16 too, holding the exact NVFP4 values of x (quantised in
-// the permute kernel) and of h (the gate/up epilogue writes h in FP32 and a
-// streaming pass quantises it).  The global scale multiplies the FP32
-// accumulator in the epilogue.
+// Both operands stay 4-bit from HBM to the tensor core.  Weights are the
+// M = 128 operand (swap-AB, as in the bf16 kernels), an expert's token rows
+// the N operand (16..128).  One k-step covers 256 elements: a 128-byte
+// swizzled row of codes per operand row, and four 512-byte scale atoms per
+// operand (the scales of 128 rows x 64 elements, row r = m0 + 32*m1 at byte
+// 16*m0 + 4*m1).  The MMA issuer copies the atoms from shared memory into
+// tensor memory (tcgen05.cp, 32x128b, replicated to the four lane quarters)
+// and runs tcgen05.mma kind::mxf4nvf4 with block16 scales, which
+// accumulates sum(q_a*sf_a * q_b*sf_b) in FP32.  The FP32 global scale of
+// the weights multiplies the accumulator in the epilogue (activations have
+// global scale 1).
 //
-// Warp roles:
-//   warp 0      producer: TMA of the code tile + bulk copy of its 512 scale
-//               bytes into a deep "raw" ring, and TMA of the token tile into
-//               the B ring
-//   warp 1      TMEM allocator and MMA issuer
-//   next 4*EPI_WG warps: epilogue warpgroup(s), splitting a tile's columns
-//   last 4 warps converters, one weight row per thread: raw ring -> FP16 A
-//               tiles (128-byte swizzled, K-major) of the A ring
+// Activation scales are laid out per token chunk (the N tile of one work
+// unit): [chunk, K/64, 512 bytes], written by the kernels that quantise x
+// and h.  K must be a multiple of 64: a last k-step with fewer than four
+// 64-blocks issues fewer MMAs, and its code tiles are zero-filled by TMA
+// past the row end.
+//
+// Warp roles: warp 0 TMA/bulk-copy producer, warp 1 TMEM allocator and MMA
+// issuer, then EPI_WG epilogue warpgroups splitting a tile's columns.
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "internal.h"
@@ -35,44 +39,45 @@ namespace beam {
 namespace {
 
 constexpr int kBlockM = 128;
-constexpr int kBlockK = 64;
-constexpr int kCodeBytes = kBlockM * kBlockK / 2;  // 4096
-constexpr int kSfBytes = kBlockM * kBlockK / 16;   // 512
-constexpr int kAF16Bytes = kBlockM * kBlockK * 2;  // 16384
+constexpr int kKStep = 256;                       // FP4 elements per k-step
+constexpr int kRowBytes = kKStep / 2;             // 128: one swizzle row
+constexpr int kACodeBytes = kBlockM * kRowBytes;  // 16384
+constexpr int kAtom = 512;                        // scales of 128 rows x 64 elements
+constexpr int kSfStep = 4 * kAtom;                // scales of one k-step
 constexpr int kMaxExperts = 256;
 
-template <bool GATEUP, int BN, int RS, int AS, int BS, int ACC_BUFS, int BOX, int EPI_WG>
-struct CfgF {
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG>
+struct CfgN {
     static constexpr int NA = GATEUP ? 2 : 1;
-    static constexpr int THREADS = 64 + 128 * EPI_WG + 128;
-    static constexpr int CONV_WARP0 = 2 + 4 * EPI_WG;
-    static constexpr int BOX_BYTES = BOX * kBlockK * 2;
-    static constexpr int RAW_BYTES = NA * (kCodeBytes + kSfBytes);
-    static constexpr int A_BYTES = NA * kAF16Bytes;     // converted weight tiles
-    static constexpr int B_BYTES = BN * kBlockK * 2;    // token tile
+    static constexpr int THREADS = 64 + 128 * EPI_WG;
+    static constexpr int A_BYTES = NA * kACodeBytes;
+    static constexpr int B_BYTES = BN * kRowBytes;
+    static constexpr int SFA_BYTES = NA * kSfStep;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + kSfStep;
+    static constexpr int BOX_BYTES = BOX * kRowBytes;
     static constexpr int ACC_COLS = NA * BN;
-    static constexpr int COLS_RAW = ACC_BUFS * ACC_COLS;
-    static constexpr int TMEM_COLS = COLS_RAW <= 32    ? 32
-                                     : COLS_RAW <= 64  ? 64
-                                     : COLS_RAW <= 128 ? 128
-                                     : COLS_RAW <= 256 ? 256
-                                                       : 512;
-    static constexpr int N_BARS = 2 * RS + 2 * AS + 2 * BS + 2 * ACC_BUFS + 1;
+    static constexpr int SF_COLS = (NA + 1) * 16;  // per stage: 4 atoms x 4 columns per operand
+    static constexpr int SF_COL0 = ACC_BUFS * ACC_COLS;
+    static constexpr int COLS_NEED = SF_COL0 + STAGES * SF_COLS;
+    static constexpr int TMEM_COLS = COLS_NEED <= 32    ? 32
+                                     : COLS_NEED <= 64  ? 64
+                                     : COLS_NEED <= 128 ? 128
+                                     : COLS_NEED <= 256 ? 256
+                                                        : 512;
+    static constexpr int N_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int AUX_BYTES = N_BARS * 8 + 16 + 2 * (kMaxExperts + 1) * 4;
-    static constexpr int SMEM_BYTES = 1024 + AS * A_BYTES + BS * B_BYTES + RS * RAW_BYTES +
-                                      ((AUX_BYTES + 127) / 128) * 128;
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-    static_assert(BN % BOX == 0 && BOX % 16 == 0, "token boxes tile the B operand");
-    static_assert(COLS_RAW <= 512, "TMEM columns");
-    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && RAW_BYTES % 128 == 0,
-                  "alignment");
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + ((AUX_BYTES + 127) / 128) * 128;
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N; one scale atom per chunk");
+    static_assert(BN % BOX == 0 && BOX % 8 == 0, "token boxes tile the B operand");
+    static_assert(COLS_NEED <= 512, "TMEM columns");
+    static_assert(STAGE_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle-atom alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 struct Fp4Params {
     GemmArgs a;
     Fp4Weights f;
-    int ksteps_total;  // k-steps per weight matrix row block (for scale tiles)
+    int kblocks;  // K / 64 of this GEMM
 };
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
@@ -85,36 +90,44 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem()
+// Shared-memory descriptor of a 32-row x 16-byte scale atom slice without
+// swizzle: core matrices of 8 rows x 16 bytes, 128 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_atom(uint32_t saddr)
 {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
 }
 
-// two E2M1 codes (low nibble first) -> f16x2 {low, high}
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte)
+// 32 rows x 128 bits from shared memory into 4 TMEM columns, replicated to
+// all four 32-lane quarters.
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint32_t saddr)
 {
-    uint32_t r;
-    const uint16_t b = (uint16_t)byte;
-    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-        : "=r"(r)
-        : "h"(b));
-    return r;
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr),
+                 "l"(smem_desc_atom(saddr))
+                 : "memory");
 }
 
-// two E4M3 codes (low byte first) -> f16x2 {low, high}
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
+// Instruction descriptor: E2M1 x E2M1 (format 1 each), UE4M3 scales, both
+// K-major, FP32 accumulator.
+__device__ __forceinline__ uint32_t idesc_nvf4(uint32_t m, uint32_t n)
 {
-    uint32_t r;
-    const uint16_t b = (uint16_t)two;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(b));
-    return r;
+    return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate)
 {
-    const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a),
-                              *reinterpret_cast<const __half2 *>(&b));
-    return *reinterpret_cast<const uint32_t *>(&r);
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+        "[%5], [%6], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
 }
 
 __device__ __forceinline__ float silu_mul_f(float g, float u)
@@ -122,56 +135,40 @@ __device__ __forceinline__ float silu_mul_f(float g, float u)
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <bool GATEUP, int BN, int RS, int AS, int BS, int ACC_BUFS, int BOX, int EPI_WG>
-__global__ void __launch_bounds__(64 + 128 * EPI_WG + 128, 1)
-grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
-                        const __grid_constant__ CUtensorMap tmA1,
-                        const __grid_constant__ CUtensorMap tmB, const Fp4Params P)
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG>
+__global__ void __launch_bounds__(64 + 128 * EPI_WG, 1)
+grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
+                         const __grid_constant__ CUtensorMap tmA1,
+                         const __grid_constant__ CUtensorMap tmB, const Fp4Params P)
 {
-    using C = CfgF<GATEUP, BN, RS, AS, BS, ACC_BUFS, BOX, EPI_WG>;
+    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG>;
     const GemmArgs &p = P.a;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base_u32 - raw_u32);
-    // [A ring (converted weights) | B ring (tokens) | raw ring | barriers | aux]
-    const uint32_t a_u32 = base_u32;
-    const uint32_t b_u32 = base_u32 + AS * C::A_BYTES;
-    uint8_t *raw_ring = smem + AS * C::A_BYTES + BS * C::B_BYTES;
-    const uint32_t rawring_u32 = b_u32 + BS * C::B_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(raw_ring + RS * C::RAW_BYTES);
+    // stage s: [A codes | B codes | A scale atoms | B scale atoms]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::N_BARS);
     volatile int *s_abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *s_off = reinterpret_cast<int *>(tmem_slot + 4);
     int *s_cs = s_off + (kMaxExperts + 1);
 
     const uint32_t bar_u32 = smem_u32(bars);
-    auto raw_full = [&](int s) { return bar_u32 + 8u * s; };
-    auto raw_empty = [&](int s) { return bar_u32 + 8u * (RS + s); };
-    auto a_full = [&](int s) { return bar_u32 + 8u * (2 * RS + s); };
-    auto a_empty = [&](int s) { return bar_u32 + 8u * (2 * RS + AS + s); };
-    auto b_full = [&](int s) { return bar_u32 + 8u * (2 * RS + 2 * AS + s); };
-    auto b_empty = [&](int s) { return bar_u32 + 8u * (2 * RS + 2 * AS + BS + s); };
-    constexpr int TB = 2 * RS + 2 * AS + 2 * BS;
-    auto tfull_bar = [&](int a) { return bar_u32 + 8u * (TB + a); };
-    auto tempty_bar = [&](int a) { return bar_u32 + 8u * (TB + ACC_BUFS + a); };
-    const uint32_t drain_bar = bar_u32 + 8u * (TB + 2 * ACC_BUFS);
+    auto full_bar = [&](int s) { return bar_u32 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_u32 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar_u32 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar_u32 + 8u * (2 * STAGES + ACC_BUFS + a); };
+    const uint32_t drain_bar = bar_u32 + 8u * (2 * STAGES + 2 * ACC_BUFS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
+    const int KB = P.kblocks;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < RS; ++s) {
-            mbar_init(raw_full(s), 1);
-            mbar_init(raw_empty(s), 128);
-        }
-        for (int s = 0; s < AS; ++s) {
-            mbar_init(a_full(s), 128);
-            mbar_init(a_empty(s), 1);
-        }
-        for (int s = 0; s < BS; ++s) {
-            mbar_init(b_full(s), 1);
-            mbar_init(b_empty(s), 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < ACC_BUFS; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -204,75 +201,68 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
 
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------- producer: weight codes + scales, token tiles
-            int rs = 0, bs = 0;
-            uint32_t rph = 0, bph = 0, armed = 0, armed_par = 0, barmed = 0, barmed_par = 0;
+            // ------------------------- producer: codes by TMA, scales by bulk copy
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, armed_par = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const Tile tl = decode_tile(t, s_off, s_cs, E, p.m_tiles);
-                const int arow = tl.e * p.m_tiles * kBlockM + tl.m * kBlockM;
-                const size_t sf_tile = ((size_t)tl.e * p.m_tiles + tl.m) * P.ksteps_total;
+                const size_t wtile = (size_t)tl.e * p.m_tiles + tl.m;
+                const int arow = (int)wtile * kBlockM;
+                const uint8_t *sfa0 = P.f.sf0 + wtile * KB * kAtom;
+                const uint8_t *sfa1 = GATEUP ? P.f.sf1 + wtile * KB * kAtom : nullptr;
+                // the tile's token chunk (its first row sits at position 0)
+                int j0;
+                const int chunk =
+                    s_cs[tl.e] + nvfp4_chunk_of_row(tl.row0 - s_off[tl.e], s_off[tl.e + 1] - s_off[tl.e],
+                                                    s_cs[tl.e + 1] - s_cs[tl.e], &j0);
+                const uint8_t *sfb = P.f.act_sf + (size_t)chunk * KB * kAtom;
                 const int nb = (tl.nrows + BOX - 1) / BOX;
                 for (int k = 0; k < p.ksteps; ++k) {
-                    if (!mbar_wait_bounded(raw_empty(rs), rph ^ 1u, tmo, s_abort, p.status)) {
+                    const int nkb = min(4, KB - 4 * k);
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, tmo, s_abort, p.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(raw_full(rs), C::RAW_BYTES);
-                    armed |= 1u << rs;
-                    armed_par = (armed_par & ~(1u << rs)) | (rph << rs);
-                    const uint32_t dst = rawring_u32 + rs * C::RAW_BYTES;
-                    tma_load_2d(dst, &tmA0, k * (kBlockK / 2), arow, raw_full(rs));
-                    bulk_g2s(dst + C::NA * kCodeBytes, P.f.sf0 + (sf_tile + k) * kSfBytes, kSfBytes,
-                             raw_full(rs));
-                    if (GATEUP) {
-                        tma_load_2d(dst + kCodeBytes, &tmA1, k * (kBlockK / 2), arow,
-                                    raw_full(rs));
-                        bulk_g2s(dst + C::NA * kCodeBytes + kSfBytes,
-                                 P.f.sf1 + (sf_tile + k) * kSfBytes, kSfBytes, raw_full(rs));
-                    }
-                    if (++rs == RS) {
-                        rs = 0;
-                        rph ^= 1u;
-                    }
-                    if (!mbar_wait_bounded(b_empty(bs), bph ^ 1u, tmo, s_abort, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(b_full(bs), nb * C::BOX_BYTES);
-                    barmed |= 1u << bs;
-                    barmed_par = (barmed_par & ~(1u << bs)) | (bph << bs);
-                    const uint32_t sb = b_u32 + bs * C::B_BYTES;
+                    mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(C::A_BYTES + nb * C::BOX_BYTES +
+                                                                      nkb * kAtom * (C::NA + 1)));
+                    armed |= 1u << stage;
+                    armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+                    const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
+                    const uint32_t sf = st + C::A_BYTES + C::B_BYTES;
+                    tma_load_2d(st, &tmA0, k * kRowBytes, arow, full_bar(stage));
+                    if (GATEUP)
+                        tma_load_2d(st + kACodeBytes, &tmA1, k * kRowBytes, arow, full_bar(stage));
                     for (int bb = 0; bb < nb; ++bb)
-                        tma_load_2d(sb + bb * C::BOX_BYTES, &tmB, k * kBlockK, tl.row0 + bb * BOX,
-                                    b_full(bs));
-                    if (++bs == BS) {
-                        bs = 0;
-                        bph ^= 1u;
+                        tma_load_2d(st + C::A_BYTES + bb * C::BOX_BYTES, &tmB, k * kRowBytes,
+                                    tl.row0 + bb * BOX, full_bar(stage));
+                    bulk_g2s(sf, sfa0 + (size_t)4 * k * kAtom, nkb * kAtom, full_bar(stage));
+                    if (GATEUP)
+                        bulk_g2s(sf + kSfStep, sfa1 + (size_t)4 * k * kAtom, nkb * kAtom,
+                                 full_bar(stage));
+                    bulk_g2s(sf + C::SFA_BYTES, sfb + (size_t)4 * k * kAtom, nkb * kAtom,
+                             full_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
             }
-            if (!ok) {
-                for (int s = 0; s < RS; ++s)
+            if (!ok)
+                for (int s = 0; s < STAGES; ++s)
                     if ((armed >> s) & 1u)
-                        mbar_wait_drain(raw_full(s), (armed_par >> s) & 1u, tmo);
-                for (int s = 0; s < BS; ++s)
-                    if ((barmed >> s) & 1u)
-                        mbar_wait_drain(b_full(s), (barmed_par >> s) & 1u, tmo);
-            }
+                        mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, tmo);
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             // --------------------------------------------- MMA issuer
-            int as = 0, bs = 0, acc = 0;
-            uint32_t aph = 0, bph = 0, acc_phase = 0;
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const Tile tl = decode_tile(t, s_off, s_cs, E, p.m_tiles);
-                const uint32_t n = (uint32_t)((tl.nrows + 15) & ~15);
-                // f16 x f16 -> f32: the bf16 descriptor with both formats = 0
-                const uint32_t idesc = idesc_bf16_f32(kBlockM, n) & ~((7u << 7) | (7u << 10));
+                const uint32_t idesc = idesc_nvf4(kBlockM, (uint32_t)((tl.nrows + 15) & ~15));
                 if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, tmo, s_abort, p.status)) {
                     ok = false;
                     break;
@@ -280,32 +270,36 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * C::ACC_COLS;
                 for (int k = 0; k < p.ksteps; ++k) {
-                    if (!mbar_wait_bounded(b_full(bs), bph, tmo, s_abort, p.status) ||
-                        !mbar_wait_bounded(a_full(as), aph, tmo, s_abort, p.status)) {
+                    const int nkb = min(4, KB - 4 * k);
+                    if (!mbar_wait_bounded(full_bar(stage), phase, tmo, s_abort, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = a_u32 + as * C::A_BYTES;
-                    const uint32_t sb = b_u32 + bs * C::B_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < kBlockK / 16; ++kk) {
-                        const uint64_t bd = smem_desc_k128(sb + kk * 32);
-                        const uint32_t accum = (k | kk) != 0;
-                        mma_bf16_ss(d, smem_desc_k128(sa + kk * 32), bd, idesc, accum);
+                    const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
+                    const uint32_t sf = st + C::A_BYTES + C::B_BYTES;
+                    // this stage's scale columns: A0 | A1 | B, 16 columns each
+                    const uint32_t ts = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
+                    const uint32_t tsb = ts + 16 * C::NA;
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        tmem_cp_atom(ts + 4 * kb, sf + kb * kAtom);
                         if (GATEUP)
-                            mma_bf16_ss(d + BN, smem_desc_k128(sa + kAF16Bytes + kk * 32), bd,
-                                        idesc, accum);
+                            tmem_cp_atom(ts + 16 + 4 * kb, sf + kSfStep + kb * kAtom);
+                        tmem_cp_atom(tsb + 4 * kb, sf + C::SFA_BYTES + kb * kAtom);
                     }
-                    mma_commit(a_empty(as));
-                    mma_commit(b_empty(bs));
-                    if (++as == AS) {
-                        as = 0;
-                        aph ^= 1u;
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        const uint64_t bd = smem_desc_k128(st + C::A_BYTES + kb * 32);
+                        const uint32_t accum = (k | kb) != 0;
+                        mma_nvf4(d, smem_desc_k128(st + kb * 32), bd, idesc, ts + 4 * kb,
+                                 tsb + 4 * kb, accum);
+                        if (GATEUP)
+                            mma_nvf4(d + BN, smem_desc_k128(st + kACodeBytes + kb * 32), bd, idesc,
+                                     ts + 16 + 4 * kb, tsb + 4 * kb, accum);
                     }
-                    if (++bs == BS) {
-                        bs = 0;
-                        bph ^= 1u;
+                    mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
                 if (!ok)
@@ -322,7 +316,7 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
             }
         }
         __syncwarp();
-    } else if (warp < C::CONV_WARP0) {
+    } else {
         // ------------------------------------------------- epilogue
         const int q = warp & 3;
         const int i = q * 32 + lane;
@@ -345,7 +339,7 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
                     uint32_t u[16];
                     tmem_ld16(ta + BN + c0, u);
                     tmem_ld_wait();
-                    // h = silu(g) * u, kept in FP32 for a separate pass that
+                    // h = silu(g) * u, kept in FP32 for the pass that
                     // quantises it to NVFP4 before the down GEMM
                     float *out = static_cast<float *>(p.out);
 #pragma unroll
@@ -371,60 +365,6 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
                 acc_phase ^= 1u;
             }
         }
-    } else {
-        // ------------------------------------------------ converters
-        const int r = (warp - C::CONV_WARP0) * 32 + lane;  // weight row of the tile
-        int rs = 0, as = 0;
-        uint32_t rph = 0, aph = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            for (int k = 0; k < p.ksteps; ++k) {
-                if (!mbar_wait_bounded(raw_full(rs), rph, tmo, s_abort, p.status) ||
-                    !mbar_wait_bounded(a_empty(as), aph ^ 1u, tmo, s_abort, p.status)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t sa = a_u32 + as * C::A_BYTES;
-                const uint8_t *raw = raw_ring + rs * C::RAW_BYTES;
-#pragma unroll
-                for (int mat = 0; mat < C::NA; ++mat) {
-                    const uint4 c0 = *reinterpret_cast<const uint4 *>(raw + mat * kCodeBytes + r * 32);
-                    const uint4 c1 =
-                        *reinterpret_cast<const uint4 *>(raw + mat * kCodeBytes + r * 32 + 16);
-                    const uint32_t sfw = *reinterpret_cast<const uint32_t *>(
-                        raw + C::NA * kCodeBytes + mat * kSfBytes + r * 4);
-                    const uint32_t s01 = e4m3x2_to_f16x2(sfw & 0xFFFFu);
-                    const uint32_t s23 = e4m3x2_to_f16x2(sfw >> 16);
-                    const uint32_t sfb[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232),
-                                             __byte_perm(s23, 0, 0x1010), __byte_perm(s23, 0, 0x3232)};
-                    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                    const uint32_t row_base = sa + mat * kAF16Bytes + r * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t sc = sfb[c >> 1];
-                        const uint32_t o0 = hmul2_u32(e2m1x2_to_f16x2(w[c] & 0xFFu), sc);
-                        const uint32_t o1 = hmul2_u32(e2m1x2_to_f16x2((w[c] >> 8) & 0xFFu), sc);
-                        const uint32_t o2 = hmul2_u32(e2m1x2_to_f16x2((w[c] >> 16) & 0xFFu), sc);
-                        const uint32_t o3 = hmul2_u32(e2m1x2_to_f16x2(w[c] >> 24), sc);
-                        const uint32_t dst = row_base + ((uint32_t)(c ^ (r & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o0),
-                                     "r"(o1), "r"(o2), "r"(o3)
-                                     : "memory");
-                    }
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(raw_empty(rs));
-                mbar_arrive(a_full(as));
-                if (++rs == RS) {
-                    rs = 0;
-                    rph ^= 1u;
-                }
-                if (++as == AS) {
-                    as = 0;
-                    aph ^= 1u;
-                }
-            }
-        }
     }
 
     tc_fence_before();
@@ -435,13 +375,13 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA0,
     }
 }
 
-template <bool GATEUP, int BN, int RS, int AS, int BS, int ACC_BUFS, int BOX, int EPI_WG>
-cudaError_t launch_fp4_variant(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
-                               const GemmArgs &args, const Fp4Weights &f, int grid, int stage,
-                               cudaStream_t s)
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG>
+cudaError_t launch_nvf4_variant(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
+                                const GemmArgs &args, const Fp4Weights &f, int kblocks, int grid,
+                                int stage, cudaStream_t s)
 {
-    using C = CfgF<GATEUP, BN, RS, AS, BS, ACC_BUFS, BOX, EPI_WG>;
-    auto kern = grouped_gemm_fp4_kernel<GATEUP, BN, RS, AS, BS, ACC_BUFS, BOX, EPI_WG>;
+    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG>;
+    auto kern = grouped_gemm_nvf4_kernel<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -452,8 +392,9 @@ cudaError_t launch_fp4_variant(const CUtensorMap &a0, const CUtensorMap &a1, con
         return attr_err;
     Fp4Params P;
     P.a = args;
+    P.a.ksteps = (kblocks + 3) / 4;
     P.f = f;
-    P.ksteps_total = args.ksteps;
+    P.kblocks = kblocks;
     stage_begin(stage, s);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a0, a1, b, P);
     stage_end(stage, s);
@@ -462,21 +403,36 @@ cudaError_t launch_fp4_variant(const CUtensorMap &a0, const CUtensorMap &a1, con
 
 }  // namespace
 
-cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
-                              const CUtensorMap &xp, const GemmArgs &a, const Fp4Weights &f,
-                              int grid, cudaStream_t s)
+int fp4_chunk_rows(GemmVariant v)
 {
-    if (v == GemmVariant::kDecode)
-        return launch_fp4_variant<true, 32, 12, 3, 4, 2, 16, 1>(wg, wu, xp, a, f, grid, kStGateUp, s);
-    return launch_fp4_variant<true, 256, 6, 2, 3, 1, 128, 2>(wg, wu, xp, a, f, grid, kStGateUp, s);
+    return v == GemmVariant::kDecode ? 32 : 128;
 }
 
-cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
-                            const GemmArgs &a, const Fp4Weights &f, int grid, cudaStream_t s)
+int fp4_box_rows(GemmVariant v)
+{
+    return v == GemmVariant::kDecode ? 16 : 128;
+}
+
+cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
+                              const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
+                              int kblocks, int grid, cudaStream_t s)
 {
     if (v == GemmVariant::kDecode)
-        return launch_fp4_variant<false, 32, 16, 4, 6, 2, 16, 1>(wd, wd, hp, a, f, grid, kStDown, s);
-    return launch_fp4_variant<false, 256, 10, 2, 4, 2, 128, 2>(wd, wd, hp, a, f, grid, kStDown, s);
+        return launch_nvf4_variant<true, 32, 5, 2, 16, 1>(wg, wu, xq, a, f, kblocks, grid,
+                                                          kStGateUp, s);
+    return launch_nvf4_variant<true, 128, 4, 1, 128, 2>(wg, wu, xq, a, f, kblocks, grid, kStGateUp,
+                                                        s);
+}
+
+cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hq,
+                            const GemmArgs &a, const Fp4Weights &f, int kblocks, int grid,
+                            cudaStream_t s)
+{
+    if (v == GemmVariant::kDecode)
+        return launch_nvf4_variant<false, 32, 9, 2, 16, 1>(wd, wd, hq, a, f, kblocks, grid, kStDown,
+                                                           s);
+    return launch_nvf4_variant<false, 128, 6, 2, 128, 2>(wd, wd, hq, a, f, kblocks, grid, kStDown,
+                                                         s);
 }
 
 }  // namespace beam

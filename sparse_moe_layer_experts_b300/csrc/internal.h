@@ -45,15 +45,23 @@ cudaError_t launch_scan(const int32_t *cta_counts, int n_cta, int E, int chunk_r
                         int32_t *chunk_start, cudaStream_t s);
 cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
                            const int32_t *cta_base, const int32_t *offsets, int T, int K, int E,
-                           int H, int32_t *row_of, int32_t *row_src, uint16_t *x_perm,
-                           bool quant_nvfp4, cudaStream_t s);
+                           int H, int32_t *row_of, int32_t *row_src, void *x_perm,
+                           cudaStream_t s);
+// NVFP4 layers: x rows quantised (global scale 1) into codes [R, H/2] and
+// token-chunk scale atoms [chunk, H/64, 512]; row_pos[row] = chunk*128 + j
+cudaError_t launch_permute_nvfp4(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
+                                 const int32_t *cta_base, const int32_t *offsets,
+                                 const int32_t *chunk_start, int T, int K, int E, int H,
+                                 int32_t *row_of, int32_t *row_src, int32_t *row_pos,
+                                 uint8_t *x_codes, uint8_t *x_sf, cudaStream_t s);
 // route-only variant: row_of without moving activations
 cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int32_t *cta_base,
                         const int32_t *offsets, int T, int K, int E, int32_t *row_of,
                         cudaStream_t s);
-// NVFP4 activations: FP32 [rows, cols] -> FP16 holding q * sf (16-blocks, scale 1)
-cudaError_t launch_quantize_rows(const float *in, int64_t rows, int cols, uint16_t *out,
-                                 cudaStream_t s);
+// NVFP4 activations: FP32 [rows, cols] -> codes [rows, cols/2] and scales in
+// the token-chunk atoms named by row_pos (global scale 1)
+cudaError_t launch_quantize_rows(const float *in, int64_t rows, int cols, const int32_t *row_pos,
+                                 uint8_t *codes, uint8_t *sf, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t *y, const float *w, const int32_t *row_of, int T, int K,
                            int H, uint16_t *out, cudaStream_t s);
 
@@ -73,10 +81,13 @@ struct GemmArgs {
 
 enum class GemmVariant { kDecode, kPrefill };
 
-// NVFP4 weights: E2M1 codes, tiled E4M3 block scales, FP32 global scales.
+// NVFP4 operands: E2M1 codes (via TMA maps), tiled E4M3 block scales of the
+// weights, FP32 global scales of the weights, and the activations' scales
+// in token-chunk atoms.
 struct Fp4Weights {
     const uint8_t *sf0, *sf1;  // block scales of A0 / A1 (A1: up projection)
     const float *gs0, *gs1;    // global scales [E]
+    const uint8_t *act_sf;     // [chunk, K/64, 512] scales of the B operand
 };
 
 // ---- nvfp4.cu
@@ -102,12 +113,18 @@ cudaError_t launch_down(GemmVariant v, const CUtensorMap &wd, const CUtensorMap 
 cudaError_t launch_down_pair(const CUtensorMap &wd, const CUtensorMap &hp, const GemmArgs &a,
                              int grid, cudaStream_t s);
 
-// ---- grouped_gemm_fp4.cu: the same GEMMs with NVFP4 weights (codes via
-// TMA maps of the packed bytes) and FP16 activations; gate/up quantises h.
+// ---- grouped_gemm_fp4.cu: the same GEMMs in NVFP4 on the FP4 tensor cores
+// (E2M1 codes of weights and activations via 128-byte TMA rows, block
+// scales via bulk copies); gate/up writes h in FP32 for launch_quantize_rows.
+// kblocks = K/64.  Token chunks are fp4_chunk_rows(v) rows at most and the
+// activation maps use fp4_box_rows(v)-row boxes.
+int fp4_chunk_rows(GemmVariant v);
+int fp4_box_rows(GemmVariant v);
 cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
-                              const CUtensorMap &xp, const GemmArgs &a, const Fp4Weights &f,
-                              int grid, cudaStream_t s);
-cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hp,
-                            const GemmArgs &a, const Fp4Weights &f, int grid, cudaStream_t s);
+                              const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
+                              int kblocks, int grid, cudaStream_t s);
+cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hq,
+                            const GemmArgs &a, const Fp4Weights &f, int kblocks, int grid,
+                            cudaStream_t s);
 
 }  // namespace beam

@@ -3,10 +3,11 @@
 // Layouts written (see beam_moe_quantize_nvfp4 in the header):
 //   packed   [n_mat, rows, cols/2]  two E2M1 codes per byte, even element in
 //                                   the low nibble
-//   block_sf [n_mat, rows/128, cols/64, 128, 4]  the E4M3 scale of elements
-//            [16b, 16b+16) of row r sits at tile (r/128, b/4), entry
-//            (r%128, b%4): the 512 scales one 128x64 GEMM tile needs are
-//            contiguous
+//   block_sf [n_mat, rows/128, cols/64, 512]  the E4M3 scale of elements
+//            [16b, 16b+16) of row r sits in tile (r/128, b/4) at byte
+//            16*(r%32) + 4*((r%128)/32) + b%4: the 512 scales one 128x64 GEMM
+//            tile needs are contiguous, in the row order in which the tensor
+//            core's scale copy (tcgen05.cp 32x128b.warpx4) takes them
 //   global   [n_mat] FP32
 #include "common.cuh"
 #include "internal.h"
@@ -92,7 +93,7 @@ nvfp4_quantize_kernel(const uint16_t *__restrict__ w, int64_t n_blocks, int rows
     }
     *reinterpret_cast<uint2 *>(packed + elem / 2) = make_uint2(lo, hi);
     const int64_t tile = (mat * (rows / 128) + r / 128) * (cols / 64) + cb / 4;
-    block_sf[tile * 512 + (r % 128) * 4 + (cb % 4)] = (uint8_t)sc;
+    block_sf[tile * 512 + nvfp4_atom_offset(r % 128) + (cb % 4)] = (uint8_t)sc;
 }
 
 }  // namespace

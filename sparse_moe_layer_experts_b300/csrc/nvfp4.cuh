@@ -70,13 +70,52 @@ __device__ __forceinline__ uint32_t nvfp4_block_scale(float bmax, float gs, floa
     return c;
 }
 
-// Quantise-dequantise one value of a block with scale sfv (gs = 1): the
-// exact value q * sfv.
-__device__ __forceinline__ float nvfp4_fake_quant(float v, float sfv)
+// E2M1 code of one value of a block with scale value sfv (global scale 1):
+// 0 when the block scale is 0.
+__device__ __forceinline__ uint32_t nvfp4_code(float v, float sfv)
 {
-    if (sfv == 0.0f)
-        return 0.0f;
-    return e2m1_value(e2m1_code(__fdiv_rn(v, sfv))) * sfv;
+    return sfv == 0.0f ? 0u : e2m1_code(__fdiv_rn(v, sfv));
+}
+
+// Quantise 16 values with global scale 1: 8 code bytes (even element in the
+// low nibble) as two words, and the E4M3 scale code.
+__device__ __forceinline__ uint32_t nvfp4_quant16(const float (&v)[16], uint32_t *lo, uint32_t *hi)
+{
+    float bmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        bmax = fmaxf(bmax, fabsf(v[i]));
+    float sfv;
+    const uint32_t sc = nvfp4_block_scale(bmax, 1.0f, &sfv);
+    uint32_t a = 0, b = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        a |= nvfp4_code(v[i], sfv) << (4 * i);
+        b |= nvfp4_code(v[i + 8], sfv) << (4 * i);
+    }
+    *lo = a;
+    *hi = b;
+    return sc;
+}
+
+// Token chunks: an expert's n rows are split into nc near-equal chunks,
+// chunk c holding rows [floor(c*n/nc), floor((c+1)*n/nc)) (the N tiles of
+// the grouped GEMMs).  Returns the chunk of row i (0-based inside the
+// expert), the largest c with floor(c*n/nc) <= i, and *j, the row's position
+// in it.
+__device__ __forceinline__ int nvfp4_chunk_of_row(int i, int n, int nc, int *j)
+{
+    const int c = (int)((((long long)i + 1) * nc - 1) / n);
+    *j = i - (int)(((long long)c * n) / nc);
+    return c;
+}
+
+// Byte offset, inside one 512-byte scale atom (128 rows x 4 scales), of the
+// 4 scales of row j: row j = m0 + 32*m1 sits at 16*m0 + 4*m1, the order in
+// which tcgen05.cp 32x128b.warpx4 hands the rows to the tensor core.
+__device__ __forceinline__ int nvfp4_atom_offset(int j)
+{
+    return 16 * (j & 31) + 4 * (j >> 5);
 }
 
 }  // namespace beam

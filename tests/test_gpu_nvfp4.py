@@ -21,9 +21,10 @@ def unpack_codes(packed: np.ndarray) -> np.ndarray:
 
 
 def untile_scales(flat: np.ndarray, n_mat, rows, cols) -> np.ndarray:
-    """tiled [n, rows/128, cols/64, 128, 4] -> [n, rows, cols/16]."""
-    t = flat.reshape(n_mat, rows // 128, cols // 64, 128, 4)
-    return t.transpose(0, 1, 3, 2, 4).reshape(n_mat, rows, cols // 16)
+    """tiled [n, rows/128, cols/64, 512] -> [n, rows, cols/16].  Inside a tile,
+    row r = m0 + 32*m1 holds its 4 scales at byte 16*m0 + 4*m1."""
+    t = flat.reshape(n_mat, rows // 128, cols // 64, 32, 4, 4)  # .., m0, m1, kb
+    return t.transpose(0, 1, 4, 3, 2, 5).reshape(n_mat, rows, cols // 16)
 
 
 def test_quantizer_bitexact(oracle_mod):
