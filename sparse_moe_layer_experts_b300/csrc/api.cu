@@ -40,7 +40,8 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
     size_t status, scores, ids, wts, local_rank, cta_counts, cta_base, counts, offsets,
-        chunk_start, row_of, row_src, x_perm, h, h_raw, y, row_pos, x_sf, h_sf, total;
+        chunk_start, chunk_start2, row_of, row_src, x_perm, h, h_raw, y, row_pos, x_sf, h_sf,
+        total;
 };
 
 GemmVariant pick_variant(int64_t T, const beam_moe_cfg &c)
@@ -49,11 +50,17 @@ GemmVariant pick_variant(int64_t T, const beam_moe_cfg &c)
     return (T * c.top_k <= 16LL * c.n_experts) ? GemmVariant::kDecode : GemmVariant::kPrefill;
 }
 
-// Rows per token chunk (the N tile of the grouped GEMMs).
+// Rows per token chunk (the N tile of the grouped GEMMs); NVFP4 layers
+// chunk the down GEMM's rows separately (chunk_rows2).
 int chunk_rows(int64_t T, const beam_moe_cfg &c)
 {
     const GemmVariant v = pick_variant(T, c);
     return c.wtype == BEAM_MOE_W_NVFP4 ? fp4_chunk_rows(v) : gemm_chunk_rows(v);
+}
+
+int chunk_rows2(int64_t T, const beam_moe_cfg &c)
+{
+    return fp4_down_chunk_rows(pick_variant(T, c));
 }
 
 Layout make_layout(int64_t T, const beam_moe_cfg &c)
@@ -78,6 +85,7 @@ Layout make_layout(int64_t T, const beam_moe_cfg &c)
     L.counts = take(sizeof(int32_t) * E);
     L.offsets = take(sizeof(int32_t) * (E + 1));
     L.chunk_start = take(sizeof(int32_t) * (E + 1));
+    L.chunk_start2 = take(sizeof(int32_t) * (E + 1));
     L.row_of = take(sizeof(int32_t) * R);
     L.row_src = take(sizeof(int32_t) * R);
     const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4;
@@ -86,13 +94,16 @@ Layout make_layout(int64_t T, const beam_moe_cfg &c)
     L.h = take(fp4 ? R * I / 2 : 2 * R * I);
     L.h_raw = take(fp4 ? 4 * R * I : 0);  // FP32 h before quantisation
     L.y = take(2 * R * H);
-    // NVFP4: chunk*128 + position of each row, and the activations' scales
-    // in token-chunk atoms [chunk, K/64, 512]
-    const int64_t cr = chunk_rows(T, c);
+    // NVFP4: each row's place in the down GEMM's chunking, and the
+    // activations' scales per token chunk: x in atoms [chunk, H/64, 512],
+    // h in atoms or in the replicated 256-row images [chunk2, I/64, 4096]
+    const int64_t cr = chunk_rows(T, c), cr2 = chunk_rows2(T, c);
     const int64_t chunks = fp4 ? (R + cr - 1) / cr + E : 0;
+    const int64_t chunks2 = fp4 ? (R + cr2 - 1) / cr2 + E : 0;
+    const size_t h_unit = fp4_down_rep(pick_variant(T, c)) ? 4096 : 512;
     L.row_pos = take(fp4 ? 4 * R : 0);
     L.x_sf = take((size_t)chunks * (H / 64) * 512);
-    L.h_sf = take((size_t)chunks * (I / 64) * 512);
+    L.h_sf = take((size_t)chunks2 * (I / 64) * h_unit);
     L.total = o;
     return L;
 }
@@ -214,8 +225,8 @@ int device_sms()
 
 // Steps 1-6 plus histogram/scan into the workspace.
 int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cfg &c,
-              const Layout &L, float *scores, int32_t *ids, float *wts, int chunk_rows,
-              cudaStream_t s)
+              const Layout &L, float *scores, int32_t *ids, float *wts, int rows_per_chunk,
+              int rows_per_chunk2, cudaStream_t s)
 {
     void *ws = c.workspace;
     int *status = at<int>(ws, L.status);
@@ -226,9 +237,10 @@ int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cf
                             c.routed_scale, ids, wts, status, s));
     BEAM_CUDA(launch_hist(ids, (int)T, c.top_k, c.n_experts, at<int32_t>(ws, L.local_rank),
                           at<int32_t>(ws, L.cta_counts), status, s));
-    BEAM_CUDA(launch_scan(at<int32_t>(ws, L.cta_counts), n_cta, c.n_experts, chunk_rows,
-                          at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.counts),
-                          at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start), s));
+    BEAM_CUDA(launch_scan(at<int32_t>(ws, L.cta_counts), n_cta, c.n_experts, rows_per_chunk,
+                          rows_per_chunk2, at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.counts),
+                          at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start),
+                          rows_per_chunk2 > 0 ? at<int32_t>(ws, L.chunk_start2) : nullptr, s));
     return BEAM_MOE_OK;
 }
 
@@ -238,18 +250,18 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     const Layout L = make_layout(T, c);
     void *ws = c.workspace;
     const GemmVariant v = pick_variant(T, c);
+    const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4;
     int rc = run_route(x, router_w, T, c, L, at<float>(ws, L.scores), at<int32_t>(ws, L.ids),
-                       at<float>(ws, L.wts), chunk_rows(T, c), s);
+                       at<float>(ws, L.wts), chunk_rows(T, c), fp4 ? chunk_rows2(T, c) : 0, s);
     if (rc != BEAM_MOE_OK)
         return rc;
     const int K = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
     const int64_t R = T * K;
-    const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4;
     if (fp4)
         BEAM_CUDA(launch_permute_nvfp4(
             static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids), at<int32_t>(ws, L.local_rank),
             at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start),
-            (int)T, K, E, H, at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.row_src),
+            at<int32_t>(ws, L.chunk_start2), (int)T, K, E, H, at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.row_src),
             at<int32_t>(ws, L.row_pos), at<uint8_t>(ws, L.x_perm), at<uint8_t>(ws, L.x_sf), s));
     else
         BEAM_CUDA(launch_permute(static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids),
@@ -300,7 +312,8 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
         a.out = at<void>(ws, L.h_raw);
         BEAM_CUDA(launch_gateup_fp4(v, m_wg, m_wu, m_xp, a, f, H / 64, sms, s));
         BEAM_CUDA(launch_quantize_rows(at<float>(ws, L.h_raw), R, I, at<int32_t>(ws, L.row_pos),
-                                       at<uint8_t>(ws, L.h), at<uint8_t>(ws, L.h_sf), s));
+                                       fp4_down_rep(v), at<uint8_t>(ws, L.h),
+                                       at<uint8_t>(ws, L.h_sf), s));
     } else {
         BEAM_CUDA(launch_gateup(v, m_wg, m_wu, m_xp, a, sms, s));
     }
@@ -313,6 +326,7 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     if (fp4) {
         Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, c.w_down_gs, nullptr,
                      at<uint8_t>(ws, L.h_sf)};
+        a.chunk_start = at<int32_t>(ws, L.chunk_start2);  // the down GEMM's own chunking
         BEAM_CUDA(launch_down_fp4(v, m_wd, m_h, a, f, I / 64, sms, s));
     } else {
         BEAM_CUDA(launch_down(v, m_wd, m_h, a, sms, s));
@@ -379,7 +393,7 @@ int beam_moe_route(const void *x, const float *router_w, int64_t T, const beam_m
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *ws = c.workspace;
     float *sc = scores ? scores : at<float>(ws, L.scores);
-    rc = run_route(x, router_w, T, c, L, sc, topk_ids, topk_w, chunk_rows(T, c),
+    rc = run_route(x, router_w, T, c, L, sc, topk_ids, topk_w, chunk_rows(T, c), 0,
                    s);
     if (rc != BEAM_MOE_OK)
         return rc;

@@ -20,10 +20,16 @@
 // global scale 1).
 //
 // Activation scales are laid out per token chunk (the N tile of one work
-// unit): [chunk, K/64, 512 bytes], written by the kernels that quantise x
-// and h.  K must be a multiple of 64: a last k-step with fewer than four
-// 64-blocks issues fewer MMAs, and its code tiles are zero-filled by TMA
-// past the row end.
+// unit), written by the kernels that quantise x and h: atoms
+// [chunk, K/64, 512] for chunks of <= 128 rows, or (SFB_REP, chunks of <= 256
+// rows) [chunk, K/64, 4096]: per 64-block the atoms of rows 0-127 and
+// 128-255, each replicated 4 times, which one 128-lane x 256-bit tcgen05.cp
+// turns into the 8 scale columns of an N = 256 MMA.  Every tensor-core
+// instruction costs a roughly fixed number of cycles (about 140 for an MMA of
+// N <= 128, 160 for N = 256, 80-130 for a scale copy), so the N = 256 form
+// does twice the work per MMA with fewer copies.  K must be a multiple of
+// 64: a last k-step with fewer than four 64-blocks issues fewer MMAs, and its
+// code tiles are zero-filled by TMA past the row end.
 //
 // Warp roles: warp 0 TMA/bulk-copy producer, warp 1 TMEM allocator and MMA
 // issuer, then EPI_WG epilogue warpgroups splitting a tile's columns.
@@ -46,17 +52,20 @@ constexpr int kAtom = 512;                        // scales of 128 rows x 64 ele
 constexpr int kSfStep = 4 * kAtom;                // scales of one k-step
 constexpr int kMaxExperts = 256;
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP>
 struct CfgN {
     static constexpr int NA = GATEUP ? 2 : 1;
     static constexpr int THREADS = 64 + 128 * EPI_WG;
     static constexpr int A_BYTES = NA * kACodeBytes;
     static constexpr int B_BYTES = BN * kRowBytes;
     static constexpr int SFA_BYTES = NA * kSfStep;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + kSfStep;
+    static constexpr int SFB_KB_BYTES = SFB_REP ? 4096 : kAtom;  // token scales of one 64-block
+    static constexpr int SFB_BYTES = 4 * SFB_KB_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int BOX_BYTES = BOX * kRowBytes;
     static constexpr int ACC_COLS = NA * BN;
-    static constexpr int SF_COLS = (NA + 1) * 16;  // per stage: 4 atoms x 4 columns per operand
+    static constexpr int SFB_COLS = SFB_REP ? 32 : 16;
+    static constexpr int SF_COLS = NA * 16 + SFB_COLS;  // per stage: 4 columns per atom
     static constexpr int SF_COL0 = ACC_BUFS * ACC_COLS;
     static constexpr int COLS_NEED = SF_COL0 + STAGES * SF_COLS;
     static constexpr int TMEM_COLS = COLS_NEED <= 32    ? 32
@@ -67,7 +76,8 @@ struct CfgN {
     static constexpr int N_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int AUX_BYTES = N_BARS * 8 + 16 + 2 * (kMaxExperts + 1) * 4;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + ((AUX_BYTES + 127) / 128) * 128;
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N; one scale atom per chunk");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= (SFB_REP ? 256 : 128),
+                  "MMA N; token scale atoms per chunk");
     static_assert(BN % BOX == 0 && BOX % 8 == 0, "token boxes tile the B operand");
     static_assert(COLS_NEED <= 512, "TMEM columns");
     static_assert(STAGE_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle-atom alignment");
@@ -110,6 +120,17 @@ __device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint32_t saddr)
                  : "memory");
 }
 
+// 128 rows x 256 bits into 8 TMEM columns: the two 2 KB halves of a 4 KB
+// image (128 rows x 16 bytes each) land in columns 0-3 and 4-7.
+__device__ __forceinline__ void tmem_cp_pair(uint32_t taddr, uint32_t saddr)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(2048u >> 4) << 16;  // between the halves
+    d |= (uint64_t)(128u >> 4) << 32;   // between 8-row groups
+    d |= (uint64_t)1 << 46;
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+
 // Instruction descriptor: E2M1 x E2M1 (format 1 each), UE4M3 scales, both
 // K-major, FP32 accumulator.
 __device__ __forceinline__ uint32_t idesc_nvf4(uint32_t m, uint32_t n)
@@ -135,13 +156,13 @@ __device__ __forceinline__ float silu_mul_f(float g, float u)
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP>
 __global__ void __launch_bounds__(64 + 128 * EPI_WG, 1)
 grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                          const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB, const Fp4Params P)
 {
-    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG>;
+    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP>;
     const GemmArgs &p = P.a;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -216,7 +237,7 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                 const int chunk =
                     s_cs[tl.e] + nvfp4_chunk_of_row(tl.row0 - s_off[tl.e], s_off[tl.e + 1] - s_off[tl.e],
                                                     s_cs[tl.e + 1] - s_cs[tl.e], &j0);
-                const uint8_t *sfb = P.f.act_sf + (size_t)chunk * KB * kAtom;
+                const uint8_t *sfb = P.f.act_sf + (size_t)chunk * KB * C::SFB_KB_BYTES;
                 const int nb = (tl.nrows + BOX - 1) / BOX;
                 for (int k = 0; k < p.ksteps; ++k) {
                     const int nkb = min(4, KB - 4 * k);
@@ -224,8 +245,9 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(C::A_BYTES + nb * C::BOX_BYTES +
-                                                                      nkb * kAtom * (C::NA + 1)));
+                    mbar_arrive_expect_tx(full_bar(stage),
+                                          (uint32_t)(C::A_BYTES + nb * C::BOX_BYTES +
+                                                     nkb * (kAtom * C::NA + C::SFB_KB_BYTES)));
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                     const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
@@ -240,8 +262,8 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                     if (GATEUP)
                         bulk_g2s(sf + kSfStep, sfa1 + (size_t)4 * k * kAtom, nkb * kAtom,
                                  full_bar(stage));
-                    bulk_g2s(sf + C::SFA_BYTES, sfb + (size_t)4 * k * kAtom, nkb * kAtom,
-                             full_bar(stage));
+                    bulk_g2s(sf + C::SFA_BYTES, sfb + (size_t)4 * k * C::SFB_KB_BYTES,
+                             nkb * C::SFB_KB_BYTES, full_bar(stage));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -278,23 +300,29 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                     tc_fence_after();
                     const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
                     const uint32_t sf = st + C::A_BYTES + C::B_BYTES;
-                    // this stage's scale columns: A0 | A1 | B, 16 columns each
+                    // this stage's scale columns: A0 | A1 (16 each) | B (16, or
+                    // 32 = 8 per 64-block in the replicated form); every MMA
+                    // scale address is a multiple of 4 columns
                     const uint32_t ts = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
                     const uint32_t tsb = ts + 16 * C::NA;
+                    constexpr uint32_t kbB = SFB_REP ? 8 : 4;
                     for (int kb = 0; kb < nkb; ++kb) {
                         tmem_cp_atom(ts + 4 * kb, sf + kb * kAtom);
                         if (GATEUP)
                             tmem_cp_atom(ts + 16 + 4 * kb, sf + kSfStep + kb * kAtom);
-                        tmem_cp_atom(tsb + 4 * kb, sf + C::SFA_BYTES + kb * kAtom);
+                        if constexpr (SFB_REP)
+                            tmem_cp_pair(tsb + kbB * kb, sf + C::SFA_BYTES + kb * C::SFB_KB_BYTES);
+                        else
+                            tmem_cp_atom(tsb + kbB * kb, sf + C::SFA_BYTES + kb * kAtom);
                     }
                     for (int kb = 0; kb < nkb; ++kb) {
                         const uint64_t bd = smem_desc_k128(st + C::A_BYTES + kb * 32);
                         const uint32_t accum = (k | kb) != 0;
                         mma_nvf4(d, smem_desc_k128(st + kb * 32), bd, idesc, ts + 4 * kb,
-                                 tsb + 4 * kb, accum);
+                                 tsb + kbB * kb, accum);
                         if (GATEUP)
                             mma_nvf4(d + BN, smem_desc_k128(st + kACodeBytes + kb * 32), bd, idesc,
-                                     ts + 16 + 4 * kb, tsb + 4 * kb, accum);
+                                     ts + 16 + 4 * kb, tsb + kbB * kb, accum);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == STAGES) {
@@ -332,34 +360,64 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
             tc_fence_after();
             const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::ACC_COLS;
             const int col = tl.m * kBlockM + i;
-            for (int c0 = wg * 16; c0 < tl.nrows; c0 += 16 * EPI_WG) {
-                uint32_t g[16];
-                tmem_ld16(ta + c0, g);
-                if constexpr (GATEUP) {
-                    uint32_t u[16];
-                    tmem_ld16(ta + BN + c0, u);
-                    tmem_ld_wait();
-                    // h = silu(g) * u, kept in FP32 for the pass that
-                    // quantises it to NVFP4 before the down GEMM
-                    float *out = static_cast<float *>(p.out);
+            // Drain this thread's columns into registers first and release
+            // the accumulator, so the next tile's MMAs overlap the stores.
+            // Column chunks of this warpgroup: (ch * EPI_WG + wg) * 16.
+            constexpr int NCH = BN / 16 / EPI_WG;
+            if constexpr (GATEUP) {
+                // h = silu(g) * u in FP32, for the pass that quantises it
+                float hv[NCH][16];
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const int c0 = (ch * EPI_WG + wg) * 16;
+                    if (c0 < tl.nrows) {
+                        uint32_t g[16], u[16];
+                        tmem_ld16(ta + c0, g);
+                        tmem_ld16(ta + BN + c0, u);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            hv[ch][j] = silu_mul_f(__fmul_rn(__uint_as_float(g[j]), g0),
+                                                   __fmul_rn(__uint_as_float(u[j]), g1));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(tempty_bar(acc));
+                float *out = static_cast<float *>(p.out);
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const int c0 = (ch * EPI_WG + wg) * 16;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         if (c0 + j < tl.nrows)
-                            out[(size_t)(tl.row0 + c0 + j) * p.out_ld + col] =
-                                silu_mul_f(__fmul_rn(__uint_as_float(g[j]), g0),
-                                           __fmul_rn(__uint_as_float(u[j]), g1));
-                } else {
-                    tmem_ld_wait();
-                    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+                            out[(size_t)(tl.row0 + c0 + j) * p.out_ld + col] = hv[ch][j];
+                }
+            } else {
+                __nv_bfloat16 yv[NCH][16];
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const int c0 = (ch * EPI_WG + wg) * 16;
+                    if (c0 < tl.nrows) {
+                        uint32_t g[16];
+                        tmem_ld16(ta + c0, g);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            yv[ch][j] = __float2bfloat16_rn(__fmul_rn(__uint_as_float(g[j]), g0));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(tempty_bar(acc));
+                __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const int c0 = (ch * EPI_WG + wg) * 16;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         if (c0 + j < tl.nrows)
-                            out[(size_t)(tl.row0 + c0 + j) * p.out_ld + col] =
-                                __float2bfloat16_rn(__fmul_rn(__uint_as_float(g[j]), g0));
+                            out[(size_t)(tl.row0 + c0 + j) * p.out_ld + col] = yv[ch][j];
                 }
             }
-            tc_fence_before();
-            mbar_arrive(tempty_bar(acc));
             if (++acc == ACC_BUFS) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -375,13 +433,13 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
     }
 }
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP = false>
 cudaError_t launch_nvf4_variant(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                                 const GemmArgs &args, const Fp4Weights &f, int kblocks, int grid,
                                 int stage, cudaStream_t s)
 {
-    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG>;
-    auto kern = grouped_gemm_nvf4_kernel<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG>;
+    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP>;
+    auto kern = grouped_gemm_nvf4_kernel<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -408,6 +466,16 @@ int fp4_chunk_rows(GemmVariant v)
     return v == GemmVariant::kDecode ? 32 : 128;
 }
 
+int fp4_down_chunk_rows(GemmVariant v)
+{
+    return v == GemmVariant::kDecode ? 32 : 256;
+}
+
+bool fp4_down_rep(GemmVariant v)
+{
+    return v != GemmVariant::kDecode;
+}
+
 int fp4_box_rows(GemmVariant v)
 {
     return v == GemmVariant::kDecode ? 16 : 128;
@@ -431,8 +499,8 @@ cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensor
     if (v == GemmVariant::kDecode)
         return launch_nvf4_variant<false, 32, 9, 2, 16, 1>(wd, wd, hq, a, f, kblocks, grid, kStDown,
                                                            s);
-    return launch_nvf4_variant<false, 128, 6, 2, 128, 2>(wd, wd, hq, a, f, kblocks, grid, kStDown,
-                                                         s);
+    return launch_nvf4_variant<false, 256, 3, 1, 128, 2, true>(wd, wd, hq, a, f, kblocks, grid,
+                                                               kStDown, s);
 }
 
 }  // namespace beam
