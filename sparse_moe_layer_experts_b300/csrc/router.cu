@@ -127,7 +127,9 @@ __device__ __forceinline__ void cp_async_wait()
 
 // Large batches: register-tiled FP32 GEMM, 16x16 threads, R x R outputs per
 // thread (CTA tile 16R tokens x 16R experts), K chunks of 16 double-buffered
-// in shared memory with the next chunk prefetched into registers.  Every
+// in shared memory.  The next chunk of router weights streams in by cp.async
+// and the next x chunk through registers (bf16 -> FP32); inside a chunk the
+// fragments of step k+1 are loaded while step k's FMAs issue.  Every
 // accumulator walks h = 0..H-1 in order, so the tiling does not change any
 // result.
 constexpr int kLKC = 16;
@@ -146,74 +148,64 @@ router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;
     const int t0 = blockIdx.x * TM, e0 = blockIdx.y * TE;
-
-    // loaders: x: TM rows x 16 bf16 (TM*2 16-byte vectors); w: 16 rows x TE fp32
-    constexpr int XV = TM * 2;          // x vectors per chunk
-    constexpr int WV = kLKC * TE / 4;   // w float4 per chunk
-    constexpr int XPT = XV / 256 > 0 ? XV / 256 : 1;
-    constexpr int WPT = WV / 256;
-    static_assert(WV % 256 == 0, "w loader");
-    uint4 xq[XPT];
-    float4 wq[WPT];
-    auto gload = [&](int k0) {
-#pragma unroll
-        for (int v = 0; v < XPT; ++v) {
-            const int c = tid + v * 256;
-            const int r = c >> 1, col = (c & 1) * 8;
-            const bool ok = c < XV && t0 + r < T;
-            xq[v] = ok ? *reinterpret_cast<const uint4 *>(x + (size_t)(t0 + r) * H + k0 + col)
-                       : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int v = 0; v < WPT; ++v) {
-            const int c = tid + v * 256;
-            const int r = c / (TE / 4), col = (c % (TE / 4)) * 4;
-            wq[v] = (e0 + col < E)
-                        ? *reinterpret_cast<const float4 *>(wr + (size_t)(k0 + r) * E + e0 + col)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+    constexpr int XV = TM * 2;                // 16-byte x vectors per chunk (<= 256)
+    constexpr int WPT = kLKC * TE / 4 / 256;  // float4 of w per thread
+    static_assert(XV <= 256 && WPT >= 1, "loaders");
+    uint4 xq = make_uint4(0, 0, 0, 0);
+    auto xload = [&](int k0) {
+        const int r = tid >> 1, col = (tid & 1) * 8;
+        if (tid < XV)
+            xq = (t0 + r < T) ? *reinterpret_cast<const uint4 *>(x + (size_t)(t0 + r) * H + k0 + col)
+                              : make_uint4(0, 0, 0, 0);
     };
-    auto sstore = [&](int b) {
+    auto xstore = [&](int b) {
+        if (tid < XV) {
+            const int r = tid >> 1, col = (tid & 1) * 8;
+            const uint32_t q[4] = {xq.x, xq.y, xq.z, xq.w};
 #pragma unroll
-        for (int v = 0; v < XPT; ++v) {
-            const int c = tid + v * 256;
-            if (c < XV) {
-                const int r = c >> 1, col = (c & 1) * 8;
-                const uint32_t q[4] = {xq[v].x, xq[v].y, xq[v].z, xq[v].w};
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    xs[b][col + 2 * p][r] = bf16_bits_to_f32(q[p] & 0xFFFFu);
-                    xs[b][col + 2 * p + 1][r] = bf16_bits_to_f32(q[p] >> 16);
-                }
+            for (int p = 0; p < 4; ++p) {
+                xs[b][col + 2 * p][r] = bf16_bits_to_f32(q[p] & 0xFFFFu);
+                xs[b][col + 2 * p + 1][r] = bf16_bits_to_f32(q[p] >> 16);
             }
         }
+    };
+    auto wasync = [&](int b, int k0) {
 #pragma unroll
         for (int v = 0; v < WPT; ++v) {
             const int c = tid + v * 256;
             const int r = c / (TE / 4), col = (c % (TE / 4)) * 4;
-            *reinterpret_cast<float4 *>(&ws[b][r][col]) = wq[v];
+            float *dst = &ws[b][r][col];
+            if (e0 + col < E) {
+                const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d),
+                             "l"(wr + (size_t)(k0 + r) * E + e0 + col)
+                             : "memory");
+            } else {
+                *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     };
-
     float acc[R][R];
 #pragma unroll
     for (int i = 0; i < R; ++i)
 #pragma unroll
         for (int j = 0; j < R; ++j)
             acc[i][j] = 0.0f;
-
     const int nk = H / kLKC;
-    gload(0);
-    sstore(0);
+    wasync(0, 0);
+    xload(0);
+    xstore(0);
+    cp_async_wait<0>();
     __syncthreads();
     for (int kc = 0; kc < nk; ++kc) {
         const int b = kc & 1;
-        if (kc + 1 < nk)
-            gload((kc + 1) * kLKC);
-        // a partial unroll keeps the 8x8 tile free of register spills
-#pragma unroll 4
-        for (int k = 0; k < kLKC; ++k) {
-            float a[R], bb[R];
+        if (kc + 1 < nk) {
+            wasync(b ^ 1, (kc + 1) * kLKC);
+            xload((kc + 1) * kLKC);
+        }
+        float a[2][R], bb[2][R];
+        auto frag = [&](int s, int k) {
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 const float *ap = &xs[b][k][h2 * HALF + ty * Q];
@@ -221,35 +213,41 @@ router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr
                 if constexpr (Q == 4) {
                     const float4 av = *reinterpret_cast<const float4 *>(ap);
                     const float4 bv = *reinterpret_cast<const float4 *>(bp);
-                    a[h2 * 4] = av.x;
-                    a[h2 * 4 + 1] = av.y;
-                    a[h2 * 4 + 2] = av.z;
-                    a[h2 * 4 + 3] = av.w;
-                    bb[h2 * 4] = bv.x;
-                    bb[h2 * 4 + 1] = bv.y;
-                    bb[h2 * 4 + 2] = bv.z;
-                    bb[h2 * 4 + 3] = bv.w;
+                    a[s][h2 * 4] = av.x;
+                    a[s][h2 * 4 + 1] = av.y;
+                    a[s][h2 * 4 + 2] = av.z;
+                    a[s][h2 * 4 + 3] = av.w;
+                    bb[s][h2 * 4] = bv.x;
+                    bb[s][h2 * 4 + 1] = bv.y;
+                    bb[s][h2 * 4 + 2] = bv.z;
+                    bb[s][h2 * 4 + 3] = bv.w;
                 } else {
                     const float2 av = *reinterpret_cast<const float2 *>(ap);
                     const float2 bv = *reinterpret_cast<const float2 *>(bp);
-                    a[h2 * 2] = av.x;
-                    a[h2 * 2 + 1] = av.y;
-                    bb[h2 * 2] = bv.x;
-                    bb[h2 * 2 + 1] = bv.y;
+                    a[s][h2 * 2] = av.x;
+                    a[s][h2 * 2 + 1] = av.y;
+                    bb[s][h2 * 2] = bv.x;
+                    bb[s][h2 * 2 + 1] = bv.y;
                 }
             }
+        };
+        frag(0, 0);
+#pragma unroll
+        for (int k = 0; k < kLKC; ++k) {
+            if (k + 1 < kLKC)
+                frag((k + 1) & 1, k + 1);
 #pragma unroll
             for (int i = 0; i < R; ++i)
 #pragma unroll
                 for (int j = 0; j < R; ++j)
-                    acc[i][j] = __fmaf_rn(a[i], bb[j], acc[i][j]);
+                    acc[i][j] = __fmaf_rn(a[k & 1][i], bb[k & 1][j], acc[i][j]);
         }
-        if (kc + 1 < nk)
-            sstore(b ^ 1);
+        if (kc + 1 < nk) {
+            xstore(b ^ 1);
+            cp_async_wait<0>();
+        }
         __syncthreads();
     }
-
-    // thread (ty, tx) owns tokens {h*HALF + ty*Q + i} x experts {h*HALF + tx*Q + j}
 #pragma unroll
     for (int i = 0; i < R; ++i) {
         const int t = t0 + (i / Q) * HALF + ty * Q + (i % Q);
