@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import datetime
 import json
 import os
 import statistics
@@ -108,57 +109,92 @@ def max_over_ranks(v: float, world: int, device=None) -> float:
 # ----------------------------------------------------------------- helpers
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    """nvidia-smi clock / throttle-reason samples during the timed region.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    The sampler starts before the caller's timed region and waits (bounded)
+    for its first sample; mark_start()/mark_stop() bracket the region, and
+    only samples whose nvidia-smi timestamp falls inside it are summarised
+    (the nearest later sample when the region is shorter than the interval)."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.lines.append(line)
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except (OSError, ValueError):
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+        t_end = time.time() + 5.0
+        while not self.lines and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.01)
         return self
 
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_stop(self):
+        self.t1 = datetime.datetime.now()
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
+            time.sleep(2 * self.INTERVAL_MS / 1000.0)
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+                self.proc.wait()
+            self.thread.join(timeout=5)
         return False
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in getattr(self, "lines", []):
+        rows = []
+        for line in list(self.lines):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sel = rows
+        if self.t0 is not None and self.t1 is not None:
+            slack = datetime.timedelta(milliseconds=self.INTERVAL_MS)
+            sel = [r for r in rows if self.t0 - slack <= r[0] <= self.t1 + slack]
+            if not sel:
+                later = [r for r in rows if r[0] >= self.t0]
+                sel = later[:1] or rows[-1:]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = set()
+        for r in sel:
+            for n, v in zip(names, r[3]):
                 if v.lower() == "active":
                     reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": sel[-1][2],
+                "reasons": sorted(reasons), "samples": len(sel)}
 
 
 KERNEL_SOURCES = {
@@ -372,7 +408,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     with ClockSampler(local) as clk:
-        time.sleep(0.05)
+        clk.mark_start()
         start.record(stream)
         for i in range(args.steps):
             B.check(B.beam_moe_set_kernel_events([e[0].cuda_event for e in ev[i]],
@@ -380,6 +416,7 @@ def run_ours(args, world, rank, local):
             layer.forward(x, out)
         stop.record(stream)
         torch.cuda.synchronize()
+        clk.mark_stop()
     B.beam_moe_set_kernel_events([], [])
     barrier(world)
     launches = B.beam_moe_launch_count() - launches0
