@@ -17,6 +17,10 @@
  *            scaled by 2.5; each expert is a SwiGLU MLP of intermediate 2560.
  *  [P1-FP32] same page, section "Residual stream", last paragraph: the router
  *            and the SwiGLU product are computed in FP32.
+ *  [P1-ARCH] same page, section "Architecture: hybrid attention, grouped
+ *            experts, constant-scale residual stream", first paragraph: 52
+ *            decoder layers of hidden size 5120, the first 3 with a dense
+ *            SwiGLU MLP, the other 49 with the MoE block.
  *  [P4-MoE]  "Beam 501B open model" (aixai.ru), section "256 experts per
  *            layer": the same routing restated.
  *  [P5-MoE]  "Reflection 501B-parameter Beam model" (dothoosh.com), section
@@ -353,6 +357,40 @@ int oracle_forward(const uint16_t *x, const float *wr, const uint16_t *wg,
         free(hbuf);
         free(y);
         free(acc);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------ dense layer */
+
+/*
+ * The dense SwiGLU MLP of Beam's first three decoder layers ([P1-ARCH]: the
+ * first 3 of the 52 layers use a dense SwiGLU MLP, the other 49 the MoE
+ * block), with the SwiGLU product in FP32 ([P1-FP32]).  The pages give no
+ * intermediate size for it; I is the caller's.
+ *   x [T,H] bf16; wg, wu [I,H] bf16; wd [H,I] bf16; out [n,H] bf16 bits
+ *   (row r is token tokens[r], all tokens when tokens == NULL)
+ */
+int oracle_dense_forward(const uint16_t *x, const uint16_t *wg, const uint16_t *wu,
+                         const uint16_t *wd, int64_t T, int H, int I,
+                         const int64_t *tokens, int64_t n_tokens, uint16_t *out)
+{
+    const int64_t n = tokens ? n_tokens : T;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t t = tokens ? tokens[r] : r;
+        if (t < 0 || t >= T) {
+            bad = 1;
+            continue;
+        }
+        float *hbuf = (float *)malloc(sizeof(float) * (size_t)I);
+        double *y = (double *)malloc(sizeof(double) * (size_t)H);
+        expert_swiglu(x + t * H, wg, wu, wd, H, I, hbuf, y);
+        for (int j = 0; j < H; ++j)
+            out[r * H + j] = float_to_bf16_bits_rne((float)y[j]);
+        free(hbuf);
+        free(y);
     }
     return bad ? -1 : 0;
 }

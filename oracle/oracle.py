@@ -58,6 +58,8 @@ def lib():
         L.oracle_forward.argtypes = [p, p, p, p, p, i64, i32, i32, i32, i32, i32, i32,
                                      f32, p, i64, p, p, p]
         L.oracle_forward.restype = i32
+        L.oracle_dense_forward.argtypes = [p, p, p, p, i64, i32, i32, p, i64, p]
+        L.oracle_dense_forward.restype = i32
         L.oracle_e2m1_value.argtypes = [i32]
         L.oracle_e2m1_value.restype = f32
         L.oracle_e2m1_code.argtypes = [f32]
@@ -172,6 +174,26 @@ def forward(x_bits, router_w, wg_bits, wu_bits, wd_bits, n_groups, topk_groups, 
     if rc != 0:
         raise ValueError("oracle_forward failed (bad configuration or token index)")
     return out, ids, w
+
+
+def dense_forward(x_bits, wg_bits, wu_bits, wd_bits, tokens=None):
+    """Dense SwiGLU MLP (x [T,H], wg/wu [I,H], wd [H,I], bf16 bits) for
+    `tokens` (all when None) -> out bits [n,H] uint16."""
+    x_bits = _c(x_bits, np.uint16)
+    wg_bits = _c(wg_bits, np.uint16)
+    wu_bits = _c(wu_bits, np.uint16)
+    wd_bits = _c(wd_bits, np.uint16)
+    T, H = x_bits.shape
+    I, H2 = wg_bits.shape
+    assert H2 == H and wu_bits.shape == (I, H) and wd_bits.shape == (H, I)
+    tok = None if tokens is None else _c(np.asarray(tokens, np.int64), np.int64)
+    n = T if tok is None else tok.shape[0]
+    out = np.empty((n, H), np.uint16)
+    rc = lib().oracle_dense_forward(_ptr(x_bits), _ptr(wg_bits), _ptr(wu_bits), _ptr(wd_bits),
+                                    T, H, I, _ptr(tok), n, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_dense_forward failed (bad token index)")
+    return out
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:

@@ -235,6 +235,28 @@ def test_single_expert_layer_is_dense_swiglu(oracle_mod):
     assert (np.abs(got - ref) <= np.abs(ref) * 2 ** -8 + 1e-6).all()
 
 
+def test_dense_forward_is_swiglu_mlp(oracle_mod):
+    # The dense layer against an independent numpy SwiGLU, and equal to the
+    # single-expert layer row for row.
+    g = torch.Generator().manual_seed(23)
+    T, H, I = 12, 128, 96
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    wg = (torch.randn(I, H, generator=g) * 0.1).to(torch.bfloat16)
+    wu = (torch.randn(I, H, generator=g) * 0.1).to(torch.bfloat16)
+    wd = (torch.randn(H, I, generator=g) * 0.1).to(torch.bfloat16)
+    xb, gb, ub, db = (synth.to_bits(t) for t in (x, wg, wu, wd))
+    out = oracle_mod.dense_forward(xb, gb, ub, db)
+    ref = _np_swiglu(x.double().numpy(), wg.double().numpy(), wu.double().numpy(),
+                     wd.double().numpy())
+    got = oracle_mod.bf16_bits_to_f32(out).astype(np.float64)
+    assert (np.abs(got - ref) <= np.abs(ref) * 2 ** -8 + 1e-6).all()
+    moe, _, _ = oracle_mod.forward(xb, np.ones((H, 1), np.float32), gb[None], ub[None], db[None],
+                                   1, 1, 1, 1.0)
+    assert np.array_equal(moe, out)
+    sub = oracle_mod.dense_forward(xb, gb, ub, db, tokens=[3, 0, 11])
+    assert np.array_equal(sub, out[[3, 0, 11]])
+
+
 def test_layer_is_weighted_sum_of_expert_mlps(oracle_mod, tiny):
     # Independent composition: exhaustive-search routing + numpy expert MLPs.
     sh, d = tiny
