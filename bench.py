@@ -53,7 +53,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="decode",
-                    choices=["tiny", "decode", "prefill", "skewed", "nvfp4"])
+                    choices=["tiny", "decode", "prefill", "skewed", "nvfp4", "dense"])
     ap.add_argument("--cpu-tokens", type=int, default=16,
                     help="tokens of the batch the CPU oracle baseline computes")
     ap.add_argument("--override", default="",
@@ -329,6 +329,9 @@ def run_reference(args, world, rank):
     import torch
     from oracle import oracle
     from sparse_moe_layer_experts_b300 import synth
+    if args.config == "dense":
+        run_reference_dense(args)
+        return
     sh = synth.shape(args.config)
     # the inputs are drawn exactly as the GPU arm draws them
     dev = "cuda" if torch.cuda.is_available() else "cpu"
@@ -355,6 +358,42 @@ def run_reference(args, world, rank):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def run_reference_dense(args):
+    """Reference arm of the dense workload: the oracle's dense SwiGLU on a
+    seeded sample of the batch's tokens per step."""
+    import numpy as np
+    import torch
+    from oracle import oracle
+    from sparse_moe_layer_experts_b300 import synth
+    sh = dict(synth.DENSE_CONFIGS["dense"])
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    d = synth.make_dense_inputs(sh["T"], sh["H"], sh["I"], seed=0, device=dev)
+    xb, gb, ub, db = (synth.to_bits(d[k]) for k in ("x", "w_gate", "w_up", "w_down"))
+    del d
+    ntok = min(args.cpu_tokens, sh["T"])
+    toks = sorted(np.random.default_rng(0).choice(sh["T"], size=ntok, replace=False).tolist())
+    times = []
+    for _ in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.dense_forward(xb, gb, ub, db, tokens=toks)
+        times.append(time.perf_counter() - t0)
+    total = sum(times[args.warmup:])
+    value = ntok * args.steps / total
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "Beam dense SwiGLU layer tokens/s at 1 B300 (first three decoder layers)",
+        "value": value, "unit": UNIT, "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32/f64", "data": "synthetic",
+        "config": {"workload": f"dense: T={sh['T']} tokens, hidden {sh['H']}, "
+                               f"intermediate {sh['I']}",
+                   "sample": f"{ntok} seeded tokens of the batch per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(oracle.num_threads(), ntok),
+                         "kind": "oracle", "sample": f"{ntok} seeded tokens per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
 
 
 def run_ours(args, world, rank, local):
@@ -549,6 +588,107 @@ def run_route_only(args):
                       "router_tflops": gflop / ms["router_scores"]}), flush=True)
 
 
+def run_dense(args, world, rank, local):
+    """Dense SwiGLU layer (Beam's first three decoder layers) through
+    beam_moe_dense_forward: a second workload of the same GEMM kernels."""
+    import torch
+    from sparse_moe_layer_experts_b300 import binding as B, synth
+    from sparse_moe_layer_experts_b300.layer import DenseSwiGLU
+    from oracle import oracle
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sh = dict(synth.DENSE_CONFIGS["dense"])
+    sh.update(parse_override(args.override))
+    T, H, I = sh["T"], sh["H"], sh["I"]
+    d = synth.make_dense_inputs(T, H, I, seed=rank, device=dev)
+    layer = DenseSwiGLU(d["w_gate"], d["w_up"], d["w_down"])
+    x, out = d["x"], torch.empty_like(d["x"])
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        layer.forward(x, out)
+    torch.cuda.synchronize()
+    nst = len(B.KERNEL_STAGES)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nst)] for _ in range(args.steps)]
+    for pair in ev:
+        for e0, e1 in pair:
+            e0.record(stream)
+            e1.record(stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = B.beam_moe_launch_count()
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        clk.mark_start()
+        start.record(stream)
+        for i in range(args.steps):
+            B.check(B.beam_moe_set_kernel_events([e[0].cuda_event for e in ev[i]],
+                                                 [e[1].cuda_event for e in ev[i]]), "events")
+            layer.forward(x, out)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        clk.mark_stop()
+    B.beam_moe_set_kernel_events([], [])
+    barrier(world)
+    launches = B.beam_moe_launch_count() - launches0
+    ms_max = max_over_ranks(start.elapsed_time(stop), world, dev)
+    if layer.status() != 0:
+        raise SystemExit("device status word reports an error in the timed region")
+    used = {"scan": "setup", "gateup_gemm": "gateup_gemm", "down_gemm": "down_gemm"}
+    per_kernel_ms = {used[name]: sum(ev[i][j][0].elapsed_time(ev[i][j][1])
+                                     for i in range(args.steps)) / args.steps
+                     for j, name in enumerate(B.KERNEL_STAGES) if name in used}
+    value = world * T * args.steps / (ms_max / 1e3)
+    peaks, peak_src = load_peaks()
+    flops = {"gateup_gemm": 4.0 * T * H * I, "down_gemm": 2.0 * T * H * I}
+    dom = max(flops, key=lambda k: per_kernel_ms[k])
+    achieved = flops[dom] / (per_kernel_ms[dom] / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+            "kernel": dom, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)",
+            "algorithmic_flops_per_launch": flops[dom]}
+    t_step = ms_max / args.steps / 1e3
+    layer_roof = {"tensor_frac": 6.0 * T * H * I / t_step / 1e12 / peaks["bf16_tflops"],
+                  "hbm_frac": (3.0 * H * I * 2 + 2 * T * H * 2) / t_step / 1e9 / peaks["hbm_gbs"]}
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            xd = xh.to(dev, non_blocking=True)
+            layer.forward(xd, out)
+            oh.copy_(out, non_blocking=True)
+            torch.cuda.synchronize()
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": world * T * args.steps / dt, "unit": UNIT,
+               "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        toks = list(range(0, T, max(1, T // args.cpu_tokens)))[:args.cpu_tokens]
+        xb, gb, ub, db = (synth.to_bits(d[k]) for k in ("x", "w_gate", "w_up", "w_down"))
+        t0 = time.perf_counter()
+        oracle.dense_forward(xb, gb, ub, db, tokens=toks)
+        dtc = time.perf_counter() - t0
+        cpu = {"value": len(toks) / dtc, "unit": UNIT, "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": f"{len(toks)} seeded tokens of the dense batch ({dtc:.1f} s)"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": "Beam dense SwiGLU layer tokens/s at 1 B300 (first three decoder layers)",
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02) bf16 weights)",
+            "config": {"workload": f"dense: T={T} tokens, hidden {H}, intermediate {I}",
+                       "tokens_per_step_per_gpu": T,
+                       "l2": "no flush: the 0.63 GB of weights read per step exceed the 126 MB L2",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "layer_roofline": layer_roof, "kernels_ms": per_kernel_ms,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk.summary(),
+        }), flush=True)
+
+
 def main():
     args = parse_args()
     if args.route_only:
@@ -557,6 +697,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.config == "dense":
+        run_dense(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -228,6 +228,29 @@ int beam_moe_quantize_nvfp4(const void *w, int64_t n_mat, int64_t rows,
                             float *global_sf, void *stream);
 
 /*
+ * Dense SwiGLU MLP, the feed-forward block of Beam's first three decoder
+ * layers ("Reflection Beam 1.0", section "Architecture: hybrid attention,
+ * grouped experts, constant-scale residual stream": the first 3 of the 52
+ * layers use a dense SwiGLU MLP, the other 49 the MoE block).  The pages
+ * give no intermediate size for it: cfg->inter is the caller's.
+ *   out[t] = bf16( (silu(x[t] . Wg^T) * (x[t] . Wu^T)) . Wd^T )
+ * with FP32 accumulation and the SiLU*up product in FP32 (h is rounded to
+ * bf16 as the operand of the second GEMM, as in the MoE experts).
+ *   x      [T,H] bf16, device        w_gate, w_up [I,H] bf16, device
+ *   w_down [H,I] bf16, device        out [T,H] bf16, device, written
+ * Uses cfg->hidden (H), cfg->inter (I), cfg->workspace/workspace_bytes
+ * (>= beam_moe_dense_workspace_size) and cfg->wait_timeout_ns; the routing
+ * fields are ignored.  Requirements: H and I multiples of 128, bf16 weights
+ * (BEAM_MOE_ERR_UNSUPPORTED for NVFP4), 16-byte aligned pointers, out not
+ * overlapping x.  Asynchronous on `stream`; T = 0 is a no-op; device errors
+ * land in the workspace status word (beam_moe_read_status).  Deterministic.
+ */
+size_t beam_moe_dense_workspace_size(int64_t T, const beam_moe_cfg *cfg);
+int beam_moe_dense_forward(const void *x, const void *w_gate, const void *w_up,
+                           const void *w_down, int64_t T, const beam_moe_cfg *cfg,
+                           void *out, void *stream);
+
+/*
  * Synchronise `stream`, read the device status word of cfg->workspace and
  * clear it.  Returns BEAM_MOE_OK, BEAM_MOE_ERR_TIMEOUT or BEAM_MOE_ERR_DEVICE
  * (or BEAM_MOE_ERR_CUDA if the synchronisation itself failed).

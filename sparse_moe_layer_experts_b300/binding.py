@@ -92,6 +92,10 @@ def lib():
         L.beam_moe_set_kernel_events.restype = ctypes.c_int
         L.beam_moe_device_sms.argtypes = []
         L.beam_moe_device_sms.restype = ctypes.c_int
+        L.beam_moe_dense_workspace_size.argtypes = [i64, cfgp]
+        L.beam_moe_dense_workspace_size.restype = sz
+        L.beam_moe_dense_forward.argtypes = [vp, vp, vp, vp, i64, cfgp, vp, vp]
+        L.beam_moe_dense_forward.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -127,6 +131,14 @@ def beam_moe_forward_hostio(x_host, router_w, w_gate, w_up, w_down, T, cfg, out_
                             stream) -> int:
     return lib().beam_moe_forward_hostio(x_host, router_w, w_gate, w_up, w_down, T,
                                          ctypes.byref(cfg), out_host, stream)
+
+
+def beam_moe_dense_workspace_size(T: int, cfg: beam_moe_cfg) -> int:
+    return int(lib().beam_moe_dense_workspace_size(T, ctypes.byref(cfg)))
+
+
+def beam_moe_dense_forward(x, w_gate, w_up, w_down, T, cfg, out, stream) -> int:
+    return lib().beam_moe_dense_forward(x, w_gate, w_up, w_down, T, ctypes.byref(cfg), out, stream)
 
 
 def beam_moe_quantize_nvfp4(w, n_mat, rows, cols, packed, block_sf, global_sf, stream) -> int:

@@ -337,6 +337,80 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     return BEAM_MOE_OK;
 }
 
+// ---- dense SwiGLU layers (the first three decoder layers): the same
+// grouped GEMMs with one segment of all T rows, x read in place and the
+// down GEMM writing the output rows.
+struct DenseLayout {
+    size_t status, offsets, chunk_start, h, total;
+};
+
+DenseLayout make_dense_layout(int64_t T, const beam_moe_cfg &c)
+{
+    DenseLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes);
+        return at;
+    };
+    L.status = take(256);
+    L.offsets = take(sizeof(int32_t) * 2);
+    L.chunk_start = take(sizeof(int32_t) * 2);
+    L.h = take((size_t)2 * T * c.inter);
+    L.total = o;
+    return L;
+}
+
+int check_dense_cfg(const beam_moe_cfg *c)
+{
+    if (!c)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (c->hidden <= 0 || c->inter <= 0 || c->hidden % 128 || c->inter % 128)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (c->wtype != BEAM_MOE_W_BF16)
+        return c->wtype == BEAM_MOE_W_NVFP4 ? BEAM_MOE_ERR_UNSUPPORTED : BEAM_MOE_ERR_INVALID_ARG;
+    return BEAM_MOE_OK;
+}
+
+int run_dense(const void *x, const void *w_gate, const void *w_up, const void *w_down, int64_t T,
+              const beam_moe_cfg &c, void *out, cudaStream_t s)
+{
+    const DenseLayout L = make_dense_layout(T, c);
+    void *ws = c.workspace;
+    const int H = c.hidden, I = c.inter;
+    const GemmVariant v = T <= 16 ? GemmVariant::kDecode : GemmVariant::kPrefill;
+    BEAM_CUDA(launch_dense_setup((int)T, gemm_chunk_rows(v), at<int32_t>(ws, L.offsets),
+                                 at<int32_t>(ws, L.chunk_start), at<int>(ws, L.status), s));
+    const uint32_t box = (uint32_t)gemm_box_rows(v);
+    CUtensorMap m_wg, m_wu, m_wd, m_x, m_h;
+    if (!make_map(&m_wg, w_gate, H, (uint64_t)I, 128) ||
+        !make_map(&m_wu, w_up, H, (uint64_t)I, 128) ||
+        !make_map(&m_wd, w_down, I, (uint64_t)H, 128) ||
+        !make_map(&m_x, x, H, (uint64_t)T, box) ||
+        !make_map(&m_h, at<void>(ws, L.h), I, (uint64_t)T, box))
+        return BEAM_MOE_ERR_CUDA;
+    const int sms = device_sms();
+    if (sms <= 0)
+        return BEAM_MOE_ERR_CUDA;
+    GemmArgs a{};
+    a.offsets = at<int32_t>(ws, L.offsets);
+    a.chunk_start = at<int32_t>(ws, L.chunk_start);
+    a.E = 1;
+    a.status = at<int>(ws, L.status);
+    a.timeout_ns = c.wait_timeout_ns > 0 ? (unsigned long long)c.wait_timeout_ns : kDefaultTimeoutNs;
+    a.m_tiles = I / 128;
+    a.ksteps = H / 64;
+    a.out = at<void>(ws, L.h);
+    a.out_ld = I;
+    BEAM_CUDA(launch_gateup(v, m_wg, m_wu, m_x, a, sms, s));
+    a.m_tiles = H / 128;
+    a.ksteps = I / 64;
+    a.out = out;
+    a.out_ld = H;
+    BEAM_CUDA(launch_down(v, m_wd, m_h, a, sms, s));
+    return BEAM_MOE_OK;
+}
+
 }  // namespace
 }  // namespace beam
 
@@ -536,5 +610,32 @@ int beam_moe_set_kernel_events(void *const *start, void *const *stop, int n)
 }
 
 int beam_moe_device_sms(void) { return device_sms(); }
+
+size_t beam_moe_dense_workspace_size(int64_t T, const beam_moe_cfg *cfg)
+{
+    if (check_dense_cfg(cfg) != BEAM_MOE_OK || T < 0)
+        return 0;
+    return make_dense_layout(T, *cfg).total;
+}
+
+int beam_moe_dense_forward(const void *x, const void *w_gate, const void *w_up, const void *w_down,
+                           int64_t T, const beam_moe_cfg *cfg, void *out, void *stream)
+{
+    int rc = check_dense_cfg(cfg);
+    if (rc != BEAM_MOE_OK)
+        return rc;
+    if (T < 0 || T > (int64_t(1) << 24))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_MOE_OK;
+    if (!x || !w_gate || !w_up || !w_down || !out)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+        !aligned16(out))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(T, cfg, make_dense_layout(T, *cfg).total)) != BEAM_MOE_OK)
+        return rc;
+    return run_dense(x, w_gate, w_up, w_down, T, *cfg, out, static_cast<cudaStream_t>(stream));
+}
 
 }  // extern "C"

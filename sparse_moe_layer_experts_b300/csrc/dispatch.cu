@@ -314,6 +314,20 @@ combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ w,
     }
 }
 
+
+// Dense layers: the whole batch is one segment, offsets {0, T}, cut into
+// ceil(T / chunk_rows) token chunks; also resets the call's status word.
+__global__ void dense_setup_kernel(int T, int chunk_rows, int32_t *__restrict__ offsets,
+                                   int32_t *__restrict__ chunk_start, int *__restrict__ status)
+{
+    if (threadIdx.x == 0) {
+        offsets[0] = 0;
+        offsets[1] = T;
+        chunk_start[0] = 0;
+        chunk_start[1] = (T + chunk_rows - 1) / chunk_rows;
+        *status = 0;
+    }
+}
 }  // namespace
 
 cudaError_t launch_hist(const int32_t *ids, int T, int K, int E, int32_t *local_rank,
@@ -395,6 +409,15 @@ cudaError_t launch_combine(const uint16_t *y, const float *w, const int32_t *row
     stage_begin(kStCombine, s);
     combine_kernel<<<T, 256, 0, s>>>(y, w, row_of, T, K, H, out);
     stage_end(kStCombine, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dense_setup(int T, int chunk_rows, int32_t *offsets, int32_t *chunk_start,
+                               int *status, cudaStream_t s)
+{
+    stage_begin(kStScan, s);
+    dense_setup_kernel<<<1, 32, 0, s>>>(T, chunk_rows, offsets, chunk_start, status);
+    stage_end(kStScan, s);
     return cudaGetLastError();
 }
 

@@ -69,6 +69,9 @@ cudaError_t launch_quantize_rows(const float *in, int64_t rows, int cols, const 
                                  bool rep_layout, uint8_t *codes, uint8_t *sf, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t *y, const float *w, const int32_t *row_of, int T, int K,
                            int H, uint16_t *out, cudaStream_t s);
+// dense layers: offsets {0, T}, chunk_start {0, ceil(T/chunk_rows)}, status 0
+cudaError_t launch_dense_setup(int T, int chunk_rows, int32_t *offsets, int32_t *chunk_start,
+                               int *status, cudaStream_t s);
 
 // ---- grouped_gemm.cu
 struct GemmArgs {

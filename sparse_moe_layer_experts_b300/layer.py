@@ -138,3 +138,49 @@ class BeamMoE:
 
     def status(self, stream=None) -> int:
         return B.beam_moe_read_status(self.cfg, _stream_handle(stream))
+
+
+class DenseSwiGLU:
+    """Dense SwiGLU MLP with resident bf16 weights: w_gate/w_up [I,H],
+    w_down [H,I], contiguous on one CUDA device."""
+
+    def __init__(self, w_gate, w_up, w_down, wait_timeout_ns=0):
+        I, H = w_gate.shape
+        for t, shape in ((w_gate, (I, H)), (w_up, (I, H)), (w_down, (H, I))):
+            if (tuple(t.shape) != shape or t.dtype != torch.bfloat16 or not t.is_cuda
+                    or not t.is_contiguous()):
+                raise ValueError(f"expected contiguous CUDA bf16 of shape {shape}")
+        self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
+        self.H, self.I = H, I
+        self.cfg = B.beam_moe_cfg()
+        self.cfg.hidden, self.cfg.inter = H, I
+        self.cfg.wtype = B.BEAM_MOE_W_BF16
+        self.cfg.wait_timeout_ns = wait_timeout_ns
+        self.device = w_gate.device
+        self._ws = None
+
+    def workspace(self, T: int) -> torch.Tensor:
+        need = B.beam_moe_dense_workspace_size(T, self.cfg)
+        if need == 0:
+            raise ValueError("invalid layer configuration")
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        self.cfg.workspace = self._ws.data_ptr()
+        self.cfg.workspace_bytes = self._ws.numel()
+        return self._ws
+
+    def forward(self, x, out=None, stream=None):
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != self.H or not x.is_contiguous():
+            raise ValueError("x must be contiguous bf16 [T, H]")
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty_like(x)
+        self.workspace(T)
+        B.check(B.beam_moe_dense_forward(x.data_ptr(), self.w_gate.data_ptr(), self.w_up.data_ptr(),
+                                         self.w_down.data_ptr(), T, self.cfg, out.data_ptr(),
+                                         _stream_handle(stream)), "beam_moe_dense_forward")
+        return out
+
+    def status(self, stream=None) -> int:
+        return B.beam_moe_read_status(self.cfg, _stream_handle(stream))
+

@@ -18,6 +18,15 @@ expert's rank r).  The layer itself has no bias term, so the shift is carried
 by the inputs: hidden channel 0 of every token is set to 1.0 and router row 0
 is set to b.  The logit of expert e then contains exactly 1.0 * b_e.
 
+Dense SwiGLU layers (Beam's first three decoder layers) draw
+  x        [T,H]    N(0,1) bf16                                     sub-seed 10
+  w_gate   [I,H]    N(0,0.02) bf16                                  sub-seed 11
+  w_up     [I,H]    same                                            sub-seed 12
+  w_down   [H,I]    same                                            sub-seed 13
+The pages give no intermediate size for the dense layers; the "dense"
+workload takes I = 8 * 2560 = 20480, the FFN width one MoE layer's eight
+active experts add up to.
+
 Tensors are drawn on ``device``.  CPU and CUDA generators produce different
 streams, so a test draws each tensor once and hands the same tensor to both
 sides.
@@ -38,6 +47,10 @@ CONFIGS = {
                    routing="zipf"),
     "nvfp4": dict(T=8192, H=5120, I=2560, E=256, G=8, topk_groups=4, top_k=8,
                   routing="random"),
+}
+
+DENSE_CONFIGS = {
+    "dense": dict(T=4096, H=5120, I=20480),
 }
 
 ROUTED_SCALE = 2.5
@@ -111,6 +124,18 @@ def make_inputs(sh: LayerShape, seed: int = 0, device="cpu", weights=True):
         d["w_up"] = _normal_bf16((sh.E, sh.I, sh.H), 0.02, _gen(dev, seed, 3), dev, chunk)
         d["w_down"] = _normal_bf16((sh.E, sh.H, sh.I), 0.02, _gen(dev, seed, 4), dev, chunk)
     return d
+
+
+def make_dense_inputs(T: int, H: int, I: int, seed: int = 0, device="cpu"):
+    """x [T,H], w_gate/w_up [I,H], w_down [H,I] per the module recipe."""
+    dev = torch.device(device)
+    chunk = 1024 if I * H > (1 << 26) else None
+    return dict(
+        x=_normal_bf16((T, H), 1.0, _gen(dev, seed, 10), dev),
+        w_gate=_normal_bf16((I, H), 0.02, _gen(dev, seed, 11), dev, chunk),
+        w_up=_normal_bf16((I, H), 0.02, _gen(dev, seed, 12), dev, chunk),
+        w_down=_normal_bf16((H, I), 0.02, _gen(dev, seed, 13), dev, chunk),
+    )
 
 
 def to_bits(t: torch.Tensor):

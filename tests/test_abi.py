@@ -114,3 +114,20 @@ def test_status_strings(L):
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert B.beam_moe_status_string(code) != "unknown status"
     assert B.beam_moe_status_string(12345) == "unknown status"
+
+
+def test_dense_entry_point_checks(L):
+    c = B.beam_moe_cfg()
+    c.hidden, c.inter, c.wtype = 256, 384, B.BEAM_MOE_W_BF16
+    assert B.beam_moe_dense_workspace_size(64, c) > 64 * 384 * 2
+    before = B.beam_moe_launch_count()
+    assert B.beam_moe_dense_forward(None, None, None, None, 0, c, None, None) == B.BEAM_MOE_OK
+    assert B.beam_moe_dense_forward(16, 16, 16, 16, 4, c, 16, None) == B.BEAM_MOE_ERR_WORKSPACE
+    assert B.beam_moe_dense_forward(18, 16, 16, 16, 4, c, 16, None) == B.BEAM_MOE_ERR_INVALID_ARG
+    c.inter = 100
+    assert B.beam_moe_dense_forward(16, 16, 16, 16, 4, c, 16, None) == B.BEAM_MOE_ERR_INVALID_ARG
+    c.inter, c.wtype = 384, B.BEAM_MOE_W_NVFP4
+    assert B.beam_moe_dense_forward(16, 16, 16, 16, 4, c, 16, None) == B.BEAM_MOE_ERR_UNSUPPORTED
+    assert B.beam_moe_dense_workspace_size(64, c) == 0
+    assert B.beam_moe_launch_count() == before
+
