@@ -21,6 +21,11 @@
  *            experts, constant-scale residual stream", first paragraph: 52
  *            decoder layers of hidden size 5120, the first 3 with a dense
  *            SwiGLU MLP, the other 49 with the MoE block.
+ *  [P1-RES]  same page, section "Residual stream: a constant scale with
+ *            depth-dependent weights": the input embedding is step 1; at step
+ *            k the sublayer output is added with weight 1/sqrt(k) and the
+ *            stream kept with weight sqrt((k-1)/k); every sublayer is also
+ *            normalised before and after, and normalisations run in FP32.
  *  [P4-MoE]  "Beam 501B open model" (aixai.ru), section "256 experts per
  *            layer": the same routing restated.
  *  [P5-MoE]  "Reflection 501B-parameter Beam model" (dothoosh.com), section
@@ -393,6 +398,116 @@ int oracle_dense_forward(const uint16_t *x, const uint16_t *wg, const uint16_t *
         free(y);
     }
     return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------ fused MoE block */
+
+/*
+ * RMS normalisation of one row ([P1-RES]: sublayers are normalised before
+ * and after, in FP32; the pages name RMSNorm for queries and keys and no
+ * other norm, so the reading is RMSNorm with a learned per-channel gain).
+ * The sum of squares is accumulated in FP64 and rounded to FP32 once as a
+ * mean; r = 1 / sqrt(mean + eps) in FP32; v[h] * r * gamma[h] in FP32.
+ */
+static float rms_inv(const float *v, int n, float eps)
+{
+    double ss = 0.0;
+    for (int h = 0; h < n; ++h)
+        ss += (double)v[h] * (double)v[h];
+    const float mean = (float)(ss / (double)n);
+    return 1.0f / sqrtf(mean + eps);
+}
+
+/*
+ * One MoE sublayer of the decoder with its norms and residual ([P1-RES]):
+ *   x  = bf16( rmsnorm(s) * gamma_pre )        the layer's bf16 input
+ *   o  = MoE(x) in FP32 (combine before the output rounding)
+ *   z  = rmsnorm(o) * gamma_post               FP32
+ *   s' = bf16( a*s + b*z ),  a = sqrt((k-1)/k), b = 1/sqrt(k) (FP32)
+ *   s  [T,H] bf16 bits (the residual stream at step k-1); out [n,H] bf16
+ *   bits (row r is token tokens[r], all tokens when tokens == NULL).
+ */
+int oracle_block_forward(const uint16_t *s, int step, const float *gamma_pre,
+                         const float *gamma_post, float eps, const float *wr,
+                         const uint16_t *wg, const uint16_t *wu, const uint16_t *wd,
+                         int64_t T, int H, int I, int E, int G, int topk_groups,
+                         int top_k, float scale, const int64_t *tokens, int64_t n_tokens,
+                         uint16_t *out)
+{
+    if (step < 1 || E % G != 0 || top_k > topk_groups * (E / G))
+        return -1;
+    const float a = (float)sqrt((double)(step - 1) / (double)step);
+    const float b = (float)(1.0 / sqrt((double)step));
+    const int64_t n = tokens ? n_tokens : T;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t t = tokens ? tokens[r] : r;
+        if (t < 0 || t >= T) {
+            bad = 1;
+            continue;
+        }
+        float *sv = (float *)malloc(sizeof(float) * (size_t)H);
+        uint16_t *xb = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)H);
+        float *o = (float *)malloc(sizeof(float) * (size_t)H);
+        float *scores = (float *)malloc(sizeof(float) * (size_t)E);
+        int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)top_k);
+        float *w = (float *)malloc(sizeof(float) * (size_t)top_k);
+        float *hbuf = (float *)malloc(sizeof(float) * (size_t)I);
+        double *y = (double *)malloc(sizeof(double) * (size_t)H);
+        double *acc = (double *)calloc((size_t)H, sizeof(double));
+
+        for (int h = 0; h < H; ++h)
+            sv[h] = bf16_bits_to_float(s[t * H + h]);
+        const float rp = rms_inv(sv, H, eps);
+        for (int h = 0; h < H; ++h) {
+            const float v = sv[h] * rp;
+            xb[h] = float_to_bf16_bits_rne(v * gamma_pre[h]);
+        }
+        oracle_router_scores(xb, wr, 1, H, E, NULL, scores);
+        if (oracle_select(scores, 1, E, G, topk_groups, top_k, scale, ids, w) != 0)
+            bad = 1;
+        for (int k = 0; k < top_k && !bad; ++k) {
+            const int64_t e = ids[k];
+            expert_swiglu(xb, wg + e * I * H, wu + e * I * H, wd + e * H * I, H, I, hbuf, y);
+            for (int j = 0; j < H; ++j)
+                acc[j] += (double)w[k] * y[j];
+        }
+        for (int j = 0; j < H; ++j)
+            o[j] = (float)acc[j];
+        const float rq = rms_inv(o, H, eps);
+        for (int j = 0; j < H; ++j) {
+            const float z = (o[j] * rq) * gamma_post[j];
+            out[r * H + j] = float_to_bf16_bits_rne(a * sv[j] + b * z);
+        }
+        free(sv);
+        free(xb);
+        free(o);
+        free(scores);
+        free(ids);
+        free(w);
+        free(hbuf);
+        free(y);
+        free(acc);
+    }
+    return bad ? -1 : 0;
+}
+
+/* the pre-norm alone, for its pins: x = bf16(rmsnorm(s) * gamma) */
+void oracle_rmsnorm_bf16(const uint16_t *s, const float *gamma, float eps, int64_t T, int H,
+                         uint16_t *x)
+{
+    float *sv = (float *)malloc(sizeof(float) * (size_t)H);
+    for (int64_t t = 0; t < T; ++t) {
+        for (int h = 0; h < H; ++h)
+            sv[h] = bf16_bits_to_float(s[t * H + h]);
+        const float rp = rms_inv(sv, H, eps);
+        for (int h = 0; h < H; ++h) {
+            const float v = sv[h] * rp;
+            x[t * H + h] = float_to_bf16_bits_rne(v * gamma[h]);
+        }
+    }
+    free(sv);
 }
 
 /* ------------------------------------------------------------------ NVFP4 */

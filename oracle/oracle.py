@@ -60,6 +60,11 @@ def lib():
         L.oracle_forward.restype = i32
         L.oracle_dense_forward.argtypes = [p, p, p, p, i64, i32, i32, p, i64, p]
         L.oracle_dense_forward.restype = i32
+        L.oracle_block_forward.argtypes = [p, i32, p, p, f32, p, p, p, p, i64, i32, i32, i32,
+                                           i32, i32, i32, f32, p, i64, p]
+        L.oracle_block_forward.restype = i32
+        L.oracle_rmsnorm_bf16.argtypes = [p, p, f32, i64, i32, p]
+        L.oracle_rmsnorm_bf16.restype = None
         L.oracle_e2m1_value.argtypes = [i32]
         L.oracle_e2m1_value.restype = f32
         L.oracle_e2m1_code.argtypes = [f32]
@@ -194,6 +199,42 @@ def dense_forward(x_bits, wg_bits, wu_bits, wd_bits, tokens=None):
     if rc != 0:
         raise ValueError("oracle_dense_forward failed (bad token index)")
     return out
+
+
+def block_forward(s_bits, step, gamma_pre, gamma_post, eps, router_w, wg_bits, wu_bits, wd_bits,
+                  n_groups, topk_groups, top_k, scale, tokens=None):
+    """MoE sublayer with pre-norm, post-norm and the constant-scale residual
+    at step `step`: the new stream rows (bf16 bits [n,H]) for `tokens`."""
+    s_bits = _c(s_bits, np.uint16)
+    gp = _c(gamma_pre, np.float32)
+    gq = _c(gamma_post, np.float32)
+    router_w = _c(router_w, np.float32)
+    wg_bits = _c(wg_bits, np.uint16)
+    wu_bits = _c(wu_bits, np.uint16)
+    wd_bits = _c(wd_bits, np.uint16)
+    T, H = s_bits.shape
+    E, I, _ = wg_bits.shape
+    assert gp.shape == (H,) and gq.shape == (H,) and router_w.shape == (H, E)
+    tok = None if tokens is None else _c(np.asarray(tokens, np.int64), np.int64)
+    n = T if tok is None else tok.shape[0]
+    out = np.empty((n, H), np.uint16)
+    rc = lib().oracle_block_forward(_ptr(s_bits), int(step), _ptr(gp), _ptr(gq), float(eps),
+                                    _ptr(router_w), _ptr(wg_bits), _ptr(wu_bits), _ptr(wd_bits),
+                                    T, H, I, E, n_groups, topk_groups, top_k, float(scale),
+                                    _ptr(tok), n, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_block_forward failed (bad configuration, step or token)")
+    return out
+
+
+def rmsnorm_bf16(s_bits, gamma, eps):
+    """x = bf16(rmsnorm(s) * gamma) row by row (bf16 bits in and out)."""
+    s_bits = _c(s_bits, np.uint16)
+    g = _c(gamma, np.float32)
+    T, H = s_bits.shape
+    x = np.empty((T, H), np.uint16)
+    lib().oracle_rmsnorm_bf16(_ptr(s_bits), _ptr(g), float(eps), T, H, _ptr(x))
+    return x
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
