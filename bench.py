@@ -33,6 +33,11 @@ sys.path.insert(0, ROOT)
 METRIC = "Beam MoE-layer tokens/s at 1 B300; % of HBM (decode) / tensor (prefill) roofline"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# fused-block runs: the first MoE sublayer of the decoder is step 9 of the
+# residual stream (embedding 1, then attention and MLP of layers 0-2 and
+# the attention of layer 3)
+BLOCK_STEP = 9
+BLOCK_EPS = 1e-6
 # ratio of nominal dense fp4 to bf16 tensor rates
 NVFP4_OVER_BF16 = 13.5 / 2.25
 
@@ -61,6 +66,9 @@ def parse_args():
     ap.add_argument("--route-only", action="store_true",
                     help="profiling mode: time only the routing kernels (no expert weights "
                          "are allocated); prints a diagnostic line, not a bench line")
+    ap.add_argument("--block", action="store_true",
+                    help="time the fused block (pre-norm, MoE, post-norm, residual at step 9) "
+                         "instead of the bare layer (bf16 configs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -258,6 +266,7 @@ def workload_algorithmic(sh, n_active: int, nvfp4: bool = False):
         "down_gemm": dict(bytes=int(w_d + R * I * ab + R * H * 2), flops=2 * R * I * H),
         "combine": dict(bytes=R * H * 2 + T * H * 2 + R * 8, flops=2 * R * H),
         "quantize_h": dict(bytes=int(R * I * (4 + 0.5625)), flops=0),
+        "prenorm": dict(bytes=2 * T * H * 2 + H * 4, flops=0),
         "layer": dict(bytes=w_gu + w_d + H * E * 4 + 2 * T * H * 2,
                       flops=2 * T * H * E + 6 * R * H * I),
     }
@@ -423,13 +432,20 @@ def run_ours(args, world, rank, local):
                         topk_groups=sh.topk_groups, top_k=sh.top_k, routed_scale=sh.scale)
     x = d["x"]
     out = torch.empty_like(x)
+    if args.block:
+        if nvfp4:
+            raise SystemExit("--block runs the bf16 configs")
+        gp, gq = synth.make_block_gains(sh.H, seed=0, device=dev)
+        step_fn = lambda: layer.block_forward(x, BLOCK_STEP, gp, gq, BLOCK_EPS, out=out)
+    else:
+        step_fn = lambda: layer.forward(x, out)
     r = layer.route(x, want_scores=False)
     counts = r["counts"].cpu().numpy()
     n_active = int((counts > 0).sum())
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
-        layer.forward(x, out)
+        step_fn()
     torch.cuda.synchronize()
     if layer.status() != 0:
         raise SystemExit("device status word reports an error during warm-up")
@@ -452,7 +468,7 @@ def run_ours(args, world, rank, local):
         for i in range(args.steps):
             B.check(B.beam_moe_set_kernel_events([e[0].cuda_event for e in ev[i]],
                                                  [e[1].cuda_event for e in ev[i]]), "events")
-            layer.forward(x, out)
+            step_fn()
         stop.record(stream)
         torch.cuda.synchronize()
         clk.mark_stop()
@@ -465,19 +481,27 @@ def run_ours(args, world, rank, local):
         raise SystemExit("device status word reports an error in the timed region")
     per_kernel_ms = {name: sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps))
                      / args.steps for j, name in enumerate(B.KERNEL_STAGES)
-                     if nvfp4 or name != "quantize_h"}
+                     if (nvfp4 or name != "quantize_h") and (args.block or name != "prenorm")}
 
     # end to end through the host-I/O entry point (pinned host buffers)
     e2e = None
     if not args.no_e2e:
         xh = x.cpu().pin_memory()
         oh = torch.empty_like(xh).pin_memory()
+        if args.block:  # host copies around the block call, through torch
+            def host_step():
+                x.copy_(xh, non_blocking=True)
+                step_fn()
+                oh.copy_(out, non_blocking=True)
+                torch.cuda.synchronize()
+        else:
+            host_step = lambda: layer.forward_host(xh, oh)
         for _ in range(max(1, args.warmup)):
-            layer.forward_host(xh, oh)
+            host_step()
         barrier(world)
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            layer.forward_host(xh, oh)
+            host_step()
         dt = max_over_ranks(time.perf_counter() - t0, world, dev)
         nbytes = sh.T * sh.H * 2
         e2e = {"value": world * sh.T * args.steps / dt, "unit": UNIT,
@@ -534,7 +558,9 @@ def run_ours(args, world, rank, local):
             "data": "synthetic (seeded N(0,1) activations, N(0,0.02) bf16 weights)",
             "config": {"workload": f"{args.config}{'(' + args.override + ')' if args.override else ''}: T={sh.T} tokens, hidden {sh.H}, "
                                    f"intermediate {sh.I}, {sh.E} experts in {sh.G} groups, "
-                                   f"top-{sh.topk_groups} groups, top-{sh.top_k}",
+                                   f"top-{sh.topk_groups} groups, top-{sh.top_k}"
+                                   + (f"; fused block: RMS pre-norm, the layer, RMS post-norm, "
+                                      f"residual step {BLOCK_STEP}" if args.block else ""),
                        "tokens_per_step_per_gpu": sh.T, "active_experts": n_active,
                        "max_expert_load_over_mean": float(counts.max() / counts.mean()),
                        "l2": "no flush: expert weights read per step exceed the 126 MB L2",

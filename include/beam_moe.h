@@ -251,6 +251,35 @@ int beam_moe_dense_forward(const void *x, const void *w_gate, const void *w_up,
                            void *out, void *stream);
 
 /*
+ * One MoE sublayer of the decoder with its norms and residual update
+ * ("Reflection Beam 1.0", section "Residual stream: a constant scale with
+ * depth-dependent weights": the input embedding is step 1; at step k the
+ * sublayer output is added with weight 1/sqrt(k) and the stream kept with
+ * weight sqrt((k-1)/k); every sublayer is normalised before and after, and
+ * normalisations run in FP32).  Readings where the pages are silent: the
+ * norm is RMSNorm with a per-channel gain; the sum of squares is
+ * accumulated in FP64 and rounded to FP32 once as a mean; r = 1/sqrt(mean +
+ * eps) in FP32; the stream is bf16.
+ *   x      = bf16( (s * r_s) * norm_pre )            the MoE layer's input
+ *   o      = the layer's FP32 combine of the K expert rows (no bf16 rounding)
+ *   z      = (o * r_o) * norm_post
+ *   s_out  = bf16( a * s + b * z ),  a = sqrt((step-1)/step), b = 1/sqrt(step)
+ *   stream_in  [T,H] bf16, device (the residual stream at step-1)
+ *   norm_pre, norm_post [H] fp32, device;  eps in [0, 1]
+ *   stream_out [T,H] bf16, device, written; may be stream_in (in place), must
+ *              not partly overlap it
+ * Routing and experts as beam_moe_forward on x (bf16 weights only:
+ * BEAM_MOE_ERR_UNSUPPORTED for NVFP4; H <= 8192).  Workspace:
+ * beam_moe_block_workspace_size.  step >= 1.  Asynchronous; deterministic.
+ */
+size_t beam_moe_block_workspace_size(int64_t T, const beam_moe_cfg *cfg);
+int beam_moe_block_forward(const void *stream_in, int step, const float *norm_pre,
+                           const float *norm_post, float eps, const float *router_w,
+                           const void *w_gate, const void *w_up, const void *w_down,
+                           int64_t T, const beam_moe_cfg *cfg, void *stream_out,
+                           void *stream);
+
+/*
  * Synchronise `stream`, read the device status word of cfg->workspace and
  * clear it.  Returns BEAM_MOE_OK, BEAM_MOE_ERR_TIMEOUT or BEAM_MOE_ERR_DEVICE
  * (or BEAM_MOE_ERR_CUDA if the synchronisation itself failed).
@@ -269,10 +298,10 @@ int64_t beam_moe_launch_count(void);
  * cudaEventRecord(start[i]) and cudaEventRecord(stop[i]) on its stream, i
  * being the kernel's stage: 0 router scores, 1 selection, 2 histogram,
  * 3 scan, 4 permute, 5 gate/up GEMM, 6 down GEMM, 7 combine, 8 NVFP4
- * quantisation of h (NVFP4 layers only).  Events are cudaEvent_t handles
- * passed as void*, owned by the caller and alive while set; n = 0 turns the
- * hook off.  Returns BEAM_MOE_ERR_INVALID_ARG for n < 0, n > 9 or NULL
- * arrays.
+ * quantisation of h (NVFP4 layers only), 9 pre-norm (beam_moe_block_forward
+ * only).  Events are cudaEvent_t handles passed as void*, owned by the caller
+ * and alive while set; n = 0 turns the hook off.  Returns
+ * BEAM_MOE_ERR_INVALID_ARG for n < 0, n > 10 or NULL arrays.
  */
 int beam_moe_set_kernel_events(void *const *start, void *const *stop, int n);
 

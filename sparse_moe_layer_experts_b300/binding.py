@@ -96,6 +96,11 @@ def lib():
         L.beam_moe_dense_workspace_size.restype = sz
         L.beam_moe_dense_forward.argtypes = [vp, vp, vp, vp, i64, cfgp, vp, vp]
         L.beam_moe_dense_forward.restype = ctypes.c_int
+        L.beam_moe_block_workspace_size.argtypes = [i64, cfgp]
+        L.beam_moe_block_workspace_size.restype = sz
+        L.beam_moe_block_forward.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_float, vp, vp, vp,
+                                             vp, i64, cfgp, vp, vp]
+        L.beam_moe_block_forward.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -141,6 +146,16 @@ def beam_moe_dense_forward(x, w_gate, w_up, w_down, T, cfg, out, stream) -> int:
     return lib().beam_moe_dense_forward(x, w_gate, w_up, w_down, T, ctypes.byref(cfg), out, stream)
 
 
+def beam_moe_block_workspace_size(T: int, cfg: beam_moe_cfg) -> int:
+    return int(lib().beam_moe_block_workspace_size(T, ctypes.byref(cfg)))
+
+
+def beam_moe_block_forward(stream_in, step, norm_pre, norm_post, eps, router_w, w_gate, w_up,
+                           w_down, T, cfg, stream_out, stream) -> int:
+    return lib().beam_moe_block_forward(stream_in, step, norm_pre, norm_post, eps, router_w, w_gate,
+                                        w_up, w_down, T, ctypes.byref(cfg), stream_out, stream)
+
+
 def beam_moe_quantize_nvfp4(w, n_mat, rows, cols, packed, block_sf, global_sf, stream) -> int:
     return lib().beam_moe_quantize_nvfp4(w, n_mat, rows, cols, packed, block_sf, global_sf,
                                          stream)
@@ -166,7 +181,7 @@ def beam_moe_set_kernel_events(starts, stops) -> int:
 
 
 KERNEL_STAGES = ("router_scores", "select", "hist", "scan", "permute", "gateup_gemm",
-                 "down_gemm", "combine", "quantize_h")
+                 "down_gemm", "combine", "quantize_h", "prenorm")
 
 
 def beam_moe_device_sms() -> int:

@@ -9,6 +9,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <mutex>
 
 namespace beam {
@@ -244,8 +245,18 @@ int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cf
     return BEAM_MOE_OK;
 }
 
+// Fused-block epilogue: the combine also applies the post-norm and the
+// residual update s_out = bf16(a * s_in + b * rmsnorm(o) * gamma).
+struct BlockTail {
+    const uint16_t *s_in;
+    const float *gamma;
+    float eps, a, b;
+    uint16_t *s_out;
+};
+
 int run_forward(const void *x, const float *router_w, const void *w_gate, const void *w_up,
-                const void *w_down, int64_t T, const beam_moe_cfg &c, void *out, cudaStream_t s)
+                const void *w_down, int64_t T, const beam_moe_cfg &c, void *out, cudaStream_t s,
+                const BlockTail *tail = nullptr)
 {
     const Layout L = make_layout(T, c);
     void *ws = c.workspace;
@@ -332,8 +343,14 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
         BEAM_CUDA(launch_down(v, m_wd, m_h, a, sms, s));
     }
 
-    BEAM_CUDA(launch_combine(at<uint16_t>(ws, L.y), at<float>(ws, L.wts), at<int32_t>(ws, L.row_of),
-                             (int)T, K, H, static_cast<uint16_t *>(out), s));
+    if (tail)
+        BEAM_CUDA(launch_combine_block(at<uint16_t>(ws, L.y), at<float>(ws, L.wts),
+                                       at<int32_t>(ws, L.row_of), (int)T, K, H, tail->s_in,
+                                       tail->gamma, tail->eps, tail->a, tail->b, tail->s_out, s));
+    else
+        BEAM_CUDA(launch_combine(at<uint16_t>(ws, L.y), at<float>(ws, L.wts),
+                                 at<int32_t>(ws, L.row_of), (int)T, K, H,
+                                 static_cast<uint16_t *>(out), s));
     return BEAM_MOE_OK;
 }
 
@@ -636,6 +653,55 @@ int beam_moe_dense_forward(const void *x, const void *w_gate, const void *w_up, 
     if ((rc = check_ws(T, cfg, make_dense_layout(T, *cfg).total)) != BEAM_MOE_OK)
         return rc;
     return run_dense(x, w_gate, w_up, w_down, T, *cfg, out, static_cast<cudaStream_t>(stream));
+}
+
+size_t beam_moe_block_workspace_size(int64_t T, const beam_moe_cfg *cfg)
+{
+    if (check_cfg(cfg) != BEAM_MOE_OK || T < 0)
+        return 0;
+    return make_layout(T, *cfg).total + align_up((size_t)2 * T * cfg->hidden);
+}
+
+int beam_moe_block_forward(const void *stream_in, int step, const float *norm_pre,
+                           const float *norm_post, float eps, const float *router_w,
+                           const void *w_gate, const void *w_up, const void *w_down, int64_t T,
+                           const beam_moe_cfg *cfg, void *stream_out, void *stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc != BEAM_MOE_OK)
+        return rc;
+    if (cfg->wtype != BEAM_MOE_W_BF16)
+        return BEAM_MOE_ERR_UNSUPPORTED;
+    if (cfg->hidden > 8192)
+        return BEAM_MOE_ERR_UNSUPPORTED;
+    if ((rc = check_T(T, cfg)) != BEAM_MOE_OK)
+        return rc;
+    if (step < 1 || !(eps >= 0.0f) || eps > 1.0f)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_MOE_OK;
+    if (!stream_in || !norm_pre || !norm_post || !router_w || !w_gate || !w_up || !w_down ||
+        !stream_out)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (!aligned16(stream_in) || !aligned16(norm_pre) || !aligned16(norm_post) ||
+        !aligned16(router_w) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+        !aligned16(stream_out))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    const size_t base = make_layout(T, *cfg).total;
+    if ((rc = check_ws(T, cfg, base + align_up((size_t)2 * T * cfg->hidden))) != BEAM_MOE_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint16_t *x = at<uint16_t>(cfg->workspace, base);
+    BEAM_CUDA(launch_rmsnorm_bf16(static_cast<const uint16_t *>(stream_in), norm_pre, eps, (int)T,
+                                  cfg->hidden, x, s));
+    BlockTail tail;
+    tail.s_in = static_cast<const uint16_t *>(stream_in);
+    tail.gamma = norm_post;
+    tail.eps = eps;
+    tail.a = (float)std::sqrt((double)(step - 1) / (double)step);
+    tail.b = (float)(1.0 / std::sqrt((double)step));
+    tail.s_out = static_cast<uint16_t *>(stream_out);
+    return run_forward(x, router_w, w_gate, w_up, w_down, T, *cfg, nullptr, s, &tail);
 }
 
 }  // extern "C"

@@ -315,6 +315,163 @@ combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ w,
 }
 
 
+// ---- fused MoE block ("Reflection Beam 1.0", section "Residual stream":
+// sublayers are normalised before and after, in FP32; step k keeps the
+// stream with sqrt((k-1)/k) and adds the sublayer output with 1/sqrt(k)).
+// RMSNorm with a per-channel gain: the sum of squares is accumulated in FP64
+// and rounded to FP32 once as a mean, r = 1/sqrt(mean + eps) in FP32.  Per
+// thread the squares are summed as float-float pairs (FP64 arithmetic is
+// slow on this part): a bf16 value's square is exact in FP32, an FP32
+// value's square is p + e with e = fma(v, v, -p), and each addition keeps
+// its rounding error (two-sum); hi + lo is exact in FP64, where the CTA's
+// partial sums are added.
+
+// hi + lo += p + e, with the rounding error of hi + p kept in lo
+__device__ __forceinline__ void ff_acc(float &hi, float &lo, float p, float e)
+{
+    const float s = __fadd_rn(hi, p);
+    const float bp = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(err, e));
+}
+
+// FP64 sum over the 256 threads of a CTA; every thread gets the total.
+__device__ double block_sum_f64(double v, double *red)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0)
+        red[w] = v;
+    __syncthreads();
+    double t = 0.0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        t += red[i];
+    __syncthreads();
+    return t;
+}
+
+__device__ __forceinline__ float rms_inv_f32(double ss, int H, float eps)
+{
+    const float mean = __double2float_rn(ss / (double)H);
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+}
+
+// CTA per token: x = bf16((s * r) * gamma), the MoE layer's input.
+__global__ void __launch_bounds__(256)
+rmsnorm_bf16_kernel(const uint16_t *__restrict__ s, const float *__restrict__ gamma, float eps,
+                    int H, uint16_t *__restrict__ x)
+{
+    __shared__ double red[8];
+    const int t = blockIdx.x;
+    const uint4 *row = reinterpret_cast<const uint4 *>(s + (size_t)t * H);
+    const int nvec = H / 8;
+    float hi = 0.0f, lo = 0.0f;
+    for (int i = threadIdx.x; i < nvec; i += 256) {
+        const uint4 q = row[i];
+        const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = bf16_bits_to_f32(v[j] & 0xFFFFu), b = bf16_bits_to_f32(v[j] >> 16);
+            ff_acc(hi, lo, __fmul_rn(a, a), 0.0f);  // exact squares of bf16 values
+            ff_acc(hi, lo, __fmul_rn(b, b), 0.0f);
+        }
+    }
+    const float r = rms_inv_f32(block_sum_f64((double)hi + (double)lo, red), H, eps);
+    for (int i = threadIdx.x; i < nvec; i += 256) {
+        const uint4 q = row[i];
+        const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+        const float4 g0 = reinterpret_cast<const float4 *>(gamma)[2 * i];
+        const float4 g1 = reinterpret_cast<const float4 *>(gamma)[2 * i + 1];
+        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __fmul_rn(__fmul_rn(bf16_bits_to_f32(v[j] & 0xFFFFu), r), g[2 * j]);
+            const float hi = __fmul_rn(__fmul_rn(bf16_bits_to_f32(v[j] >> 16), r), g[2 * j + 1]);
+            o[j] = pack_bf16x2(lo, hi);
+        }
+        reinterpret_cast<uint4 *>(x + (size_t)t * H)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// CTA per token: o = sum_k w_k y_k (FP32, slot order, as combine_kernel),
+// kept in registers (H <= 256 * 8 * kBlockMaxVec); z = (o * r) * gamma;
+// s_out = bf16(a * s_in + b * z).  Each element is read and written by the
+// same thread, so s_out may be s_in.
+constexpr int kBlockMaxVec = 4;
+
+__global__ void __launch_bounds__(256)
+combine_block_kernel(const uint16_t *__restrict__ y, const float *__restrict__ w,
+                     const int32_t *__restrict__ row_of, int K, int H, const uint16_t *s_in,
+                     const float *__restrict__ gamma, float eps, float a, float b, uint16_t *s_out)
+{
+    __shared__ float ws[32];
+    __shared__ int rs[32];
+    __shared__ double red[8];
+    const int t = blockIdx.x;
+    if (threadIdx.x < K) {
+        ws[threadIdx.x] = w[(size_t)t * K + threadIdx.x];
+        rs[threadIdx.x] = row_of[(size_t)t * K + threadIdx.x];
+    }
+    __syncthreads();
+    const int nvec = H / 8;
+    float o[kBlockMaxVec][8];
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kBlockMaxVec; ++c) {
+        const int i = threadIdx.x + c * 256;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[c][j] = 0.0f;
+        if (i < nvec) {
+            for (int k = 0; k < K; ++k) {
+                const uint4 q = reinterpret_cast<const uint4 *>(y + (size_t)rs[k] * H)[i];
+                const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+                const float wk = ws[k];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    o[c][2 * j] = __fmaf_rn(wk, bf16_bits_to_f32(v[j] & 0xFFFFu), o[c][2 * j]);
+                    o[c][2 * j + 1] = __fmaf_rn(wk, bf16_bits_to_f32(v[j] >> 16), o[c][2 * j + 1]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float p = __fmul_rn(o[c][j], o[c][j]);
+                ff_acc(hi, lo, p, __fmaf_rn(o[c][j], o[c][j], -p));
+            }
+        }
+    }
+    const float r = rms_inv_f32(block_sum_f64((double)hi + (double)lo, red), H, eps);
+#pragma unroll
+    for (int c = 0; c < kBlockMaxVec; ++c) {
+        const int i = threadIdx.x + c * 256;
+        if (i < nvec) {
+            const uint4 q = reinterpret_cast<const uint4 *>(s_in + (size_t)t * H)[i];
+            const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+            const float4 g0 = reinterpret_cast<const float4 *>(gamma)[2 * i];
+            const float4 g1 = reinterpret_cast<const float4 *>(gamma)[2 * i + 1];
+            const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            uint32_t res[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float z0 = __fmul_rn(__fmul_rn(o[c][2 * j], r), g[2 * j]);
+                const float z1 = __fmul_rn(__fmul_rn(o[c][2 * j + 1], r), g[2 * j + 1]);
+                const float s0 = __fadd_rn(__fmul_rn(a, bf16_bits_to_f32(v[j] & 0xFFFFu)),
+                                           __fmul_rn(b, z0));
+                const float s1 = __fadd_rn(__fmul_rn(a, bf16_bits_to_f32(v[j] >> 16)),
+                                           __fmul_rn(b, z1));
+                res[j] = pack_bf16x2(s0, s1);
+            }
+            reinterpret_cast<uint4 *>(s_out + (size_t)t * H)[i] =
+                make_uint4(res[0], res[1], res[2], res[3]);
+        }
+    }
+}
+
 // Dense layers: the whole batch is one segment, offsets {0, T}, cut into
 // ceil(T / chunk_rows) token chunks; also resets the call's status word.
 __global__ void dense_setup_kernel(int T, int chunk_rows, int32_t *__restrict__ offsets,
@@ -418,6 +575,27 @@ cudaError_t launch_dense_setup(int T, int chunk_rows, int32_t *offsets, int32_t 
     stage_begin(kStScan, s);
     dense_setup_kernel<<<1, 32, 0, s>>>(T, chunk_rows, offsets, chunk_start, status);
     stage_end(kStScan, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_bf16(const uint16_t *s_in, const float *gamma, float eps, int T, int H,
+                               uint16_t *x, cudaStream_t st)
+{
+    stage_begin(kStNorm, st);
+    rmsnorm_bf16_kernel<<<T, 256, 0, st>>>(s_in, gamma, eps, H, x);
+    stage_end(kStNorm, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_block(const uint16_t *y, const float *w, const int32_t *row_of, int T,
+                                 int K, int H, const uint16_t *s_in, const float *gamma, float eps,
+                                 float a, float b, uint16_t *s_out, cudaStream_t st)
+{
+    if (H > 256 * 8 * kBlockMaxVec)
+        return cudaErrorInvalidValue;
+    stage_begin(kStCombine, st);
+    combine_block_kernel<<<T, 256, 0, st>>>(y, w, row_of, K, H, s_in, gamma, eps, a, b, s_out);
+    stage_end(kStCombine, st);
     return cudaGetLastError();
 }
 

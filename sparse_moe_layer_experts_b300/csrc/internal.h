@@ -19,6 +19,7 @@ enum Stage {
     kStDown,
     kStCombine,
     kStQuantH,  // NVFP4 layers only: quantise h before the down GEMM
+    kStNorm,    // fused block only: the pre-norm of the residual stream
     kNumStages
 };
 // Bracket one kernel launch: records the calling thread's timing events for
@@ -69,6 +70,15 @@ cudaError_t launch_quantize_rows(const float *in, int64_t rows, int cols, const 
                                  bool rep_layout, uint8_t *codes, uint8_t *sf, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t *y, const float *w, const int32_t *row_of, int T, int K,
                            int H, uint16_t *out, cudaStream_t s);
+// fused MoE block: x = bf16(rmsnorm(s_in) * gamma) (FP64 sum of squares,
+// FP32 r = 1/sqrt(mean + eps)), and the combine with post-norm and the
+// residual s_out = bf16(a * s_in + b * rmsnorm(o) * gamma) (H <= 8192;
+// s_out may be s_in)
+cudaError_t launch_rmsnorm_bf16(const uint16_t *s_in, const float *gamma, float eps, int T, int H,
+                               uint16_t *x, cudaStream_t st);
+cudaError_t launch_combine_block(const uint16_t *y, const float *w, const int32_t *row_of, int T,
+                                 int K, int H, const uint16_t *s_in, const float *gamma, float eps,
+                                 float a, float b, uint16_t *s_out, cudaStream_t st);
 // dense layers: offsets {0, T}, chunk_start {0, ceil(T/chunk_rows)}, status 0
 cudaError_t launch_dense_setup(int T, int chunk_rows, int32_t *offsets, int32_t *chunk_start,
                                int *status, cudaStream_t s);

@@ -123,6 +123,27 @@ class BeamMoE:
                                    out.data_ptr(), _stream_handle(stream)), "beam_moe_forward")
         return out
 
+    def block_forward(self, s, step, norm_pre, norm_post, eps=1e-6, out=None, stream=None):
+        """The MoE sublayer at residual step `step` with its pre-/post-norms:
+        returns bf16(sqrt((step-1)/step) * s + rmsnorm(layer(rmsnorm(s) *
+        norm_pre)) * norm_post / sqrt(step)).  out may be s (in place)."""
+        self._check_x(s)
+        for g in (norm_pre, norm_post):
+            if (g.dtype != torch.float32 or tuple(g.shape) != (self.H,) or not g.is_cuda
+                    or not g.is_contiguous()):
+                raise ValueError("norm gains must be contiguous CUDA fp32 [H]")
+        T = s.shape[0]
+        if out is None:
+            out = torch.empty_like(s)
+        need = B.beam_moe_block_workspace_size(T, self.cfg)
+        self.workspace(T, max(0, need - B.beam_moe_workspace_size(T, self.cfg)))
+        B.check(B.beam_moe_block_forward(s.data_ptr(), int(step), norm_pre.data_ptr(),
+                                         norm_post.data_ptr(), float(eps), self.router_w.data_ptr(),
+                                         self.w_gate.data_ptr(), self.w_up.data_ptr(),
+                                         self.w_down.data_ptr(), T, self.cfg, out.data_ptr(),
+                                         _stream_handle(stream)), "beam_moe_block_forward")
+        return out
+
     def forward_host(self, x_host, out_host, stream=None):
         """x_host/out_host: CPU bf16 [T,H] tensors (pinned for speed)."""
         if x_host.is_cuda or out_host.is_cuda:

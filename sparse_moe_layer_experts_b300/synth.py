@@ -27,6 +27,9 @@ The pages give no intermediate size for the dense layers; the "dense"
 workload takes I = 8 * 2560 = 20480, the FFN width one MoE layer's eight
 active experts add up to.
 
+The fused block's RMS-norm gains are 1 + 0.1 N(0,1) in FP32 (norm_pre
+sub-seed 20, norm_post sub-seed 21).
+
 Tensors are drawn on ``device``.  CPU and CUDA generators produce different
 streams, so a test draws each tensor once and hands the same tensor to both
 sides.
@@ -136,6 +139,13 @@ def make_dense_inputs(T: int, H: int, I: int, seed: int = 0, device="cpu"):
         w_up=_normal_bf16((I, H), 0.02, _gen(dev, seed, 12), dev, chunk),
         w_down=_normal_bf16((H, I), 0.02, _gen(dev, seed, 13), dev, chunk),
     )
+
+
+def make_block_gains(H: int, seed: int = 0, device="cpu"):
+    """(norm_pre, norm_post) gains [H] fp32 per the module recipe."""
+    dev = torch.device(device)
+    return tuple(torch.randn(H, generator=_gen(dev, seed, sub), device=dev,
+                             dtype=torch.float32).mul_(0.1).add_(1.0) for sub in (20, 21))
 
 
 def to_bits(t: torch.Tensor):

@@ -131,3 +131,20 @@ def test_dense_entry_point_checks(L):
     assert B.beam_moe_dense_workspace_size(64, c) == 0
     assert B.beam_moe_launch_count() == before
 
+
+def test_block_entry_point_checks(L):
+    c = B.make_cfg(256, 128, 32, 8, 4, 8)
+    assert B.beam_moe_block_workspace_size(64, c) > B.beam_moe_workspace_size(64, c)
+    before = B.beam_moe_launch_count()
+    assert B.beam_moe_block_forward(16, 9, 16, 16, 1e-6, 16, 16, 16, 16, 0, c, 16, None) == B.BEAM_MOE_OK
+    assert B.beam_moe_block_forward(16, 0, 16, 16, 1e-6, 16, 16, 16, 16, 4, c, 16, None) == \
+        B.BEAM_MOE_ERR_INVALID_ARG
+    assert B.beam_moe_block_forward(16, 9, 16, 16, -1.0, 16, 16, 16, 16, 4, c, 16, None) == \
+        B.BEAM_MOE_ERR_INVALID_ARG
+    assert B.beam_moe_block_forward(16, 9, 16, 16, 1e-6, 16, 16, 16, 16, 4, c, 16, None) == \
+        B.BEAM_MOE_ERR_WORKSPACE
+    c.wtype = B.BEAM_MOE_W_NVFP4
+    assert B.beam_moe_block_forward(16, 9, 16, 16, 1e-6, 16, 16, 16, 16, 4, c, 16, None) == \
+        B.BEAM_MOE_ERR_UNSUPPORTED
+    assert B.beam_moe_launch_count() == before
+

@@ -1,0 +1,70 @@
+"""Fused MoE block (pre-norm -> layer -> post-norm -> constant-scale
+residual) on the GPU against the oracle, every token at small shapes and
+sampled tokens at the prefill size; in-place equals out-of-place."""
+import numpy as np
+import pytest
+import torch
+
+from sparse_moe_layer_experts_b300 import synth
+from sparse_moe_layer_experts_b300.layer import BeamMoE
+
+from tests._gpu_util import REL_L2_TOL, host_inputs, out_bits, rel_l2_per_token, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer(sh, d):
+    return BeamMoE(d["router_w"], d["w_gate"], d["w_up"], d["w_down"], n_groups=sh.G,
+                   topk_groups=sh.topk_groups, top_k=sh.top_k, routed_scale=sh.scale)
+
+
+def _oracle(oracle_mod, sh, h, gp, gq, step, eps, tokens=None):
+    return oracle_mod.block_forward(h["x"], step, gp.cpu().numpy(), gq.cpu().numpy(), eps,
+                                    h["router_w"], h["w_gate"], h["w_up"], h["w_down"], sh.G,
+                                    sh.topk_groups, sh.top_k, sh.scale, tokens=tokens)
+
+
+@pytest.mark.parametrize("T,step", [(64, 9), (200, 9), (200, 1), (33, 1000)])
+def test_block_all_tokens(oracle_mod, T, step):
+    sh = synth.shape("tiny", T=T)
+    d = synth.make_inputs(sh, seed=7, device="cuda")
+    gp, gq = synth.make_block_gains(sh.H, seed=7, device="cuda")
+    layer = _layer(sh, d)
+    out = layer.block_forward(d["x"], step, gp, gq, 1e-6)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    ref = _oracle(oracle_mod, sh, host_inputs(d), gp, gq, step, 1e-6)
+    rel = rel_l2_per_token(out_bits(out), ref)
+    assert rel.max() <= REL_L2_TOL, (rel.max(), int(rel.argmax()))
+
+
+def test_block_in_place_and_deterministic():
+    sh = synth.shape("tiny", T=150)
+    d = synth.make_inputs(sh, seed=8, device="cuda")
+    gp, gq = synth.make_block_gains(sh.H, seed=8, device="cuda")
+    layer = _layer(sh, d)
+    a = layer.block_forward(d["x"], 5, gp, gq, 1e-6).clone()
+    b = layer.block_forward(d["x"], 5, gp, gq, 1e-6).clone()
+    s = d["x"].clone()
+    layer.block_forward(s, 5, gp, gq, 1e-6, out=s)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), s.view(torch.int16))
+
+
+@pytest.mark.slow
+def test_block_prefill_sampled(oracle_mod):
+    sh = synth.shape("prefill")
+    d = synth.make_inputs(sh, seed=0, device="cuda")
+    gp, gq = synth.make_block_gains(sh.H, seed=0, device="cuda")
+    layer = _layer(sh, d)
+    out = layer.block_forward(d["x"], 9, gp, gq, 1e-6)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    # the oracle routes on its own normalised x; sample tokens across the batch
+    rng = np.random.default_rng(1)
+    toks = sorted({0, sh.T - 1} | set(int(v) for v in rng.choice(sh.T, 10, replace=False)))
+    h = host_inputs(d)
+    ref = _oracle(oracle_mod, sh, h, gp, gq, 9, 1e-6, tokens=toks)
+    rel = rel_l2_per_token(out_bits(out)[toks], ref)
+    assert rel.max() <= REL_L2_TOL, (rel.max(), toks[int(rel.argmax())])
