@@ -720,3 +720,162 @@ int oracle_forward_nvfp4(const uint16_t *x, const float *wr, const uint8_t *gc, 
     }
     return bad ? -1 : 0;
 }
+
+/* ------------------------------------------------------------------ MXFP8 */
+
+/*
+ * MXFP8 expert weights and activations: E4M3 values with one power-of-two
+ * (UE8M0) scale per 32 consecutive elements of a row.  The pages only say an
+ * FP8 checkpoint exists ([P1-MoE] checkpoints paragraph; [P5] checkpoint
+ * list); the recipe is a reading: the OCP microscaling rule, shared exponent
+ * E = floor(log2(amax32)) - 8 (8 = the largest E4M3 exponent), clamped to
+ * [-127, 127], E = -127 for an all-zero block; q = e4m3_rn_satfinite(v / 2^E);
+ * the scale byte is E + 127.  Dequantised value: e4m3(q) * 2^E.
+ */
+int oracle_mx_shared_exp(float amax)
+{
+    if (!(amax > 0.0f))
+        return -127;
+    int ex;
+    frexpf(amax, &ex); /* amax = m * 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1 */
+    int e = ex - 1 - 8;
+    if (e < -127)
+        e = -127;
+    if (e > 127)
+        e = 127;
+    return e;
+}
+
+/* signed E4M3 code: the sign bit and the nearest magnitude (even-mantissa
+ * ties, saturating at 448) */
+static int e4m3_code_signed(float v)
+{
+    return (signbit(v) ? 0x80 : 0) | oracle_e4m3_code(fabsf(v));
+}
+
+static void mx_quantize_row(const float *v, int64_t n, uint8_t *codes, uint8_t *sf)
+{
+    for (int64_t b = 0; b < n / 32; ++b) {
+        const float *blk = v + b * 32;
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i)
+            if (fabsf(blk[i]) > amax)
+                amax = fabsf(blk[i]);
+        const int e = oracle_mx_shared_exp(amax);
+        sf[b] = (uint8_t)(e + 127);
+        for (int i = 0; i < 32; ++i)
+            codes[b * 32 + i] = (uint8_t)e4m3_code_signed(ldexpf(blk[i], -e));
+    }
+}
+
+static double mx_value(uint8_t code, uint8_t sfb)
+{
+    return ldexp((double)oracle_e4m3_value(code), (int)sfb - 127);
+}
+
+/* w [n_mat, rows, cols] bf16 -> codes [n_mat, rows, cols] E4M3 bytes, sf
+ * [n_mat, rows, cols/32] UE8M0 bytes (plain row-major layout) */
+int oracle_quantize_mxfp8(const uint16_t *w, int64_t n_mat, int64_t rows, int64_t cols,
+                          uint8_t *codes, uint8_t *sf)
+{
+    if (cols % 32 != 0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n_mat * rows; ++r) {
+        float *row = (float *)malloc(sizeof(float) * (size_t)cols);
+        for (int64_t c = 0; c < cols; ++c)
+            row[c] = bf16_bits_to_float(w[r * cols + c]);
+        mx_quantize_row(row, cols, codes + r * cols, sf + r * (cols / 32));
+        free(row);
+    }
+    return 0;
+}
+
+/* in place: v[i] <- its MXFP8 value (the activations' quantisation) */
+void oracle_fake_quant_mxfp8_rows(float *v, int64_t n_rows, int64_t n)
+{
+    uint8_t *codes = (uint8_t *)malloc((size_t)n);
+    uint8_t *sf = (uint8_t *)malloc((size_t)(n / 32));
+    for (int64_t r = 0; r < n_rows; ++r) {
+        float *row = v + r * n;
+        mx_quantize_row(row, n, codes, sf);
+        for (int64_t i = 0; i < n; ++i)
+            row[i] = (float)mx_value(codes[i], sf[i / 32]);
+    }
+    free(codes);
+    free(sf);
+}
+
+/*
+ * The layer forward with MXFP8 experts: routing as oracle_forward (FP32 on
+ * the bf16 x); x and h quantised to MXFP8 as above; FP64 dot products of
+ * the dequantised values; h = silu(g)*u in FP32 from g, u rounded to FP32.
+ */
+int oracle_forward_mxfp8(const uint16_t *x, const float *wr, const uint8_t *gc, const uint8_t *gsf,
+                         const uint8_t *uc, const uint8_t *usf, const uint8_t *dc,
+                         const uint8_t *dsf, int64_t T, int H, int I, int E, int G,
+                         int topk_groups, int top_k, float scale, const int64_t *tokens,
+                         int64_t n_tokens, uint16_t *out, int32_t *ids_out, float *w_out)
+{
+    if (E % G != 0 || top_k > topk_groups * (E / G) || H % 32 || I % 32)
+        return -1;
+    const int64_t n = tokens ? n_tokens : T;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t t = tokens ? tokens[r] : r;
+        if (t < 0 || t >= T) {
+            bad = 1;
+            continue;
+        }
+        const uint16_t *xrow = x + t * H;
+        float *scores = (float *)malloc(sizeof(float) * (size_t)E);
+        int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)top_k);
+        float *w = (float *)malloc(sizeof(float) * (size_t)top_k);
+        float *xq = (float *)malloc(sizeof(float) * (size_t)H);
+        float *hq = (float *)malloc(sizeof(float) * (size_t)I);
+        double *acc = (double *)calloc((size_t)H, sizeof(double));
+
+        oracle_router_scores(xrow, wr, 1, H, E, NULL, scores);
+        if (oracle_select(scores, 1, E, G, topk_groups, top_k, scale, ids, w) != 0)
+            bad = 1;
+        for (int h = 0; h < H; ++h)
+            xq[h] = bf16_bits_to_float(xrow[h]);
+        oracle_fake_quant_mxfp8_rows(xq, 1, H);
+        for (int k = 0; k < top_k && !bad; ++k) {
+            const int64_t e = ids[k];
+            for (int i = 0; i < I; ++i) {
+                double gd = 0.0, ud = 0.0;
+                const int64_t row = e * I + i;
+                for (int h = 0; h < H; ++h) {
+                    gd += (double)xq[h] * mx_value(gc[row * H + h], gsf[row * (H / 32) + h / 32]);
+                    ud += (double)xq[h] * mx_value(uc[row * H + h], usf[row * (H / 32) + h / 32]);
+                }
+                const float g = (float)gd, u = (float)ud;
+                hq[i] = (g * sigmoid_f32(g)) * u;
+            }
+            oracle_fake_quant_mxfp8_rows(hq, 1, I);
+            for (int j = 0; j < H; ++j) {
+                double yd = 0.0;
+                const int64_t row = e * H + j;
+                for (int i = 0; i < I; ++i)
+                    yd += (double)hq[i] * mx_value(dc[row * I + i], dsf[row * (I / 32) + i / 32]);
+                acc[j] += (double)w[k] * yd;
+            }
+        }
+        for (int j = 0; j < H; ++j)
+            out[r * H + j] = float_to_bf16_bits_rne((float)acc[j]);
+        if (ids_out)
+            memcpy(ids_out + r * top_k, ids, sizeof(int32_t) * (size_t)top_k);
+        if (w_out)
+            memcpy(w_out + r * top_k, w, sizeof(float) * (size_t)top_k);
+        free(scores);
+        free(ids);
+        free(w);
+        free(xq);
+        free(hq);
+        free(acc);
+    }
+    return bad ? -1 : 0;
+}
+

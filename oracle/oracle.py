@@ -65,6 +65,15 @@ def lib():
         L.oracle_block_forward.restype = i32
         L.oracle_rmsnorm_bf16.argtypes = [p, p, f32, i64, i32, p]
         L.oracle_rmsnorm_bf16.restype = None
+        L.oracle_mx_shared_exp.argtypes = [f32]
+        L.oracle_mx_shared_exp.restype = i32
+        L.oracle_quantize_mxfp8.argtypes = [p, i64, i64, i64, p, p]
+        L.oracle_quantize_mxfp8.restype = i32
+        L.oracle_fake_quant_mxfp8_rows.argtypes = [p, i64, i64]
+        L.oracle_fake_quant_mxfp8_rows.restype = None
+        L.oracle_forward_mxfp8.argtypes = [p, p, p, p, p, p, p, p, i64, i32, i32, i32, i32, i32,
+                                           i32, f32, p, i64, p, p, p]
+        L.oracle_forward_mxfp8.restype = i32
         L.oracle_e2m1_value.argtypes = [i32]
         L.oracle_e2m1_value.restype = f32
         L.oracle_e2m1_code.argtypes = [f32]
@@ -311,3 +320,66 @@ def forward_nvfp4(x_bits, router_w, q_gate, q_up, q_down, n_groups, topk_groups,
     if rc != 0:
         raise ValueError("oracle_forward_nvfp4 failed")
     return out, ids, w
+
+
+# ---------------------------------------------------------------- MXFP8
+
+def mx_shared_exp(amax: float) -> int:
+    """floor(log2(amax)) - 8 clamped to [-127, 127]; -127 for amax = 0."""
+    return int(lib().oracle_mx_shared_exp(float(amax)))
+
+
+def quantize_mxfp8(w_bits: np.ndarray):
+    """bf16 bits [n_mat, rows, cols] -> (E4M3 codes [n_mat, rows, cols] uint8,
+    UE8M0 scales [n_mat, rows, cols/32] uint8)."""
+    w_bits = _c(w_bits, np.uint16)
+    n_mat, rows, cols = w_bits.shape
+    codes = np.empty((n_mat, rows, cols), np.uint8)
+    sf = np.empty((n_mat, rows, cols // 32), np.uint8)
+    rc = lib().oracle_quantize_mxfp8(_ptr(w_bits), n_mat, rows, cols, _ptr(codes), _ptr(sf))
+    if rc != 0:
+        raise ValueError("cols must be a multiple of 32")
+    return codes, sf
+
+
+def fake_quant_mxfp8_rows(v: np.ndarray) -> np.ndarray:
+    """Rows of FP32 values -> their MXFP8 values (a copy)."""
+    v = np.array(v, np.float32, copy=True, order="C")
+    lib().oracle_fake_quant_mxfp8_rows(_ptr(v), v.shape[0], v.shape[1])
+    return v
+
+
+def dequantize_mxfp8(codes, sf) -> np.ndarray:
+    """E4M3 codes and UE8M0 scales -> float64 values."""
+    codes = np.asarray(codes, np.uint8)
+    mag_e = (codes >> 3) & 15
+    mag_m = (codes & 7).astype(np.float64)
+    mag = np.where(mag_e == 0, mag_m * 2.0 ** -9, (1.0 + mag_m / 8.0) * 2.0 ** (mag_e.astype(np.float64) - 7))
+    val = np.where(codes & 0x80, -mag, mag)
+    scale = 2.0 ** (np.repeat(np.asarray(sf, np.float64), 32, axis=-1) - 127)
+    return val * scale
+
+
+def forward_mxfp8(x_bits, router_w, q_gate, q_up, q_down, n_groups, topk_groups, top_k, scale,
+                  tokens=None):
+    """Layer output with MXFP8 experts; q_* = quantize_mxfp8(w_*) (codes, sf)."""
+    x_bits = _c(x_bits, np.uint16)
+    router_w = _c(router_w, np.float32)
+    T, H = x_bits.shape
+    E, I, _ = q_gate[0].shape
+    gc, gsf = (_c(a, np.uint8) for a in q_gate)
+    uc, usf = (_c(a, np.uint8) for a in q_up)
+    dc, dsf = (_c(a, np.uint8) for a in q_down)
+    tok = None if tokens is None else _c(np.asarray(tokens, np.int64), np.int64)
+    n = T if tok is None else tok.shape[0]
+    out = np.empty((n, H), np.uint16)
+    ids = np.empty((n, top_k), np.int32)
+    w = np.empty((n, top_k), np.float32)
+    rc = lib().oracle_forward_mxfp8(_ptr(x_bits), _ptr(router_w), _ptr(gc), _ptr(gsf), _ptr(uc),
+                                    _ptr(usf), _ptr(dc), _ptr(dsf), T, H, I, E, n_groups,
+                                    topk_groups, top_k, float(scale), _ptr(tok), n, _ptr(out),
+                                    _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise ValueError("oracle_forward_mxfp8 failed")
+    return out, ids, w
+
