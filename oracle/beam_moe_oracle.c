@@ -746,11 +746,39 @@ int oracle_mx_shared_exp(float amax)
     return e;
 }
 
-/* signed E4M3 code: the sign bit and the nearest magnitude (even-mantissa
- * ties, saturating at 448) */
+/* the finite non-negative E4M3 values, codes 0..126, ascending */
+static double kE4M3Pos[127];
+
+static void e4m3_table_init(void)
+{
+    for (int c = 0; c < 127; ++c)
+        kE4M3Pos[c] = (double)oracle_e4m3_value(c);
+}
+
+/* signed E4M3 code: the sign bit and the nearest magnitude, as
+ * oracle_e4m3_code (ties to the even code, saturating at 448) but found by
+ * bisection of the ascending value table; call e4m3_table_init() first */
 static int e4m3_code_signed(float v)
 {
-    return (signbit(v) ? 0x80 : 0) | oracle_e4m3_code(fabsf(v));
+    const double a = fabs((double)v);
+    int c;
+    if (a >= kE4M3Pos[126]) {
+        c = 126;
+    } else {
+        int lo = 0, hi = 126; /* largest c with value(c) <= a */
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) / 2;
+            if (kE4M3Pos[mid] <= a)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        c = lo;
+        const double d0 = a - kE4M3Pos[c], d1 = kE4M3Pos[c + 1] - a;
+        if (d1 < d0 || (d1 == d0 && ((c + 1) & 1) == 0))
+            c = c + 1;
+    }
+    return (signbit(v) ? 0x80 : 0) | c;
 }
 
 static void mx_quantize_row(const float *v, int64_t n, uint8_t *codes, uint8_t *sf)
@@ -780,6 +808,7 @@ int oracle_quantize_mxfp8(const uint16_t *w, int64_t n_mat, int64_t rows, int64_
 {
     if (cols % 32 != 0)
         return -1;
+    e4m3_table_init();
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n_mat * rows; ++r) {
         float *row = (float *)malloc(sizeof(float) * (size_t)cols);
@@ -791,9 +820,22 @@ int oracle_quantize_mxfp8(const uint16_t *w, int64_t n_mat, int64_t rows, int64_
     return 0;
 }
 
+/* in place: one row's values <- their MXFP8 values (table already built) */
+static void mx_fake_quant_row(float *row, int64_t n)
+{
+    uint8_t *codes = (uint8_t *)malloc((size_t)n);
+    uint8_t *sf = (uint8_t *)malloc((size_t)(n / 32));
+    mx_quantize_row(row, n, codes, sf);
+    for (int64_t i = 0; i < n; ++i)
+        row[i] = (float)mx_value(codes[i], sf[i / 32]);
+    free(codes);
+    free(sf);
+}
+
 /* in place: v[i] <- its MXFP8 value (the activations' quantisation) */
 void oracle_fake_quant_mxfp8_rows(float *v, int64_t n_rows, int64_t n)
 {
+    e4m3_table_init();
     uint8_t *codes = (uint8_t *)malloc((size_t)n);
     uint8_t *sf = (uint8_t *)malloc((size_t)(n / 32));
     for (int64_t r = 0; r < n_rows; ++r) {
@@ -819,6 +861,7 @@ int oracle_forward_mxfp8(const uint16_t *x, const float *wr, const uint8_t *gc, 
 {
     if (E % G != 0 || top_k > topk_groups * (E / G) || H % 32 || I % 32)
         return -1;
+    e4m3_table_init();
     const int64_t n = tokens ? n_tokens : T;
     int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
@@ -841,7 +884,7 @@ int oracle_forward_mxfp8(const uint16_t *x, const float *wr, const uint8_t *gc, 
             bad = 1;
         for (int h = 0; h < H; ++h)
             xq[h] = bf16_bits_to_float(xrow[h]);
-        oracle_fake_quant_mxfp8_rows(xq, 1, H);
+        mx_fake_quant_row(xq, H);
         for (int k = 0; k < top_k && !bad; ++k) {
             const int64_t e = ids[k];
             for (int i = 0; i < I; ++i) {
@@ -854,7 +897,7 @@ int oracle_forward_mxfp8(const uint16_t *x, const float *wr, const uint8_t *gc, 
                 const float g = (float)gd, u = (float)ud;
                 hq[i] = (g * sigmoid_f32(g)) * u;
             }
-            oracle_fake_quant_mxfp8_rows(hq, 1, I);
+            mx_fake_quant_row(hq, I);
             for (int j = 0; j < H; ++j) {
                 double yd = 0.0;
                 const int64_t row = e * H + j;
