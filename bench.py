@@ -40,6 +40,8 @@ BLOCK_STEP = 9
 BLOCK_EPS = 1e-6
 # ratio of nominal dense fp4 to bf16 tensor rates
 NVFP4_OVER_BF16 = 13.5 / 2.25
+# ratio of nominal dense fp8 to bf16 tensor rates
+FP8_OVER_BF16 = 4.5 / 2.25
 
 
 def load_peaks():
@@ -58,7 +60,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="decode",
-                    choices=["tiny", "decode", "prefill", "skewed", "nvfp4", "dense"])
+                    choices=["tiny", "decode", "prefill", "skewed", "nvfp4", "mxfp8", "dense"])
     ap.add_argument("--cpu-tokens", type=int, default=16,
                     help="tokens of the batch the CPU oracle baseline computes")
     ap.add_argument("--override", default="",
@@ -218,6 +220,11 @@ KERNEL_SOURCES = {
 FP4_GEMM_SOURCES = ("grouped_gemm_fp4.cu", "gemm_common.cuh", "common.cuh", "nvfp4.cuh")
 
 
+def weight_format(config: str) -> str:
+    """The expert format a benchmark config runs: bf16, nvfp4 or mxfp8."""
+    return config if config in ("nvfp4", "mxfp8") else "bf16"
+
+
 def kernel_source_sha(kernel: str, nvfp4: bool = False) -> str:
     """Hash of the source files a kernel is built from."""
     h = hashlib.sha256()
@@ -239,21 +246,22 @@ def ncu_traffic(kernel: str, workload: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_sha") != kernel_source_sha(kernel, workload == "nvfp4"):
+    if not e or e.get("source_sha") != kernel_source_sha(kernel, workload in ("nvfp4", "mxfp8")):
         return None
     return e.get("bytes_per_launch")
 
 
-def workload_algorithmic(sh, n_active: int, nvfp4: bool = False):
+def workload_algorithmic(sh, n_active: int, fmt: str = "bf16"):
     """Algorithmic bytes / FLOPs per launch of each kernel (compulsory traffic
     of the kernel's own inputs and outputs; expert weights of active experts
     only).  NVFP4 weights and activations: 0.5 B per code + 1/16 B of block
     scale; NVFP4 h leaves gate/up in FP32 for the quantize_h pass."""
     T, H, I, E, K = sh.T, sh.H, sh.I, sh.E, sh.top_k
     R = T * K
-    wb = 0.5625 if nvfp4 else 2
-    ab = 0.5625 if nvfp4 else 2  # activation operand bytes per element
-    hb = 4 if nvfp4 else 2       # h as written by gate/up
+    # bytes per element: NVFP4 0.5 + 1/16 of scale, MXFP8 1 + 1/32
+    wb = {"bf16": 2, "nvfp4": 0.5625, "mxfp8": 1.03125}[fmt]
+    ab = wb                             # activation operand bytes per element
+    hb = 2 if fmt == "bf16" else 4      # h as written by gate/up (FP32 before quantisation)
     w_gu = int(n_active * 2 * I * H * wb)
     w_d = int(n_active * H * I * wb)
     return {
@@ -293,21 +301,39 @@ def host_sample(sh, d, toks):
     return host
 
 
-def oracle_step(sh, host, toks, nvfp4=False):
+def oracle_quantize_sample(host, fmt):
+    """The oracle's quantised experts of the sample (weights are quantised
+    ahead of the layer, on both arms, so this stays outside the timing)."""
+    from oracle import oracle
+    if fmt == "bf16":
+        return None
+    q = []
+    for k in ("w_gate", "w_up", "w_down"):
+        w = host[k]
+        blk = 32 if fmt == "mxfp8" else 16
+        codes = np.zeros(w.shape, np.uint8)
+        sf = np.zeros(w.shape[:-1] + (w.shape[-1] // blk,), np.uint8)
+        gs = np.ones(w.shape[0], np.float32)
+        for e in host["experts"]:
+            if fmt == "mxfp8":
+                c1, s1 = oracle.quantize_mxfp8(w[e:e + 1])
+            else:
+                c1, s1, g1 = oracle.quantize_nvfp4(w[e:e + 1])
+                gs[e] = g1[0]
+            codes[e], sf[e] = c1[0], s1[0]
+        q.append((codes, sf) if fmt == "mxfp8" else (codes, sf, gs))
+    return q
+
+
+def oracle_step(sh, host, toks, fmt="bf16", q=None):
+    """One timed oracle pass over the sampled tokens (q: the quantised
+    experts for the NVFP4 and MXFP8 formats)."""
     from oracle import oracle
     t0 = time.perf_counter()
-    if nvfp4:
-        # the oracle quantises the experts the sample uses, then runs the layer
-        q = []
-        for k in ("w_gate", "w_up", "w_down"):
-            w = host[k]
-            codes = np.zeros(w.shape, np.uint8)
-            sf = np.zeros(w.shape[:-1] + (w.shape[-1] // 16,), np.uint8)
-            gs = np.ones(w.shape[0], np.float32)
-            for e in host["experts"]:
-                c1, s1, g1 = oracle.quantize_nvfp4(w[e:e + 1])
-                codes[e], sf[e], gs[e] = c1[0], s1[0], g1[0]
-            q.append((codes, sf, gs))
+    if fmt == "mxfp8":
+        oracle.forward_mxfp8(host["x"], host["router_w"], *q, sh.G, sh.topk_groups, sh.top_k,
+                             sh.scale, tokens=toks)
+    elif fmt == "nvfp4":
         oracle.forward_nvfp4(host["x"], host["router_w"], *q, sh.G, sh.topk_groups, sh.top_k,
                              sh.scale, tokens=toks)
     else:
@@ -316,14 +342,14 @@ def oracle_step(sh, host, toks, nvfp4=False):
     return time.perf_counter() - t0
 
 
-def cpu_oracle_run(sh, d, n_tokens, seed=0, nvfp4=False):
+def cpu_oracle_run(sh, d, n_tokens, seed=0, fmt="bf16"):
     """Time the CPU oracle on `n_tokens` seeded tokens of the batch."""
     import numpy as np
     from oracle import oracle
     rng = np.random.default_rng(seed)
     toks = sorted(rng.choice(sh.T, size=min(n_tokens, sh.T), replace=False).tolist())
     host = host_sample(sh, d, toks)
-    dt = oracle_step(sh, host, toks, nvfp4)
+    dt = oracle_step(sh, host, toks, fmt, oracle_quantize_sample(host, fmt))
     return len(toks) / dt, min(oracle.num_threads(), len(toks)), len(toks), dt
 
 
@@ -349,8 +375,9 @@ def run_reference(args, world, rank):
     toks = sorted(np.random.default_rng(0).choice(sh.T, size=ntok, replace=False).tolist())
     host = host_sample(sh, d, toks)
     del d
-    nvfp4 = args.config == "nvfp4"
-    times = [oracle_step(sh, host, toks, nvfp4) for _ in range(args.warmup + args.steps)]
+    fmt = weight_format(args.config)
+    q = oracle_quantize_sample(host, fmt)
+    times = [oracle_step(sh, host, toks, fmt, q) for _ in range(args.warmup + args.steps)]
     total = sum(times[args.warmup:])
     value = ntok * args.steps / total
     cores = min(oracle.num_threads(), ntok)
@@ -411,7 +438,7 @@ def run_ours(args, world, rank, local):
     from sparse_moe_layer_experts_b300 import binding as B
     from sparse_moe_layer_experts_b300 import build as build_mod
     from sparse_moe_layer_experts_b300 import synth
-    from sparse_moe_layer_experts_b300.layer import BeamMoE, quantize_nvfp4
+    from sparse_moe_layer_experts_b300.layer import BeamMoE, quantize_mxfp8, quantize_nvfp4
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
@@ -419,11 +446,16 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sh = synth.shape(args.config, **parse_override(args.override))
-    nvfp4 = args.config == "nvfp4"
+    fmt = weight_format(args.config)
+    nvfp4, mx8 = fmt == "nvfp4", fmt == "mxfp8"
     d = synth.make_inputs(sh, seed=0, device=dev, weights=True)
     if rank > 0:  # each replica routes its own batch
         d["x"] = synth.make_inputs(sh, seed=rank, device=dev, weights=False)["x"]
-    if nvfp4:
+    if mx8:
+        q = [quantize_mxfp8(d[k]) for k in ("w_gate", "w_up", "w_down")]
+        layer = BeamMoE.mxfp8(d["router_w"], *q, n_groups=sh.G, topk_groups=sh.topk_groups,
+                              top_k=sh.top_k, routed_scale=sh.scale)
+    elif nvfp4:
         q = [quantize_nvfp4(d[k]) for k in ("w_gate", "w_up", "w_down")]
         layer = BeamMoE.nvfp4(d["router_w"], *q, n_groups=sh.G, topk_groups=sh.topk_groups,
                               top_k=sh.top_k, routed_scale=sh.scale)
@@ -433,7 +465,7 @@ def run_ours(args, world, rank, local):
     x = d["x"]
     out = torch.empty_like(x)
     if args.block:
-        if nvfp4:
+        if fmt != "bf16":
             raise SystemExit("--block runs the bf16 configs")
         gp, gq = synth.make_block_gains(sh.H, seed=0, device=dev)
         step_fn = lambda: layer.block_forward(x, BLOCK_STEP, gp, gq, BLOCK_EPS, out=out)
@@ -481,7 +513,7 @@ def run_ours(args, world, rank, local):
         raise SystemExit("device status word reports an error in the timed region")
     per_kernel_ms = {name: sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps))
                      / args.steps for j, name in enumerate(B.KERNEL_STAGES)
-                     if (nvfp4 or name != "quantize_h") and (args.block or name != "prenorm")}
+                     if (fmt != "bf16" or name != "quantize_h") and (args.block or name != "prenorm")}
 
     # end to end through the host-I/O entry point (pinned host buffers)
     e2e = None
@@ -511,8 +543,9 @@ def run_ours(args, world, rank, local):
     peaks, peak_src = load_peaks()
     # tensor peak of the path's MMA type: bf16, or FP4 (measured bf16 x the
     # nominal fp4/bf16 ratio)
-    t_peak = peaks["bf16_tflops"] * (NVFP4_OVER_BF16 if nvfp4 else 1.0)
-    alg = workload_algorithmic(sh, n_active, nvfp4)
+    t_peak = peaks["bf16_tflops"] * {"bf16": 1.0, "nvfp4": NVFP4_OVER_BF16,
+                                     "mxfp8": FP8_OVER_BF16}[fmt]
+    alg = workload_algorithmic(sh, n_active, fmt)
     dom = max(per_kernel_ms, key=per_kernel_ms.get)
     a = alg[dom]
     t_dom = per_kernel_ms[dom] / 1e3
@@ -532,6 +565,8 @@ def run_ours(args, world, rank, local):
         "fallback"
     if nvfp4 and roof["bound"] == "tensor":
         roof["peak_source"] += ", bf16 x 13.5/2.25 (nominal dense fp4/bf16)"
+    if mx8 and roof["bound"] == "tensor":
+        roof["peak_source"] += ", bf16 x 4.5/2.25 (nominal dense fp8/bf16)"
     roof["algorithmic_bytes_per_launch"] = a["bytes"]
     roof["algorithmic_flops_per_launch"] = a["flops"]
     lay = alg["layer"]
@@ -545,7 +580,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, n, dt = cpu_oracle_run(sh, d, args.cpu_tokens, nvfp4=nvfp4)
+        v, cores, n, dt = cpu_oracle_run(sh, d, args.cpu_tokens, fmt=fmt)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{n} seeded tokens of the {args.config} batch ({dt:.1f} s)"}
 
@@ -554,7 +589,10 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "nvfp4 weights+activations, fp4 MMA (kind::mxf4nvf4), f32 accumulate" if nvfp4 else "bf16",
+            "dtype": {"bf16": "bf16",
+                      "nvfp4": "nvfp4 weights+activations, fp4 MMA (kind::mxf4nvf4), f32 accumulate",
+                      "mxfp8": "mxfp8 weights+activations, fp8 MMA (kind::mxf8f6f4), f32 accumulate"
+                      }[fmt],
             "data": "synthetic (seeded N(0,1) activations, N(0,0.02) bf16 weights)",
             "config": {"workload": f"{args.config}{'(' + args.override + ')' if args.override else ''}: T={sh.T} tokens, hidden {sh.H}, "
                                    f"intermediate {sh.I}, {sh.E} experts in {sh.G} groups, "

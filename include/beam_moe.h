@@ -64,7 +64,8 @@ typedef enum {
 /* Expert weight formats. */
 typedef enum {
     BEAM_MOE_W_BF16 = 0,
-    BEAM_MOE_W_NVFP4 = 1
+    BEAM_MOE_W_NVFP4 = 1,
+    BEAM_MOE_W_MXFP8 = 2
 } beam_moe_wtype;
 
 /* debug_flags bits (tests only). */
@@ -278,6 +279,28 @@ int beam_moe_block_forward(const void *stream_in, int step, const float *norm_pr
                            const void *w_gate, const void *w_up, const void *w_down,
                            int64_t T, const beam_moe_cfg *cfg, void *stream_out,
                            void *stream);
+
+/*
+ * MXFP8 weight quantisation (E4M3 values, one power-of-two scale per 32
+ * consecutive elements of a row).  The pages only say an FP8 checkpoint
+ * exists ("Reflection Beam 1.0", section "Mixture of Experts", checkpoint
+ * paragraph); the recipe is a reading, the OCP microscaling rule: shared
+ * exponent E = floor(log2(amax32)) - 8 clamped to [-127, 127] (-127 for an
+ * all-zero block), q = e4m3_rn_satfinite(v / 2^E), scale byte E + 127.
+ *   w        [n_mat, rows, cols] bf16, device; rows % 128 == 0, cols % 128 == 0
+ *   codes    [n_mat, rows, cols] uint8 (E4M3 bits), device, out
+ *   block_sf [n_mat, rows/128, cols/128, 512] uint8, device, out: the scale
+ *            byte of elements [32b, 32b+32) of row r is byte
+ *            16*(r % 32) + 4*((r % 128) / 32) + b % 4 of tile (r/128, b/4)
+ * With cfg->wtype == BEAM_MOE_W_MXFP8, beam_moe_forward takes these codes as
+ * the weight pointers and cfg->w_*_sf as the matching scales (the global
+ * scale pointers are unused); x and h are quantised to MXFP8 the same way
+ * and the expert GEMMs run on the FP8 tensor cores (kind::mxf8f6f4).
+ * All pointers 16-byte aligned.  One kernel launch on `stream`.
+ */
+int beam_moe_quantize_mxfp8(const void *w, int64_t n_mat, int64_t rows,
+                            int64_t cols, void *codes, void *block_sf,
+                            void *stream);
 
 /*
  * Synchronise `stream`, read the device status word of cfg->workspace and

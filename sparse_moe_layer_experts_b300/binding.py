@@ -22,6 +22,7 @@ BEAM_MOE_ERR_DEVICE = -6
 
 BEAM_MOE_W_BF16 = 0
 BEAM_MOE_W_NVFP4 = 1
+BEAM_MOE_W_MXFP8 = 2
 BEAM_MOE_DEBUG_DROP_ONE_LOAD = 0x1
 
 
@@ -81,6 +82,8 @@ def lib():
         L.beam_moe_forward_hostio.restype = ctypes.c_int
         L.beam_moe_quantize_nvfp4.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
         L.beam_moe_quantize_nvfp4.restype = ctypes.c_int
+        L.beam_moe_quantize_mxfp8.argtypes = [vp, i64, i64, i64, vp, vp, vp]
+        L.beam_moe_quantize_mxfp8.restype = ctypes.c_int
         L.beam_moe_read_status.argtypes = [cfgp, vp]
         L.beam_moe_read_status.restype = ctypes.c_int
         L.beam_moe_status_string.argtypes = [ctypes.c_int]
@@ -159,6 +162,10 @@ def beam_moe_block_forward(stream_in, step, norm_pre, norm_post, eps, router_w, 
 def beam_moe_quantize_nvfp4(w, n_mat, rows, cols, packed, block_sf, global_sf, stream) -> int:
     return lib().beam_moe_quantize_nvfp4(w, n_mat, rows, cols, packed, block_sf, global_sf,
                                          stream)
+
+
+def beam_moe_quantize_mxfp8(w, n_mat, rows, cols, codes, block_sf, stream) -> int:
+    return lib().beam_moe_quantize_mxfp8(w, n_mat, rows, cols, codes, block_sf, stream)
 
 
 def beam_moe_read_status(cfg: beam_moe_cfg, stream) -> int:

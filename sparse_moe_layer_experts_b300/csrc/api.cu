@@ -56,7 +56,7 @@ GemmVariant pick_variant(int64_t T, const beam_moe_cfg &c)
 int chunk_rows(int64_t T, const beam_moe_cfg &c)
 {
     const GemmVariant v = pick_variant(T, c);
-    return c.wtype == BEAM_MOE_W_NVFP4 ? fp4_chunk_rows(v) : gemm_chunk_rows(v);
+    return c.wtype != BEAM_MOE_W_BF16 ? fp4_chunk_rows(v) : gemm_chunk_rows(v);
 }
 
 int chunk_rows2(int64_t T, const beam_moe_cfg &c)
@@ -89,12 +89,23 @@ Layout make_layout(int64_t T, const beam_moe_cfg &c)
     L.chunk_start2 = take(sizeof(int32_t) * (E + 1));
     L.row_of = take(sizeof(int32_t) * R);
     L.row_src = take(sizeof(int32_t) * R);
-    const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4;
-    // activations: bf16 rows, or NVFP4 codes (2 per byte)
-    L.x_perm = take(fp4 ? R * H / 2 : 2 * R * H);
-    L.h = take(fp4 ? R * I / 2 : 2 * R * I);
-    L.h_raw = take(fp4 ? 4 * R * I : 0);  // FP32 h before quantisation
+    const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4, mx8 = c.wtype == BEAM_MOE_W_MXFP8;
+    // activations: bf16 rows, NVFP4 codes (2 per byte) or MXFP8 codes
+    L.x_perm = take(fp4 ? R * H / 2 : mx8 ? R * H : 2 * R * H);
+    L.h = take(fp4 ? R * I / 2 : mx8 ? R * I : 2 * R * I);
+    L.h_raw = take(fp4 || mx8 ? 4 * R * I : 0);  // FP32 h before quantisation
     L.y = take(2 * R * H);
+    if (mx8) {
+        // MXFP8: one chunking for both GEMMs; row_pos = chunk*256 + j; scale
+        // atoms [chunk, K/128, 512] for x and h
+        const int64_t cr = chunk_rows(T, c);
+        const int64_t chunks = (R + cr - 1) / cr + E;
+        L.row_pos = take(4 * R);
+        L.x_sf = take((size_t)chunks * (H / 128) * 512);
+        L.h_sf = take((size_t)chunks * (I / 128) * 512);
+        L.total = o;
+        return L;
+    }
     // NVFP4: each row's place in the down GEMM's chunking, and the
     // activations' scales per token chunk: x in atoms [chunk, H/64, 512],
     // h in atoms or in the replicated 256-row images [chunk2, I/64, 4096]
@@ -134,7 +145,8 @@ int check_cfg(const beam_moe_cfg *c)
         return BEAM_MOE_ERR_INVALID_ARG;
     if (!(c->routed_scale == c->routed_scale))  // NaN
         return BEAM_MOE_ERR_INVALID_ARG;
-    if (c->wtype != BEAM_MOE_W_BF16 && c->wtype != BEAM_MOE_W_NVFP4)
+    if (c->wtype != BEAM_MOE_W_BF16 && c->wtype != BEAM_MOE_W_NVFP4 &&
+        c->wtype != BEAM_MOE_W_MXFP8)
         return BEAM_MOE_ERR_INVALID_ARG;
     return BEAM_MOE_OK;
 }
@@ -261,14 +273,20 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     const Layout L = make_layout(T, c);
     void *ws = c.workspace;
     const GemmVariant v = pick_variant(T, c);
-    const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4;
+    const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4, mx8 = c.wtype == BEAM_MOE_W_MXFP8;
     int rc = run_route(x, router_w, T, c, L, at<float>(ws, L.scores), at<int32_t>(ws, L.ids),
                        at<float>(ws, L.wts), chunk_rows(T, c), fp4 ? chunk_rows2(T, c) : 0, s);
     if (rc != BEAM_MOE_OK)
         return rc;
     const int K = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
     const int64_t R = T * K;
-    if (fp4)
+    if (mx8)
+        BEAM_CUDA(launch_permute_mx8(
+            static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids), at<int32_t>(ws, L.local_rank),
+            at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start),
+            (int)T, K, E, H, at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.row_src),
+            at<int32_t>(ws, L.row_pos), at<uint8_t>(ws, L.x_perm), at<uint8_t>(ws, L.x_sf), s));
+    else if (fp4)
         BEAM_CUDA(launch_permute_nvfp4(
             static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids), at<int32_t>(ws, L.local_rank),
             at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start),
@@ -283,7 +301,15 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
 
     CUtensorMap m_wg, m_wu, m_wd, m_xp, m_h;
     bool maps_ok;
-    if (fp4) {
+    if (mx8) {
+        // one byte per element: the code maps' "elements" are bytes here
+        const uint32_t box = (uint32_t)fp4_box_rows(v);
+        maps_ok = make_code_map(&m_wg, w_gate, 2 * H, (uint64_t)E * I, 128) &&
+                  make_code_map(&m_wu, w_up, 2 * H, (uint64_t)E * I, 128) &&
+                  make_code_map(&m_wd, w_down, 2 * I, (uint64_t)E * H, 128) &&
+                  make_code_map(&m_xp, at<void>(ws, L.x_perm), 2 * H, (uint64_t)R, box) &&
+                  make_code_map(&m_h, at<void>(ws, L.h), 2 * I, (uint64_t)R, box);
+    } else if (fp4) {
         const uint32_t box = (uint32_t)fp4_box_rows(v);
         maps_ok = make_code_map(&m_wg, w_gate, H, (uint64_t)E * I, 128) &&
                   make_code_map(&m_wu, w_up, H, (uint64_t)E * I, 128) &&
@@ -316,7 +342,15 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     a.ksteps = H / 64;
     a.out = at<void>(ws, L.h);
     a.out_ld = I;
-    if (fp4) {
+    if (mx8) {
+        Fp4Weights f{static_cast<const uint8_t *>(c.w_gate_sf),
+                     static_cast<const uint8_t *>(c.w_up_sf), nullptr, nullptr,
+                     at<uint8_t>(ws, L.x_sf)};
+        a.out = at<void>(ws, L.h_raw);
+        BEAM_CUDA(launch_gateup_mx8(v, m_wg, m_wu, m_xp, a, f, H / 128, sms, s));
+        BEAM_CUDA(launch_quantize_rows_mx8(at<float>(ws, L.h_raw), R, I, at<int32_t>(ws, L.row_pos),
+                                           at<uint8_t>(ws, L.h), at<uint8_t>(ws, L.h_sf), s));
+    } else if (fp4) {
         Fp4Weights f{static_cast<const uint8_t *>(c.w_gate_sf),
                      static_cast<const uint8_t *>(c.w_up_sf), c.w_gate_gs, c.w_up_gs,
                      at<uint8_t>(ws, L.x_sf)};
@@ -334,7 +368,11 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     a.out = at<void>(ws, L.y);
     a.out_ld = H;
     a.debug_flags = 0;
-    if (fp4) {
+    if (mx8) {
+        Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, nullptr, nullptr,
+                     at<uint8_t>(ws, L.h_sf)};
+        BEAM_CUDA(launch_down_mx8(v, m_wd, m_h, a, f, I / 128, sms, s));
+    } else if (fp4) {
         Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, c.w_down_gs, nullptr,
                      at<uint8_t>(ws, L.h_sf)};
         a.chunk_start = at<int32_t>(ws, L.chunk_start2);  // the down GEMM's own chunking
@@ -521,6 +559,12 @@ int beam_moe_forward(const void *x, const float *router_w, const void *w_gate, c
             if (!q || !aligned16(q))
                 return BEAM_MOE_ERR_INVALID_ARG;
     }
+    if (cfg->wtype == BEAM_MOE_W_MXFP8) {
+        const void *p[3] = {cfg->w_gate_sf, cfg->w_up_sf, cfg->w_down_sf};
+        for (const void *q : p)
+            if (!q || !aligned16(q))
+                return BEAM_MOE_ERR_INVALID_ARG;
+    }
     if (!aligned16(x) || !aligned16(router_w) || !aligned16(w_gate) || !aligned16(w_up) ||
         !aligned16(w_down) || !aligned16(out))
         return BEAM_MOE_ERR_INVALID_ARG;
@@ -574,6 +618,22 @@ int beam_moe_quantize_nvfp4(const void *w, int64_t n_mat, int64_t rows, int64_t 
     BEAM_CUDA(launch_quantize_nvfp4(static_cast<const uint16_t *>(w), n_mat, (int)rows, (int)cols,
                                     static_cast<uint8_t *>(packed),
                                     static_cast<uint8_t *>(block_sf), global_sf,
+                                    static_cast<cudaStream_t>(stream)));
+    return BEAM_MOE_OK;
+}
+
+int beam_moe_quantize_mxfp8(const void *w, int64_t n_mat, int64_t rows, int64_t cols,
+                            void *codes, void *block_sf, void *stream)
+{
+    if (n_mat == 0 || rows == 0)
+        return BEAM_MOE_OK;
+    if (n_mat < 0 || rows < 0 || cols <= 0 || rows % 128 || cols % 128 || rows > (1 << 24) ||
+        cols > (1 << 24) || n_mat > (1 << 20))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (!w || !codes || !block_sf || !aligned16(w) || !aligned16(codes) || !aligned16(block_sf))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    BEAM_CUDA(launch_quantize_mxfp8(static_cast<const uint16_t *>(w), n_mat, (int)rows, (int)cols,
+                                    static_cast<uint8_t *>(codes), static_cast<uint8_t *>(block_sf),
                                     static_cast<cudaStream_t>(stream)));
     return BEAM_MOE_OK;
 }

@@ -315,6 +315,113 @@ combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ w,
 }
 
 
+// ---- MXFP8 activations: E4M3 codes, one shared power-of-two scale per
+// 32 elements (a 32-block is 4 lanes x 8 elements; the lanes take its max
+// with shuffles), scales in token-chunk atoms [chunk, cols/128, 512] at the
+// row's place j in its chunk: byte atom_offset(j) + (32-block % 4).
+
+// 8 values of lane group member -> 8 code bytes; *e the block's exponent
+__device__ __forceinline__ uint2 mx_quant8(const float (&v)[8], unsigned live, int *e)
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(live, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(live, amax, 2));
+    *e = mx_shared_exp(amax);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        lo |= mx_code(v[i], *e) << (8 * i);
+        hi |= mx_code(v[4 + i], *e) << (8 * i);
+    }
+    return make_uint2(lo, hi);
+}
+
+// CTA per token: place its K rows (as permute_kernel), then quantise x once
+// and write the codes to every row and the scales to every row's chunk atom.
+__global__ void __launch_bounds__(256)
+permute_mx8_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
+                   const int32_t *__restrict__ local_rank, const int32_t *__restrict__ cta_base,
+                   const int32_t *__restrict__ offsets, const int32_t *__restrict__ chunk_start,
+                   int T, int K, int E, int H, int32_t *__restrict__ row_of,
+                   int32_t *__restrict__ row_src, int32_t *__restrict__ row_pos,
+                   uint8_t *__restrict__ xq, uint8_t *__restrict__ x_sf)
+{
+    __shared__ int rows[32];
+    __shared__ int pos[32];
+    const int t = blockIdx.x;
+    const int cta = t / kHistTokens;
+    if (threadIdx.x < K) {
+        const int k = threadIdx.x;
+        int e = ids[(size_t)t * K + k];
+        e = (e < 0 || e >= E) ? 0 : e;
+        const int rank = cta_base[(size_t)cta * E + e] + local_rank[(size_t)t * K + k];
+        const int row = offsets[e] + rank;
+        rows[k] = row;
+        row_of[(size_t)t * K + k] = row;
+        row_src[row] = t;
+        int j;
+        const int c = nvfp4_chunk_of_row(rank, offsets[e + 1] - offsets[e],
+                                         chunk_start[e + 1] - chunk_start[e], &j);
+        pos[k] = (chunk_start[e] + c) * 256 + j;
+        row_pos[row] = pos[k];
+    }
+    __syncthreads();
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+    const int nvec = H / 8;
+    const int lane = threadIdx.x & 31;
+    for (int v0 = threadIdx.x & ~31; v0 < nvec; v0 += 256) {
+        const int vi = v0 + lane;
+        const unsigned live = __ballot_sync(0xFFFFFFFFu, vi < nvec);
+        if (vi >= nvec)
+            break;
+        const uint4 q = src[vi];
+        const uint32_t raw[4] = {q.x, q.y, q.z, q.w};
+        float v[8];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            v[2 * p] = bf16_bits_to_f32(raw[p] & 0xFFFFu);
+            v[2 * p + 1] = bf16_bits_to_f32(raw[p] >> 16);
+        }
+        int e;
+        const uint2 codes = mx_quant8(v, live, &e);
+        for (int k = 0; k < K; ++k) {
+            *reinterpret_cast<uint2 *>(xq + (size_t)rows[k] * H + 8 * vi) = codes;
+            if ((vi & 3) == 0) {
+                const int ps = pos[k];
+                x_sf[((size_t)(ps >> 8) * (H / 128) + (vi >> 4)) * 512 +
+                     nvfp4_atom_offset(ps & 255) + ((vi >> 2) & 3)] = (uint8_t)(e + 127);
+            }
+        }
+    }
+}
+
+// MXFP8 h: thread per 8 values of the FP32 matrix [rows, cols]
+__global__ void __launch_bounds__(256)
+quantize_rows_mx8_kernel(const float *__restrict__ in, int64_t n_vec, int cols,
+                         const int32_t *__restrict__ row_pos, uint8_t *__restrict__ codes,
+                         uint8_t *__restrict__ sf)
+{
+    const int64_t b = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    const unsigned live = __ballot_sync(0xFFFFFFFFu, b < n_vec);
+    if (b >= n_vec)
+        return;
+    const float4 f0 = reinterpret_cast<const float4 *>(in)[2 * b];
+    const float4 f1 = reinterpret_cast<const float4 *>(in)[2 * b + 1];
+    const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+    int e;
+    reinterpret_cast<uint2 *>(codes)[b] = mx_quant8(v, live, &e);
+    const int vpr = cols / 8;
+    const int vi = (int)(b % vpr);
+    if ((vi & 3) == 0) {
+        const int ps = row_pos[b / vpr];
+        sf[((size_t)(ps >> 8) * (cols / 128) + (vi >> 4)) * 512 + nvfp4_atom_offset(ps & 255) +
+           ((vi >> 2) & 3)] = (uint8_t)(e + 127);
+    }
+}
+
 // ---- fused MoE block ("Reflection Beam 1.0", section "Residual stream":
 // sublayers are normalised before and after, in FP32; step k keeps the
 // stream with sqrt((k-1)/k) and adds the sublayer output with 1/sqrt(k)).
@@ -596,6 +703,30 @@ cudaError_t launch_combine_block(const uint16_t *y, const float *w, const int32_
     stage_begin(kStCombine, st);
     combine_block_kernel<<<T, 256, 0, st>>>(y, w, row_of, K, H, s_in, gamma, eps, a, b, s_out);
     stage_end(kStCombine, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute_mx8(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
+                               const int32_t *cta_base, const int32_t *offsets,
+                               const int32_t *chunk_start, int T, int K, int E, int H,
+                               int32_t *row_of, int32_t *row_src, int32_t *row_pos,
+                               uint8_t *x_codes, uint8_t *x_sf, cudaStream_t st)
+{
+    stage_begin(kStPermute, st);
+    permute_mx8_kernel<<<T, 256, 0, st>>>(x, ids, local_rank, cta_base, offsets, chunk_start, T, K,
+                                          E, H, row_of, row_src, row_pos, x_codes, x_sf);
+    stage_end(kStPermute, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows_mx8(const float *in, int64_t rows, int cols, const int32_t *row_pos,
+                                     uint8_t *codes, uint8_t *sf, cudaStream_t st)
+{
+    const int64_t n_vec = rows * (int64_t)(cols / 8);
+    stage_begin(kStQuantH, st);
+    quantize_rows_mx8_kernel<<<(unsigned)((n_vec + 255) / 256), 256, 0, st>>>(in, n_vec, cols,
+                                                                             row_pos, codes, sf);
+    stage_end(kStQuantH, st);
     return cudaGetLastError();
 }
 

@@ -31,6 +31,13 @@
 // 64: a last k-step with fewer than four 64-blocks issues fewer MMAs, and its
 // code tiles are zero-filled by TMA past the row end.
 //
+// MX8 variants run the MXFP8 experts (E4M3 values, one power-of-two UE8M0
+// scale per 32 elements, no global scale) through the same pipeline: a
+// k-step is 128 FP8 elements (the same 128-byte row), its scales one atom
+// per operand (4 bytes per row, one per 32-block), copied once, and the four
+// MMAs of kind::mxf8f6f4 (K = 32, scale_vec::1X) pick byte kk of it with the
+// scale-factor ids of the instruction descriptor.
+//
 // Warp roles: warp 0 TMA/bulk-copy producer, warp 1 TMEM allocator and MMA
 // issuer, then EPI_WG epilogue warpgroups splitting a tile's columns.
 #include "common.cuh"
@@ -52,20 +59,24 @@ constexpr int kAtom = 512;                        // scales of 128 rows x 64 ele
 constexpr int kSfStep = 4 * kAtom;                // scales of one k-step
 constexpr int kMaxExperts = 256;
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP,
+          bool MX8 = false>
 struct CfgN {
     static constexpr int NA = GATEUP ? 2 : 1;
     static constexpr int THREADS = 64 + 128 * EPI_WG;
     static constexpr int A_BYTES = NA * kACodeBytes;
     static constexpr int B_BYTES = BN * kRowBytes;
-    static constexpr int SFA_BYTES = NA * kSfStep;
-    static constexpr int SFB_KB_BYTES = SFB_REP ? 4096 : kAtom;  // token scales of one 64-block
-    static constexpr int SFB_BYTES = 4 * SFB_KB_BYTES;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int SFA_MAT = MX8 ? kAtom : kSfStep;  // one weight matrix's scales per stage
+    static constexpr int SFA_BYTES = NA * SFA_MAT;
+    static constexpr int SFB_KB_BYTES = SFB_REP ? 4096 : kAtom;  // token scales of one atom unit
+    static constexpr int SFB_BYTES = MX8 ? kAtom : 4 * SFB_KB_BYTES;
+    static constexpr int SF_BYTES = ((SFA_BYTES + SFB_BYTES + 1023) / 1024) * 1024;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
     static constexpr int BOX_BYTES = BOX * kRowBytes;
     static constexpr int ACC_COLS = NA * BN;
-    static constexpr int SFB_COLS = SFB_REP ? 32 : 16;
-    static constexpr int SF_COLS = NA * 16 + SFB_COLS;  // per stage: 4 columns per atom
+    static constexpr int SFA_COLS = MX8 ? 4 : 16;  // per weight matrix and stage
+    static constexpr int SFB_COLS = MX8 ? 4 : SFB_REP ? 32 : 16;
+    static constexpr int SF_COLS = NA * SFA_COLS + SFB_COLS;
     static constexpr int SF_COL0 = ACC_BUFS * ACC_COLS;
     static constexpr int COLS_NEED = SF_COL0 + STAGES * SF_COLS;
     static constexpr int TMEM_COLS = COLS_NEED <= 32    ? 32
@@ -78,6 +89,7 @@ struct CfgN {
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + ((AUX_BYTES + 127) / 128) * 128;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= (SFB_REP ? 256 : 128),
                   "MMA N; token scale atoms per chunk");
+    static_assert(!(MX8 && SFB_REP), "MXFP8 token scales are atoms");
     static_assert(BN % BOX == 0 && BOX % 8 == 0, "token boxes tile the B operand");
     static_assert(COLS_NEED <= 512, "TMEM columns");
     static_assert(STAGE_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle-atom alignment");
@@ -87,7 +99,7 @@ struct CfgN {
 struct Fp4Params {
     GemmArgs a;
     Fp4Weights f;
-    int kblocks;  // K / 64 of this GEMM
+    int kblocks;  // 512-byte scale atoms per operand row tile: K / 64 (NVFP4), K / 128 (MXFP8)
 };
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
@@ -151,18 +163,40 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// MXFP8: E4M3 x E4M3 (format 0), UE8M0 scales (bit 23), both K-major, FP32
+// accumulator; the scale-factor ids (bits 29-30 for A, 4-5 for B) are OR-ed
+// in per MMA.
+__device__ __forceinline__ uint32_t idesc_mx8(uint32_t m, uint32_t n)
+{
+    return (1u << 23) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_mx8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                        uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+        "[%5], [%6], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
 __device__ __forceinline__ float silu_mul_f(float g, float u)
 {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP,
+          bool MX8>
 __global__ void __launch_bounds__(64 + 128 * EPI_WG, 1)
 grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                          const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB, const Fp4Params P)
 {
-    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP>;
+    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP, MX8>;
     const GemmArgs &p = P.a;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -240,7 +274,10 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                 const uint8_t *sfb = P.f.act_sf + (size_t)chunk * KB * C::SFB_KB_BYTES;
                 const int nb = (tl.nrows + BOX - 1) / BOX;
                 for (int k = 0; k < p.ksteps; ++k) {
-                    const int nkb = min(4, KB - 4 * k);
+                    // scale atoms of this k-step: MXFP8 one per operand, NVFP4
+                    // one per 64-block (a short last k-step has fewer)
+                    const int nkb = MX8 ? 1 : min(4, KB - 4 * k);
+                    const int atom0 = MX8 ? k : 4 * k;
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, tmo, s_abort, p.status)) {
                         ok = false;
                         break;
@@ -258,11 +295,11 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                     for (int bb = 0; bb < nb; ++bb)
                         tma_load_2d(st + C::A_BYTES + bb * C::BOX_BYTES, &tmB, k * kRowBytes,
                                     tl.row0 + bb * BOX, full_bar(stage));
-                    bulk_g2s(sf, sfa0 + (size_t)4 * k * kAtom, nkb * kAtom, full_bar(stage));
+                    bulk_g2s(sf, sfa0 + (size_t)atom0 * kAtom, nkb * kAtom, full_bar(stage));
                     if (GATEUP)
-                        bulk_g2s(sf + kSfStep, sfa1 + (size_t)4 * k * kAtom, nkb * kAtom,
+                        bulk_g2s(sf + C::SFA_MAT, sfa1 + (size_t)atom0 * kAtom, nkb * kAtom,
                                  full_bar(stage));
-                    bulk_g2s(sf + C::SFA_BYTES, sfb + (size_t)4 * k * C::SFB_KB_BYTES,
+                    bulk_g2s(sf + C::SFA_BYTES, sfb + (size_t)atom0 * C::SFB_KB_BYTES,
                              nkb * C::SFB_KB_BYTES, full_bar(stage));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -284,7 +321,8 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const Tile tl = decode_tile(t, s_off, s_cs, E, p.m_tiles);
-                const uint32_t idesc = idesc_nvf4(kBlockM, (uint32_t)((tl.nrows + 15) & ~15));
+                const uint32_t n_mma = (uint32_t)((tl.nrows + 15) & ~15);
+                const uint32_t idesc = MX8 ? idesc_mx8(kBlockM, n_mma) : idesc_nvf4(kBlockM, n_mma);
                 if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, tmo, s_abort, p.status)) {
                     ok = false;
                     break;
@@ -292,7 +330,7 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * C::ACC_COLS;
                 for (int k = 0; k < p.ksteps; ++k) {
-                    const int nkb = min(4, KB - 4 * k);
+                    const int nkb = MX8 ? 4 : min(4, KB - 4 * k);  // MMAs of this k-step
                     if (!mbar_wait_bounded(full_bar(stage), phase, tmo, s_abort, p.status)) {
                         ok = false;
                         break;
@@ -304,25 +342,42 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                     // 32 = 8 per 64-block in the replicated form); every MMA
                     // scale address is a multiple of 4 columns
                     const uint32_t ts = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
-                    const uint32_t tsb = ts + 16 * C::NA;
-                    constexpr uint32_t kbB = SFB_REP ? 8 : 4;
-                    for (int kb = 0; kb < nkb; ++kb) {
-                        tmem_cp_atom(ts + 4 * kb, sf + kb * kAtom);
+                    const uint32_t tsb = ts + C::SFA_COLS * C::NA;
+                    if constexpr (MX8) {
+                        // one atom per operand; MMA kb reads byte kb of it
+                        tmem_cp_atom(ts, sf);
                         if (GATEUP)
-                            tmem_cp_atom(ts + 16 + 4 * kb, sf + kSfStep + kb * kAtom);
-                        if constexpr (SFB_REP)
-                            tmem_cp_pair(tsb + kbB * kb, sf + C::SFA_BYTES + kb * C::SFB_KB_BYTES);
-                        else
-                            tmem_cp_atom(tsb + kbB * kb, sf + C::SFA_BYTES + kb * kAtom);
-                    }
-                    for (int kb = 0; kb < nkb; ++kb) {
-                        const uint64_t bd = smem_desc_k128(st + C::A_BYTES + kb * 32);
-                        const uint32_t accum = (k | kb) != 0;
-                        mma_nvf4(d, smem_desc_k128(st + kb * 32), bd, idesc, ts + 4 * kb,
-                                 tsb + kbB * kb, accum);
-                        if (GATEUP)
-                            mma_nvf4(d + BN, smem_desc_k128(st + kACodeBytes + kb * 32), bd, idesc,
-                                     ts + 16 + 4 * kb, tsb + kbB * kb, accum);
+                            tmem_cp_atom(ts + 4, sf + C::SFA_MAT);
+                        tmem_cp_atom(tsb, sf + C::SFA_BYTES);
+                        for (int kb = 0; kb < 4; ++kb) {
+                            const uint64_t bd = smem_desc_k128(st + C::A_BYTES + kb * 32);
+                            const uint32_t accum = (k | kb) != 0;
+                            const uint32_t id = idesc | ((uint32_t)kb << 29) | ((uint32_t)kb << 4);
+                            mma_mx8(d, smem_desc_k128(st + kb * 32), bd, id, ts, tsb, accum);
+                            if (GATEUP)
+                                mma_mx8(d + BN, smem_desc_k128(st + kACodeBytes + kb * 32), bd, id,
+                                        ts + 4, tsb, accum);
+                        }
+                    } else {
+                        constexpr uint32_t kbB = SFB_REP ? 8 : 4;
+                        for (int kb = 0; kb < nkb; ++kb) {
+                            tmem_cp_atom(ts + 4 * kb, sf + kb * kAtom);
+                            if (GATEUP)
+                                tmem_cp_atom(ts + 16 + 4 * kb, sf + kSfStep + kb * kAtom);
+                            if constexpr (SFB_REP)
+                                tmem_cp_pair(tsb + kbB * kb, sf + C::SFA_BYTES + kb * C::SFB_KB_BYTES);
+                            else
+                                tmem_cp_atom(tsb + kbB * kb, sf + C::SFA_BYTES + kb * kAtom);
+                        }
+                        for (int kb = 0; kb < nkb; ++kb) {
+                            const uint64_t bd = smem_desc_k128(st + C::A_BYTES + kb * 32);
+                            const uint32_t accum = (k | kb) != 0;
+                            mma_nvf4(d, smem_desc_k128(st + kb * 32), bd, idesc, ts + 4 * kb,
+                                     tsb + kbB * kb, accum);
+                            if (GATEUP)
+                                mma_nvf4(d + BN, smem_desc_k128(st + kACodeBytes + kb * 32), bd,
+                                         idesc, ts + 16 + 4 * kb, tsb + kbB * kb, accum);
+                        }
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == STAGES) {
@@ -353,8 +408,8 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
             const Tile tl = decode_tile(t, s_off, s_cs, E, p.m_tiles);
-            const float g0 = P.f.gs0[tl.e];
-            const float g1 = GATEUP ? P.f.gs1[tl.e] : 0.0f;
+            const float g0 = MX8 ? 1.0f : P.f.gs0[tl.e];
+            const float g1 = GATEUP ? (MX8 ? 1.0f : P.f.gs1[tl.e]) : 0.0f;
             if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, tmo, s_abort, p.status))
                 break;
             tc_fence_after();
@@ -433,13 +488,14 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
     }
 }
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP = false>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP = false,
+          bool MX8 = false>
 cudaError_t launch_nvf4_variant(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                                 const GemmArgs &args, const Fp4Weights &f, int kblocks, int grid,
                                 int stage, cudaStream_t s)
 {
-    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP>;
-    auto kern = grouped_gemm_nvf4_kernel<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP>;
+    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP, MX8>;
+    auto kern = grouped_gemm_nvf4_kernel<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP, MX8>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -450,7 +506,7 @@ cudaError_t launch_nvf4_variant(const CUtensorMap &a0, const CUtensorMap &a1, co
         return attr_err;
     Fp4Params P;
     P.a = args;
-    P.a.ksteps = (kblocks + 3) / 4;
+    P.a.ksteps = MX8 ? kblocks : (kblocks + 3) / 4;
     P.f = f;
     P.kblocks = kblocks;
     stage_begin(stage, s);
@@ -501,6 +557,28 @@ cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensor
                                                            s);
     return launch_nvf4_variant<false, 256, 3, 1, 128, 2, true>(wd, wd, hq, a, f, kblocks, grid,
                                                                kStDown, s);
+}
+
+cudaError_t launch_gateup_mx8(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
+                              const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
+                              int kblocks, int grid, cudaStream_t s)
+{
+    if (v == GemmVariant::kDecode)
+        return launch_nvf4_variant<true, 32, 5, 2, 16, 1, false, true>(wg, wu, xq, a, f, kblocks,
+                                                                       grid, kStGateUp, s);
+    return launch_nvf4_variant<true, 128, 4, 1, 128, 2, false, true>(wg, wu, xq, a, f, kblocks,
+                                                                     grid, kStGateUp, s);
+}
+
+cudaError_t launch_down_mx8(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hq,
+                            const GemmArgs &a, const Fp4Weights &f, int kblocks, int grid,
+                            cudaStream_t s)
+{
+    if (v == GemmVariant::kDecode)
+        return launch_nvf4_variant<false, 32, 10, 2, 16, 1, false, true>(wd, wd, hq, a, f, kblocks,
+                                                                         grid, kStDown, s);
+    return launch_nvf4_variant<false, 128, 6, 2, 128, 2, false, true>(wd, wd, hq, a, f, kblocks,
+                                                                      grid, kStDown, s);
 }
 
 }  // namespace beam

@@ -49,6 +49,17 @@ cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t 
                            const int32_t *cta_base, const int32_t *offsets, int T, int K, int E,
                            int H, int32_t *row_of, int32_t *row_src, void *x_perm,
                            cudaStream_t s);
+// MXFP8 layers: x rows into E4M3 codes [R, H] and scale atoms
+// [chunk, H/128, 512] of the chunking (chunk_start); row_pos[row] = chunk*256 + j
+cudaError_t launch_permute_mx8(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
+                               const int32_t *cta_base, const int32_t *offsets,
+                               const int32_t *chunk_start, int T, int K, int E, int H,
+                               int32_t *row_of, int32_t *row_src, int32_t *row_pos,
+                               uint8_t *x_codes, uint8_t *x_sf, cudaStream_t s);
+// MXFP8 h: FP32 [rows, cols] -> E4M3 codes [rows, cols] and scale atoms
+// [chunk, cols/128, 512] at row_pos
+cudaError_t launch_quantize_rows_mx8(const float *in, int64_t rows, int cols, const int32_t *row_pos,
+                                     uint8_t *codes, uint8_t *sf, cudaStream_t s);
 // NVFP4 layers: x rows quantised (global scale 1) into codes [R, H/2] and
 // scale atoms [chunk, H/64, 512] of the gate/up chunking (chunk_start);
 // row_pos[row] = chunk2*256 + j2 in the down GEMM's chunking (chunk_start2)
@@ -112,6 +123,9 @@ struct Fp4Weights {
 cudaError_t launch_quantize_nvfp4(const uint16_t *w, int64_t n_mat, int rows, int cols,
                                   uint8_t *packed, uint8_t *block_sf, float *global_sf,
                                   cudaStream_t s);
+// MXFP8: codes [n_mat, rows, cols] E4M3, block_sf [n_mat, rows/128, cols/128, 512]
+cudaError_t launch_quantize_mxfp8(const uint16_t *w, int64_t n_mat, int rows, int cols,
+                                  uint8_t *codes, uint8_t *block_sf, cudaStream_t s);
 
 // chunk height (rows of one expert handled by one tile) of a variant
 int gemm_chunk_rows(GemmVariant v);
@@ -142,6 +156,16 @@ int fp4_chunk_rows(GemmVariant v);
 int fp4_down_chunk_rows(GemmVariant v);
 bool fp4_down_rep(GemmVariant v);
 int fp4_box_rows(GemmVariant v);
+// MXFP8 experts on the same kernels (kind::mxf8f6f4): E4M3 codes, one
+// UE8M0 scale per 32 elements, scale atoms [.., K/128, 512]; kblocks = K/128;
+// chunks of fp4_chunk_rows(v) rows for both GEMMs, activation scales in
+// atoms; gate/up writes h in FP32 for launch_quantize_rows_mx8.
+cudaError_t launch_gateup_mx8(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
+                              const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
+                              int kblocks, int grid, cudaStream_t s);
+cudaError_t launch_down_mx8(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hq,
+                            const GemmArgs &a, const Fp4Weights &f, int kblocks, int grid,
+                            cudaStream_t s);
 cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
                               const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
                               int kblocks, int grid, cudaStream_t s);

@@ -96,7 +96,64 @@ nvfp4_quantize_kernel(const uint16_t *__restrict__ w, int64_t n_blocks, int rows
     block_sf[tile * 512 + nvfp4_atom_offset(r % 128) + (cb % 4)] = (uint8_t)sc;
 }
 
+// MXFP8: one thread per 32-element block (codes E4M3, scale byte E + 127 in
+// the tile of 128 rows x 128 columns at the atom offset of row r % 128).
+__global__ void __launch_bounds__(256)
+mxfp8_quantize_kernel(const uint16_t *__restrict__ w, int64_t n_blocks, int rows, int cols,
+                      uint8_t *__restrict__ codes, uint8_t *__restrict__ block_sf)
+{
+    const int64_t b = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (b >= n_blocks)
+        return;
+    const int bpr = cols / 32;
+    const int64_t per_mat = (int64_t)rows * bpr;
+    const int64_t mat = b / per_mat;
+    const int64_t rem = b - mat * per_mat;
+    const int r = (int)(rem / bpr), cb = (int)(rem % bpr);
+    const int64_t elem = (mat * rows + r) * (int64_t)cols + (int64_t)cb * 32;
+    float v[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(w + elem + 8 * q);
+        const uint32_t raw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            v[8 * q + 2 * p] = bf16_bits_to_f32(raw[p] & 0xFFFFu);
+            v[8 * q + 2 * p + 1] = bf16_bits_to_f32(raw[p] >> 16);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        amax = fmaxf(amax, fabsf(v[i]));
+    const int e = mx_shared_exp(amax);
+    uint32_t out[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        out[q] = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            out[q] |= mx_code(v[4 * q + i], e) << (8 * i);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(codes + elem);
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    const int64_t tile = (mat * (rows / 128) + r / 128) * (cols / 128) + cb / 4;
+    block_sf[tile * 512 + nvfp4_atom_offset(r % 128) + (cb % 4)] = (uint8_t)(e + 127);
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_mxfp8(const uint16_t *w, int64_t n_mat, int rows, int cols,
+                                  uint8_t *codes, uint8_t *block_sf, cudaStream_t s)
+{
+    const int64_t n_blocks = n_mat * rows * (int64_t)(cols / 32);
+    stage_begin(kNumStages, s);
+    mxfp8_quantize_kernel<<<(unsigned)((n_blocks + 255) / 256), 256, 0, s>>>(w, n_blocks, rows, cols,
+                                                                             codes, block_sf);
+    stage_end(kNumStages, s);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_nvfp4(const uint16_t *w, int64_t n_mat, int rows, int cols,
                                   uint8_t *packed, uint8_t *block_sf, float *global_sf,

@@ -98,6 +98,24 @@ __device__ __forceinline__ uint32_t nvfp4_quant16(const float (&v)[16], uint32_t
     return sc;
 }
 
+// MXFP8 (OCP microscaling, E4M3 elements): shared exponent of a 32-block
+// with largest magnitude amax: floor(log2(amax)) - 8 clamped to [-127, 127],
+// -127 for an all-zero block.  The scale byte is E + 127.
+__device__ __forceinline__ int mx_shared_exp(float amax)
+{
+    if (!(amax > 0.0f))
+        return -127;
+    int ex;
+    frexpf(amax, &ex);  // amax = m * 2^ex, m in [0.5, 1)
+    return max(-127, min(127, ex - 1 - 8));
+}
+
+// E4M3 code of v / 2^e (exact scaling), round to nearest even, saturating
+__device__ __forceinline__ uint32_t mx_code(float v, int e)
+{
+    return (uint32_t)__nv_cvt_float_to_fp8(ldexpf(v, -e), __NV_SATFINITE, __NV_E4M3);
+}
+
 // Token chunks: an expert's n rows are split into nc near-equal chunks,
 // chunk c holding rows [floor(c*n/nc), floor((c+1)*n/nc)) (the N tiles of
 // the grouped GEMMs).  Returns the chunk of row i (0-based inside the

@@ -32,6 +32,22 @@ def quantize_nvfp4(w: torch.Tensor, stream=None):
     return packed, sf, gs
 
 
+def quantize_mxfp8(w: torch.Tensor, stream=None):
+    """MXFP8-quantise bf16 matrices [n_mat, rows, cols] on the GPU.
+
+    Returns (E4M3 codes [n_mat, rows, cols] uint8, block scales (flat uint8,
+    the tiled layout of beam_moe_quantize_mxfp8))."""
+    if w.dtype != torch.bfloat16 or w.dim() != 3 or not w.is_cuda or not w.is_contiguous():
+        raise ValueError("w must be a contiguous CUDA bf16 [n_mat, rows, cols] tensor")
+    n_mat, rows, cols = w.shape
+    codes = torch.empty((n_mat, rows, cols), dtype=torch.uint8, device=w.device)
+    sf = torch.empty(n_mat * rows * (cols // 32), dtype=torch.uint8, device=w.device)
+    B.check(B.beam_moe_quantize_mxfp8(w.data_ptr(), n_mat, rows, cols, codes.data_ptr(),
+                                      sf.data_ptr(), _stream_handle(stream)),
+            "beam_moe_quantize_mxfp8")
+    return codes, sf
+
+
 class BeamMoE:
     """Resident-weight layer.  Weights: w_gate/w_up [E,I,H] bf16, w_down [E,H,I]
     bf16, router_w [H,E] fp32, all contiguous on one CUDA device.  For NVFP4
@@ -71,6 +87,19 @@ class BeamMoE:
             q[1].data_ptr() for q in (q_gate, q_up, q_down))
         self.cfg.w_gate_gs, self.cfg.w_up_gs, self.cfg.w_down_gs = (
             q[2].data_ptr() for q in (q_gate, q_up, q_down))
+        return self
+
+    @classmethod
+    def mxfp8(cls, router_w, q_gate, q_up, q_down, n_groups=8, topk_groups=4, top_k=8,
+              routed_scale=2.5, wait_timeout_ns=0):
+        """Layer with MXFP8 experts; q_* = quantize_mxfp8(w_*)."""
+        self = cls.__new__(cls)
+        E, I, H = q_gate[0].shape
+        self._setup(router_w, q_gate[0], q_up[0], q_down[0], E, I, H, n_groups, topk_groups,
+                    top_k, routed_scale, wait_timeout_ns, 0, B.BEAM_MOE_W_MXFP8)
+        self._scales = (q_gate, q_up, q_down)  # keep them alive
+        self.cfg.w_gate_sf, self.cfg.w_up_sf, self.cfg.w_down_sf = (
+            q[1].data_ptr() for q in (q_gate, q_up, q_down))
         return self
 
     @property

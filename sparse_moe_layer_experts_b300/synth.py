@@ -50,6 +50,8 @@ CONFIGS = {
                    routing="zipf"),
     "nvfp4": dict(T=8192, H=5120, I=2560, E=256, G=8, topk_groups=4, top_k=8,
                   routing="random"),
+    # the decode batch with MXFP8 experts
+    "mxfp8": dict(T=32, H=5120, I=2560, E=256, G=8, topk_groups=4, top_k=8, routing="random"),
 }
 
 DENSE_CONFIGS = {
