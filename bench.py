@@ -217,7 +217,8 @@ KERNEL_SOURCES = {
     "gateup_gemm": ("grouped_gemm.cu", "gemm_common.cuh", "common.cuh"),
     "down_gemm": ("grouped_gemm.cu", "grouped_gemm_pair.cu", "gemm_common.cuh", "common.cuh"),
 }
-FP4_GEMM_SOURCES = ("grouped_gemm_fp4.cu", "gemm_common.cuh", "common.cuh", "nvfp4.cuh")
+FP4_GEMM_SOURCES = ("grouped_gemm_fp4.cu", "grouped_gemm_tm.cu", "blockscaled.cuh",
+                    "gemm_common.cuh", "common.cuh", "nvfp4.cuh")
 
 
 def weight_format(config: str) -> str:
@@ -251,17 +252,25 @@ def ncu_traffic(kernel: str, workload: str):
     return e.get("bytes_per_launch")
 
 
+def token_major(sh, fmt: str) -> bool:
+    """NVFP4 / MXFP8 layers at prefill size (more than 16 rows per expert on
+    average) run the token-major GEMMs, whose gate/up writes h quantised."""
+    return fmt != "bf16" and sh.T * sh.top_k > 16 * sh.E
+
+
 def workload_algorithmic(sh, n_active: int, fmt: str = "bf16"):
     """Algorithmic bytes / FLOPs per launch of each kernel (compulsory traffic
     of the kernel's own inputs and outputs; expert weights of active experts
     only).  NVFP4 weights and activations: 0.5 B per code + 1/16 B of block
-    scale; NVFP4 h leaves gate/up in FP32 for the quantize_h pass."""
+    scale.  At decode size an NVFP4 / MXFP8 h leaves gate/up in FP32 for the
+    quantize_h pass; at prefill size gate/up writes it quantised."""
     T, H, I, E, K = sh.T, sh.H, sh.I, sh.E, sh.top_k
     R = T * K
     # bytes per element: NVFP4 0.5 + 1/16 of scale, MXFP8 1 + 1/32
     wb = {"bf16": 2, "nvfp4": 0.5625, "mxfp8": 1.03125}[fmt]
     ab = wb                             # activation operand bytes per element
-    hb = 2 if fmt == "bf16" else 4      # h as written by gate/up (FP32 before quantisation)
+    # h as written by gate/up
+    hb = 2 if fmt == "bf16" else (wb if token_major(sh, fmt) else 4)
     w_gu = int(n_active * 2 * I * H * wb)
     w_d = int(n_active * H * I * wb)
     return {
@@ -511,9 +520,11 @@ def run_ours(args, world, rank, local):
     ms_max = max_over_ranks(ms, world, dev)
     if layer.status() != 0:
         raise SystemExit("device status word reports an error in the timed region")
+    # stages the path launched: their events were recorded inside the timed
+    # region (the others keep their setup records from before `start`)
+    ran = [start.elapsed_time(ev[-1][j][0]) >= 0.0 for j in range(nst)]
     per_kernel_ms = {name: sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps))
-                     / args.steps for j, name in enumerate(B.KERNEL_STAGES)
-                     if (fmt != "bf16" or name != "quantize_h") and (args.block or name != "prenorm")}
+                     / args.steps for j, name in enumerate(B.KERNEL_STAGES) if ran[j]}
 
     # end to end through the host-I/O entry point (pinned host buffers)
     e2e = None

@@ -93,7 +93,9 @@ Layout make_layout(int64_t T, const beam_moe_cfg &c)
     // activations: bf16 rows, NVFP4 codes (2 per byte) or MXFP8 codes
     L.x_perm = take(fp4 ? R * H / 2 : mx8 ? R * H : 2 * R * H);
     L.h = take(fp4 ? R * I / 2 : mx8 ? R * I : 2 * R * I);
-    L.h_raw = take(fp4 || mx8 ? 4 * R * I : 0);  // FP32 h before quantisation
+    // FP32 h before quantisation (decode-size batches; the token-major
+    // prefill kernels quantise h in their epilogue)
+    L.h_raw = take((fp4 || mx8) && pick_variant(T, c) == GemmVariant::kDecode ? 4 * R * I : 0);
     L.y = take(2 * R * H);
     if (mx8) {
         // MXFP8: one chunking for both GEMMs; row_pos = chunk*256 + j; scale
@@ -342,7 +344,16 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     a.ksteps = H / 64;
     a.out = at<void>(ws, L.h);
     a.out_ld = I;
-    if (mx8) {
+    const bool tm = v == GemmVariant::kPrefill;
+    if ((mx8 || fp4) && tm) {
+        // token-major gate/up with h quantised in the epilogue
+        Fp4Weights f{static_cast<const uint8_t *>(c.w_gate_sf),
+                     static_cast<const uint8_t *>(c.w_up_sf), mx8 ? nullptr : c.w_gate_gs,
+                     mx8 ? nullptr : c.w_up_gs, at<uint8_t>(ws, L.x_sf)};
+        a.out = at<void>(ws, L.h);
+        BEAM_CUDA(launch_gateup_tm(mx8, m_wg, m_wu, m_xp, a, f, mx8 ? H / 128 : H / 64,
+                                   at<uint8_t>(ws, L.h_sf), at<int32_t>(ws, L.row_pos), sms, s));
+    } else if (mx8) {
         Fp4Weights f{static_cast<const uint8_t *>(c.w_gate_sf),
                      static_cast<const uint8_t *>(c.w_up_sf), nullptr, nullptr,
                      at<uint8_t>(ws, L.x_sf)};
@@ -371,7 +382,10 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     if (mx8) {
         Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, nullptr, nullptr,
                      at<uint8_t>(ws, L.h_sf)};
-        BEAM_CUDA(launch_down_mx8(v, m_wd, m_h, a, f, I / 128, sms, s));
+        if (tm && (H / 128) % 2 == 0)
+            BEAM_CUDA(launch_down_tm_mx8(m_wd, m_h, a, f, I / 128, sms, s));
+        else
+            BEAM_CUDA(launch_down_mx8(v, m_wd, m_h, a, f, I / 128, sms, s));
     } else if (fp4) {
         Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, c.w_down_gs, nullptr,
                      at<uint8_t>(ws, L.h_sf)};

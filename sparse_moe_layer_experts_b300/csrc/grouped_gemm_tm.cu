@@ -1,0 +1,448 @@
+// Token-major NVFP4 / MXFP8 grouped expert GEMMs for token-heavy (prefill-size)
+// batches: the expert's token rows are the M = 128 operand and 256 weight
+// rows the N operand, so each block-scaled MMA is 128 x 256.
+//
+// Same computation as the prefill GEMMs of grouped_gemm_fp4.cu (the SwiGLU
+// experts of "Reflection Beam 1.0", section "Mixture of Experts", with NVFP4
+// or MXFP8 operands), laid out for the tensor pipe's cost model: every
+// tcgen05 instruction costs a roughly fixed number of cycles (about 142 for
+// an N <= 128 MMA, 161 for N = 256, plus the scale copies), so one 128 x 256
+// MMA per 64-block does the work of the two 128 x 128 MMAs the weight-major
+// gate/up kernel issues.
+//
+// Gate/up: the N operand is gate tile m (rows 0-127) stacked on up tile m
+// (rows 128-255), so one accumulator holds g and u side by side for 128
+// tokens x 128 features.  Each epilogue thread owns one token row and 64
+// consecutive features, i.e. whole quantisation blocks of h: it computes
+// h = silu(g) * u in FP32 and quantises h itself (NVFP4: 16-blocks with E4M3
+// scales; MXFP8: 32-blocks with power-of-two scales), writing the codes and
+// the token-chunk scale layout the down GEMM reads.  No FP32 h goes to
+// memory.  Down (MXFP8): the N operand is weight tiles 2m and 2m+1 (256
+// output features); the epilogue writes bf16 y rows.
+//
+// Scales: the token chunk's atom per 64-block (NVFP4) or per 128-deep k-step
+// (MXFP8) goes to tensor memory as the A scales; the two weight tiles'
+// atoms as the B scales, the second one 4 columns after the first (rows
+// 128-255 of an N = 256 operand).  Every B scale address is a multiple of 8
+// columns, every A scale address a multiple of 4.
+//
+// Warp roles: warp 0 TMA / bulk-copy producer, warp 1 TMEM allocator and MMA
+// issuer, two epilogue warpgroups (features split in halves).  One
+// accumulator: the epilogue loads its 128 values into registers and releases
+// the accumulator before the arithmetic and the stores.  Waits are bounded.
+#include "blockscaled.cuh"
+#include "common.cuh"
+#include "gemm_common.cuh"
+#include "internal.h"
+#include "nvfp4.cuh"
+
+#include <mutex>
+
+namespace beam {
+
+namespace {
+
+constexpr int kBlockM = 128;   // token rows per tile
+constexpr int kRowBytes = 128;  // one 128-byte swizzle row of codes per k-step
+constexpr int kAtom = 512;
+constexpr int kMaxExperts = 256;
+constexpr int kEpiWG = 2;
+constexpr int kThreads = 64 + 128 * kEpiWG;
+
+template <bool GATEUP, bool MX8, int STAGES>
+struct TmCfg {
+    static constexpr int A_BYTES = kBlockM * kRowBytes;  // token codes
+    static constexpr int B_BYTES = 256 * kRowBytes;      // two weight tiles
+    static constexpr int ATOMS = MX8 ? 1 : 4;            // scale atoms per operand and k-step
+    static constexpr int SF_OP = ATOMS * kAtom;          // one operand's scales per stage
+    static constexpr int SF_BYTES = ((3 * SF_OP + 1023) / 1024) * 1024;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+    static constexpr int ACC_COLS = 256;
+    // per stage: A scales (4 per atom), then B scales (8 per atom: tile 0 at
+    // +0, tile 1 at +4), B starting on a multiple of 8
+    static constexpr int SFA_COLS = MX8 ? 8 : 16;
+    static constexpr int SF_COLS = SFA_COLS + 8 * ATOMS;
+    static constexpr int SF_COL0 = ACC_COLS;
+    static constexpr int COLS_NEED = SF_COL0 + STAGES * SF_COLS;
+    static constexpr int TMEM_COLS = COLS_NEED <= 256 ? 256 : 512;
+    static constexpr int N_BARS = 2 * STAGES + 3;
+    static constexpr int AUX_BYTES = N_BARS * 8 + 16 + 2 * (kMaxExperts + 1) * 4;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + ((AUX_BYTES + 127) / 128) * 128;
+    static_assert(SF_COL0 % 8 == 0 && SF_COLS % 8 == 0 && SFA_COLS % 8 == 0,
+                  "B scale columns on multiples of 8");
+    static_assert(COLS_NEED <= 512, "TMEM columns");
+    static_assert(STAGE_BYTES % 1024 == 0, "swizzle-atom alignment");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+struct TmParams {
+    GemmArgs a;      // m_tiles = 256-row weight tile pairs per expert; out = h codes / y
+    Fp4Weights f;    // sf0 / sf1 weight atoms, gs0 / gs1 (NVFP4), act_sf token atoms
+    int kblocks;     // scale atoms per operand row tile: K/64 (NVFP4), K/128 (MXFP8)
+    int n_tiles_w;   // 128-row weight tiles per expert in sf0 / the B maps
+    uint8_t *h_sf;   // gate/up: scales of h (NVFP4: replicated 256-row images; MXFP8: atoms)
+    const int32_t *row_pos;  // gate/up: row -> chunk * 256 + position (down GEMM's chunking)
+};
+
+template <bool GATEUP, bool MX8, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB0,
+                       const __grid_constant__ CUtensorMap tmB1, const TmParams P)
+{
+    using C = TmCfg<GATEUP, MX8, STAGES>;
+    const GemmArgs &p = P.a;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base_u32 - raw_u32);
+    // stage s: [token codes | weight codes (2 tiles) | token atoms | tile-0 atoms | tile-1 atoms]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::N_BARS);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *s_off = reinterpret_cast<int *>(tmem_slot + 4);
+    int *s_cs = s_off + (kMaxExperts + 1);
+
+    const uint32_t bar_u32 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar_u32 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_u32 + 8u * (STAGES + s); };
+    const uint32_t tfull_bar = bar_u32 + 8u * (2 * STAGES);
+    const uint32_t tempty_bar = bar_u32 + 8u * (2 * STAGES + 1);
+    const uint32_t drain_bar = bar_u32 + 8u * (2 * STAGES + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E;
+    const int KB = P.kblocks;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(tfull_bar, 1);
+        mbar_init(tempty_bar, 128 * kEpiWG);
+        mbar_init(drain_bar, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB0);
+        if (GATEUP)
+            tma_prefetch_desc(&tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    for (int i = threadIdx.x; i <= E; i += kThreads) {
+        s_off[i] = p.offsets[i];
+        s_cs[i] = p.chunk_start[i];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int n_tiles = p.m_tiles * s_cs[E];
+    const uint64_t tmo = p.timeout_ns;
+
+    // weight tiles (128 rows) of work unit m: gate/up m in both maps, down 2m, 2m+1
+    auto wtile0 = [&](const Tile &tl) { return tl.e * P.n_tiles_w + (GATEUP ? tl.m : 2 * tl.m); };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------- producer: codes by TMA, scales by bulk copy
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, armed_par = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                const Tile tl = decode_tile(t, s_off, s_cs, E, p.m_tiles);
+                const int w0 = wtile0(tl);
+                const int w1 = GATEUP ? w0 : w0 + 1;
+                const uint8_t *sfb0 = P.f.sf0 + (size_t)w0 * KB * kAtom;
+                const uint8_t *sfb1 = (GATEUP ? P.f.sf1 : P.f.sf0) + (size_t)w1 * KB * kAtom;
+                int j0;
+                const int chunk =
+                    s_cs[tl.e] + nvfp4_chunk_of_row(tl.row0 - s_off[tl.e], s_off[tl.e + 1] - s_off[tl.e],
+                                                    s_cs[tl.e + 1] - s_cs[tl.e], &j0);
+                const uint8_t *sfa = P.f.act_sf + (size_t)chunk * KB * kAtom;
+                for (int k = 0; k < p.ksteps; ++k) {
+                    const int nkb = MX8 ? 1 : min(4, KB - 4 * k);
+                    const int atom0 = MX8 ? k : 4 * k;
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, tmo, s_abort, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(stage),
+                                          (uint32_t)(C::A_BYTES + C::B_BYTES + 3 * nkb * kAtom));
+                    armed |= 1u << stage;
+                    armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+                    const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
+                    const uint32_t sb = st + C::A_BYTES;
+                    const uint32_t sf = sb + C::B_BYTES;
+                    tma_load_2d(st, &tmA, k * kRowBytes, tl.row0, full_bar(stage));
+                    tma_load_2d(sb, &tmB0, k * kRowBytes, w0 * kBlockM, full_bar(stage));
+                    tma_load_2d(sb + 128 * kRowBytes, GATEUP ? &tmB1 : &tmB0, k * kRowBytes,
+                                w1 * kBlockM, full_bar(stage));
+                    bulk_g2s(sf, sfa + (size_t)atom0 * kAtom, nkb * kAtom, full_bar(stage));
+                    bulk_g2s(sf + C::SF_OP, sfb0 + (size_t)atom0 * kAtom, nkb * kAtom,
+                             full_bar(stage));
+                    bulk_g2s(sf + 2 * C::SF_OP, sfb1 + (size_t)atom0 * kAtom, nkb * kAtom,
+                             full_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok)
+                for (int s = 0; s < STAGES; ++s)
+                    if ((armed >> s) & 1u)
+                        mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, tmo);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // --------------------------------------------- MMA issuer
+            const uint32_t idesc = MX8 ? idesc_mx8(kBlockM, 256) : idesc_nvf4(kBlockM, 256);
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                if (!mbar_wait_bounded(tempty_bar, acc_phase ^ 1u, tmo, s_abort, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base;
+                for (int k = 0; k < p.ksteps; ++k) {
+                    const int nkb = MX8 ? 1 : min(4, KB - 4 * k);
+                    if (!mbar_wait_bounded(full_bar(stage), phase, tmo, s_abort, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
+                    const uint32_t sb = st + C::A_BYTES;
+                    const uint32_t sf = sb + C::B_BYTES;
+                    const uint32_t ta = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
+                    const uint32_t tb = ta + C::SFA_COLS;
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        tmem_cp_atom(ta + 4 * kb, sf + kb * kAtom);
+                        tmem_cp_atom(tb + 8 * kb, sf + C::SF_OP + kb * kAtom);
+                        tmem_cp_atom(tb + 8 * kb + 4, sf + 2 * C::SF_OP + kb * kAtom);
+                    }
+                    if constexpr (MX8) {
+                        // four K = 32 MMAs pick byte kk of the one atom per operand
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t id = idesc | ((uint32_t)kk << 29) | ((uint32_t)kk << 4);
+                            mma_mx8(d, smem_desc_k128(st + kk * 32), smem_desc_k128(sb + kk * 32),
+                                    id, ta, tb, (k | kk) != 0);
+                        }
+                    } else {
+                        for (int kb = 0; kb < nkb; ++kb)
+                            mma_nvf4(d, smem_desc_k128(st + kb * 32), smem_desc_k128(sb + kb * 32),
+                                     idesc, ta + 4 * kb, tb + 8 * kb, (k | kb) != 0);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                mma_commit(tfull_bar);
+                acc_phase ^= 1u;
+            }
+            if (!ok) {
+                mma_commit(drain_bar);
+                mbar_wait_drain(drain_bar, 0, tmo);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- epilogue
+        const int q = warp & 3;               // TMEM lane quarter of this warp
+        const int j = q * 32 + lane;          // token row in the tile
+        const int wg = (warp - 2) >> 2;       // feature half
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+            const Tile tl = decode_tile(t, s_off, s_cs, E, p.m_tiles);
+            if (!mbar_wait_bounded(tfull_bar, acc_phase, tmo, s_abort, p.status))
+                break;
+            tc_fence_after();
+            const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16);
+            const int row = tl.row0 + j;
+            const bool live = j < tl.nrows;
+            if constexpr (GATEUP) {
+                // g: columns 64wg.. (gate rows of the weight tile), u: 128 + 64wg..
+                uint32_t g[4][16], u[4][16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld16(ta + 64 * wg + 16 * c, g[c]);
+                    tmem_ld16(ta + 128 + 64 * wg + 16 * c, u[c]);
+                }
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(tempty_bar);
+                const float g0 = MX8 ? 1.0f : P.f.gs0[tl.e];
+                const float g1 = MX8 ? 1.0f : P.f.gs1[tl.e];
+                float h[4][16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        h[c][i] = silu_mul_f(__fmul_rn(__uint_as_float(g[c][i]), g0),
+                                             __fmul_rn(__uint_as_float(u[c][i]), g1));
+                if (live) {
+                    const int I = p.out_ld;  // h elements per row
+                    const int ps = P.row_pos[row];
+                    const int jc = ps & 255;
+                    uint8_t *hq = static_cast<uint8_t *>(p.out);
+                    if constexpr (MX8) {
+                        // two 32-blocks: features 64wg + 32b ..
+                        uint32_t sc = 0;
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            float amax = 0.0f;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                amax = fmaxf(amax, fabsf(h[2 * b + i / 16][i % 16]));
+                            const int e = mx_shared_exp(amax);
+                            uint32_t w[8];
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                uint32_t x = 0;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    x |= mx_code(h[2 * b + (4 * v + i) / 16][(4 * v + i) % 16], e)
+                                         << (8 * i);
+                                w[v] = x;
+                            }
+                            uint4 *dst = reinterpret_cast<uint4 *>(
+                                hq + (size_t)row * I + tl.m * 128 + 64 * wg + 32 * b);
+                            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                            sc |= (uint32_t)(e + 127) << (8 * b);
+                        }
+                        // atom of (chunk, 128-block m): bytes 2wg, 2wg+1 of the row's word
+                        *reinterpret_cast<uint16_t *>(
+                            P.h_sf + ((size_t)(ps >> 8) * (I / 128) + tl.m) * kAtom +
+                            nvfp4_atom_offset(jc) + 2 * wg) = (uint16_t)sc;
+                    } else {
+                        // four 16-blocks = the 64-block 2m + wg
+                        uint32_t lo[4], hi[4], word = 0;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            word |= nvfp4_quant16(h[c], &lo[c], &hi[c]) << (8 * c);
+                        uint4 *dst = reinterpret_cast<uint4 *>(hq + (size_t)row * (I / 2) +
+                                                               tl.m * 64 + 32 * wg);
+                        dst[0] = make_uint4(lo[0], hi[0], lo[1], hi[1]);
+                        dst[1] = make_uint4(lo[2], hi[2], lo[3], hi[3]);
+                        // replicated 256-row image of (chunk, 64-block)
+                        uint8_t *img = P.h_sf +
+                                       ((size_t)(ps >> 8) * (I / 64) + 2 * tl.m + wg) * 4096 +
+                                       2048 * (jc >> 7) + nvfp4_atom_offset(jc & 127);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            *reinterpret_cast<uint32_t *>(img + 512 * r) = word;
+                    }
+                }
+            } else {
+                // y columns 128wg .. 128wg + 127 of the 256-feature tile
+                uint32_t v[8][16];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    tmem_ld16(ta + 128 * wg + 16 * c, v[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(tempty_bar);
+                if (live) {
+                    const float g0 = MX8 ? 1.0f : P.f.gs0[tl.e];
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                                           (size_t)row * p.out_ld + tl.m * 256 +
+                                                           128 * wg);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            w[i] = pack_bf16x2(__fmul_rn(__uint_as_float(v[c][2 * i]), g0),
+                                               __fmul_rn(__uint_as_float(v[c][2 * i + 1]), g0));
+                        dst[2 * c] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[2 * c + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                }
+            }
+            acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <bool GATEUP, bool MX8, int STAGES>
+cudaError_t launch_tm(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                      const TmParams &P, int grid, int stage, cudaStream_t s)
+{
+    using C = TmCfg<GATEUP, MX8, STAGES>;
+    auto kern = grouped_gemm_tm_kernel<GATEUP, MX8, STAGES>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess)
+        return attr_err;
+    stage_begin(stage, s);
+    kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a, b0, b1, P);
+    stage_end(stage, s);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gateup_tm(bool mx8, const CUtensorMap &wg, const CUtensorMap &wu,
+                             const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
+                             int kblocks, uint8_t *h_sf, const int32_t *row_pos, int grid,
+                             cudaStream_t s)
+{
+    TmParams P;
+    P.a = a;
+    P.a.ksteps = mx8 ? kblocks : (kblocks + 3) / 4;
+    P.f = f;
+    P.kblocks = kblocks;
+    P.n_tiles_w = a.m_tiles;
+    P.h_sf = h_sf;
+    P.row_pos = row_pos;
+    if (mx8)
+        return launch_tm<true, true, 4>(xq, wg, wu, P, grid, kStGateUp, s);
+    return launch_tm<true, false, 4>(xq, wg, wu, P, grid, kStGateUp, s);
+}
+
+cudaError_t launch_down_tm_mx8(const CUtensorMap &wd, const CUtensorMap &hq, const GemmArgs &a,
+                               const Fp4Weights &f, int kblocks, int grid, cudaStream_t s)
+{
+    if (a.m_tiles % 2)
+        return cudaErrorInvalidValue;
+    TmParams P;
+    P.a = a;
+    P.a.m_tiles = a.m_tiles / 2;  // 256-feature tiles
+    P.a.ksteps = kblocks;
+    P.f = f;
+    P.kblocks = kblocks;
+    P.n_tiles_w = a.m_tiles;
+    P.h_sf = nullptr;
+    P.row_pos = nullptr;
+    return launch_tm<false, true, 4>(hq, wd, wd, P, grid, kStDown, s);
+}
+
+}  // namespace beam

@@ -101,7 +101,8 @@ struct GemmArgs {
     int E;
     int m_tiles;    // weight rows per expert / 128
     int ksteps;     // reduction length / 64
-    void *out;      // gate/up: h bf16 [R, ld] (NVFP4: FP32); down: y bf16 [R, ld]
+    void *out;      // gate/up: h bf16 [R, ld] (NVFP4 / MXFP8: FP32, or codes from the
+                    // token-major kernel); down: y bf16 [R, ld]
     int out_ld;
     int *status;
     unsigned long long timeout_ns;
@@ -147,8 +148,9 @@ cudaError_t launch_down_pair(const CUtensorMap &wd, const CUtensorMap &hp, const
 
 // ---- grouped_gemm_fp4.cu: the same GEMMs in NVFP4 on the FP4 tensor cores
 // (E2M1 codes of weights and activations via 128-byte TMA rows, block
-// scales via bulk copies); gate/up writes h in FP32 for launch_quantize_rows.
-// kblocks = K/64.  Gate/up token chunks are fp4_chunk_rows(v) rows at most,
+// scales via bulk copies).  Gate/up here is the decode-size kernel only
+// (prefill-size batches: launch_gateup_tm); it writes h in FP32 for
+// launch_quantize_rows.  kblocks = K/64.  Gate/up token chunks are fp4_chunk_rows(v) rows at most,
 // down chunks fp4_down_chunk_rows(v); the activation maps use
 // fp4_box_rows(v)-row boxes.  fp4_down_rep(v): the down GEMM takes h's
 // scales in the replicated 256-row layout (launch_quantize_rows rep_layout).
@@ -159,13 +161,28 @@ int fp4_box_rows(GemmVariant v);
 // MXFP8 experts on the same kernels (kind::mxf8f6f4): E4M3 codes, one
 // UE8M0 scale per 32 elements, scale atoms [.., K/128, 512]; kblocks = K/128;
 // chunks of fp4_chunk_rows(v) rows for both GEMMs, activation scales in
-// atoms; gate/up writes h in FP32 for launch_quantize_rows_mx8.
+// atoms.  Gate/up: decode size only, writing h in FP32 for
+// launch_quantize_rows_mx8; down: any size (prefill-size batches with an
+// even H/128 use launch_down_tm_mx8).
 cudaError_t launch_gateup_mx8(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
                               const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
                               int kblocks, int grid, cudaStream_t s);
 cudaError_t launch_down_mx8(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hq,
                             const GemmArgs &a, const Fp4Weights &f, int kblocks, int grid,
                             cudaStream_t s);
+// ---- grouped_gemm_tm.cu: token-major prefill-size GEMMs (tokens the
+// M = 128 operand, 256 weight rows the N operand).  Gate/up (NVFP4 or MXFP8,
+// chunks of fp4_chunk_rows(kPrefill) rows, 128-row token boxes) writes h
+// already quantised: codes [R, I] (NVFP4 two per byte) and scales at
+// row_pos in the down GEMM's layout (NVFP4: replicated 256-row images;
+// MXFP8: atoms).  a.out = h codes, a.out_ld = I, a.m_tiles = I/128.
+// Down (MXFP8, a.m_tiles = H/128 even) writes y bf16 [R, H].
+cudaError_t launch_gateup_tm(bool mx8, const CUtensorMap &wg, const CUtensorMap &wu,
+                             const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
+                             int kblocks, uint8_t *h_sf, const int32_t *row_pos, int grid,
+                             cudaStream_t s);
+cudaError_t launch_down_tm_mx8(const CUtensorMap &wd, const CUtensorMap &hq, const GemmArgs &a,
+                               const Fp4Weights &f, int kblocks, int grid, cudaStream_t s);
 cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
                               const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
                               int kblocks, int grid, cudaStream_t s);

@@ -1,7 +1,7 @@
 """MXFP8 experts on the GPU (kind::mxf8f6f4 tensor cores) against the oracle:
 the weight quantiser bit for bit, the layer on every token at small shapes
 (decode and prefill kernel shapes, ragged tails, several weight tiles) and
-sampled tokens at the decode size."""
+sampled tokens at the decode and prefill sizes."""
 import numpy as np
 import pytest
 import torch
@@ -65,6 +65,9 @@ SMALL = {
     "tiny": synth.shape("tiny"),
     "tiny_T200": synth.shape("tiny", T=200),
     "medium": synth.LayerShape(T=1501, H=512, I=384, E=64, G=8, topk_groups=4, top_k=8),
+    # H/128 odd and K = H not a multiple of 256: a short last NVFP4 k-step in
+    # the token-major gate/up, the weight-major MXFP8 down GEMM
+    "odd_tiles": synth.LayerShape(T=3001, H=640, I=256, E=32, G=8, topk_groups=4, top_k=8),
 }
 
 
@@ -93,8 +96,9 @@ def test_mxfp8_deterministic():
 
 
 @pytest.mark.slow
-def test_mxfp8_decode_full_size_sampled(oracle_mod):
-    sh = synth.shape("decode")
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_mxfp8_full_size_sampled(oracle_mod, name):
+    sh = synth.shape(name)
     d = synth.make_inputs(sh, seed=0, device="cuda")
     layer = _layer(sh, d)
     out = layer.forward(d["x"])

@@ -72,6 +72,9 @@ SMALL = {
     "tiny": synth.shape("tiny"),
     "tiny_T200": synth.shape("tiny", T=200),
     "medium": synth.LayerShape(T=1501, H=512, I=384, E=64, G=8, topk_groups=4, top_k=8),
+    # H/128 odd and K = H not a multiple of 256: a short last NVFP4 k-step in
+    # the token-major gate/up, the weight-major MXFP8 down GEMM
+    "odd_tiles": synth.LayerShape(T=3001, H=640, I=256, E=32, G=8, topk_groups=4, top_k=8),
 }
 
 
