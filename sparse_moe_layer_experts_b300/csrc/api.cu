@@ -383,14 +383,17 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
         Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, nullptr, nullptr,
                      at<uint8_t>(ws, L.h_sf)};
         if (tm && (H / 128) % 2 == 0)
-            BEAM_CUDA(launch_down_tm_mx8(m_wd, m_h, a, f, I / 128, sms, s));
+            BEAM_CUDA(launch_down_tm(true, m_wd, m_h, a, f, I / 128, sms, s));
         else
             BEAM_CUDA(launch_down_mx8(v, m_wd, m_h, a, f, I / 128, sms, s));
     } else if (fp4) {
         Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, c.w_down_gs, nullptr,
                      at<uint8_t>(ws, L.h_sf)};
         a.chunk_start = at<int32_t>(ws, L.chunk_start2);  // the down GEMM's own chunking
-        BEAM_CUDA(launch_down_fp4(v, m_wd, m_h, a, f, I / 64, sms, s));
+        if (tm && (H / 128) % 2 == 0)
+            BEAM_CUDA(launch_down_tm(false, m_wd, m_h, a, f, I / 64, sms, s));
+        else
+            BEAM_CUDA(launch_down_fp4(v, m_wd, m_h, a, f, I / 64, sms, s));
     } else {
         BEAM_CUDA(launch_down(v, m_wd, m_h, a, sms, s));
     }

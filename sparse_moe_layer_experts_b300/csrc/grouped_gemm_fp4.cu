@@ -438,12 +438,13 @@ int fp4_chunk_rows(GemmVariant v)
 
 int fp4_down_chunk_rows(GemmVariant v)
 {
-    return v == GemmVariant::kDecode ? 32 : 256;
+    return v == GemmVariant::kDecode ? 32 : 128;
 }
 
 bool fp4_down_rep(GemmVariant v)
 {
-    return v != GemmVariant::kDecode;
+    (void)v;
+    return false;
 }
 
 int fp4_box_rows(GemmVariant v)
@@ -469,8 +470,9 @@ cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensor
     if (v == GemmVariant::kDecode)
         return launch_nvf4_variant<false, 32, 9, 2, 16, 1>(wd, wd, hq, a, f, kblocks, grid, kStDown,
                                                            s);
-    return launch_nvf4_variant<false, 256, 3, 1, 128, 2, true>(wd, wd, hq, a, f, kblocks, grid,
-                                                               kStDown, s);
+    // prefill size with an odd H/128 (even H/128 runs token-major)
+    return launch_nvf4_variant<false, 128, 6, 2, 128, 2>(wd, wd, hq, a, f, kblocks, grid, kStDown,
+                                                         s);
 }
 
 cudaError_t launch_gateup_mx8(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,

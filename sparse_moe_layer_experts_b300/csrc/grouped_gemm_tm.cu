@@ -16,9 +16,9 @@
 // consecutive features, i.e. whole quantisation blocks of h: it computes
 // h = silu(g) * u in FP32 and quantises h itself (NVFP4: 16-blocks with E4M3
 // scales; MXFP8: 32-blocks with power-of-two scales), writing the codes and
-// the token-chunk scale layout the down GEMM reads.  No FP32 h goes to
-// memory.  Down (MXFP8): the N operand is weight tiles 2m and 2m+1 (256
-// output features); the epilogue writes bf16 y rows.
+// the token-chunk scale atoms the down GEMM reads.  No FP32 h goes to
+// memory.  Down: the N operand is weight tiles 2m and 2m+1 (256 output
+// features); the epilogue writes bf16 y rows.
 //
 // Scales: the token chunk's atom per 64-block (NVFP4) or per 128-deep k-step
 // (MXFP8) goes to tensor memory as the A scales; the two weight tiles'
@@ -26,10 +26,18 @@
 // 128-255 of an N = 256 operand).  Every B scale address is a multiple of 8
 // columns, every A scale address a multiple of 4.
 //
+// Scale staging: with SFST, a fourth warpgroup reads each stage's atoms from
+// shared memory and writes them into tensor memory with tcgen05.st (each
+// warp its lane quarter: lane 32q + i, columns c..c+3 = words 0-3 of atom
+// row i, the layout a 32x128b.warpx4 copy produces), then signals the MMA
+// thread; the tensor pipe then runs only MMAs.  Without SFST the MMA thread
+// copies the atoms with tcgen05.cp.
+//
 // Warp roles: warp 0 TMA / bulk-copy producer, warp 1 TMEM allocator and MMA
-// issuer, two epilogue warpgroups (features split in halves).  One
-// accumulator: the epilogue loads its 128 values into registers and releases
-// the accumulator before the arithmetic and the stores.  Waits are bounded.
+// issuer, two epilogue warpgroups (features split in halves), and with SFST
+// the scale warpgroup (warps 12-15; warps 2-3 idle).  One accumulator: the
+// epilogue drains it into registers in two halves, computing between the
+// loads, and releases it before quantising and storing.  Waits are bounded.
 #include "blockscaled.cuh"
 #include "common.cuh"
 #include "gemm_common.cuh"
@@ -47,10 +55,12 @@ constexpr int kRowBytes = 128;  // one 128-byte swizzle row of codes per k-step
 constexpr int kAtom = 512;
 constexpr int kMaxExperts = 256;
 constexpr int kEpiWG = 2;
-constexpr int kThreads = 64 + 128 * kEpiWG;
 
-template <bool GATEUP, bool MX8, int STAGES>
+template <bool GATEUP, bool MX8, int STAGES, bool SFST>
 struct TmCfg {
+    static constexpr int THREADS = SFST ? 512 : 64 + 128 * kEpiWG;
+    static constexpr int EPI_W0 = SFST ? 4 : 2;  // first epilogue warp
+    static constexpr int SF_W0 = 12;             // first scale warp (SFST)
     static constexpr int A_BYTES = kBlockM * kRowBytes;  // token codes
     static constexpr int B_BYTES = 256 * kRowBytes;      // two weight tiles
     static constexpr int ATOMS = MX8 ? 1 : 4;            // scale atoms per operand and k-step
@@ -65,7 +75,7 @@ struct TmCfg {
     static constexpr int SF_COL0 = ACC_COLS;
     static constexpr int COLS_NEED = SF_COL0 + STAGES * SF_COLS;
     static constexpr int TMEM_COLS = COLS_NEED <= 256 ? 256 : 512;
-    static constexpr int N_BARS = 2 * STAGES + 3;
+    static constexpr int N_BARS = 3 * STAGES + 3;
     static constexpr int AUX_BYTES = N_BARS * 8 + 16 + 2 * (kMaxExperts + 1) * 4;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + ((AUX_BYTES + 127) / 128) * 128;
     static_assert(SF_COL0 % 8 == 0 && SF_COLS % 8 == 0 && SFA_COLS % 8 == 0,
@@ -80,17 +90,17 @@ struct TmParams {
     Fp4Weights f;    // sf0 / sf1 weight atoms, gs0 / gs1 (NVFP4), act_sf token atoms
     int kblocks;     // scale atoms per operand row tile: K/64 (NVFP4), K/128 (MXFP8)
     int n_tiles_w;   // 128-row weight tiles per expert in sf0 / the B maps
-    uint8_t *h_sf;   // gate/up: scales of h (NVFP4: replicated 256-row images; MXFP8: atoms)
+    uint8_t *h_sf;   // gate/up: scale atoms of h [chunk, I/64 (NVFP4) or I/128 (MXFP8), 512]
     const int32_t *row_pos;  // gate/up: row -> chunk * 256 + position (down GEMM's chunking)
 };
 
-template <bool GATEUP, bool MX8, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool GATEUP, bool MX8, int STAGES, bool SFST>
+__global__ void __launch_bounds__(TmCfg<GATEUP, MX8, STAGES, SFST>::THREADS, 1)
 grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1, const TmParams P)
 {
-    using C = TmCfg<GATEUP, MX8, STAGES>;
+    using C = TmCfg<GATEUP, MX8, STAGES, SFST>;
     const GemmArgs &p = P.a;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -106,9 +116,10 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint32_t bar_u32 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar_u32 + 8u * s; };
     auto empty_bar = [&](int s) { return bar_u32 + 8u * (STAGES + s); };
-    const uint32_t tfull_bar = bar_u32 + 8u * (2 * STAGES);
-    const uint32_t tempty_bar = bar_u32 + 8u * (2 * STAGES + 1);
-    const uint32_t drain_bar = bar_u32 + 8u * (2 * STAGES + 2);
+    auto sfready_bar = [&](int s) { return bar_u32 + 8u * (2 * STAGES + s); };
+    const uint32_t tfull_bar = bar_u32 + 8u * (3 * STAGES);
+    const uint32_t tempty_bar = bar_u32 + 8u * (3 * STAGES + 1);
+    const uint32_t drain_bar = bar_u32 + 8u * (3 * STAGES + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
@@ -118,6 +129,7 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
+            mbar_init(sfready_bar(s), 4);  // one arrive per scale warp
         }
         mbar_init(tfull_bar, 1);
         mbar_init(tempty_bar, 128 * kEpiWG);
@@ -135,7 +147,7 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
-    for (int i = threadIdx.x; i <= E; i += kThreads) {
+    for (int i = threadIdx.x; i <= E; i += C::THREADS) {
         s_off[i] = p.offsets[i];
         s_cs[i] = p.chunk_start[i];
     }
@@ -217,7 +229,10 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
                 const uint32_t d = tmem_base;
                 for (int k = 0; k < p.ksteps; ++k) {
                     const int nkb = MX8 ? 1 : min(4, KB - 4 * k);
-                    if (!mbar_wait_bounded(full_bar(stage), phase, tmo, s_abort, p.status)) {
+                    // operands in shared memory, and (SFST) the scales in tensor memory
+                    if (!mbar_wait_bounded(full_bar(stage), phase, tmo, s_abort, p.status) ||
+                        (SFST &&
+                         !mbar_wait_bounded(sfready_bar(stage), phase, tmo, s_abort, p.status))) {
                         ok = false;
                         break;
                     }
@@ -227,10 +242,12 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const uint32_t sf = sb + C::B_BYTES;
                     const uint32_t ta = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
                     const uint32_t tb = ta + C::SFA_COLS;
-                    for (int kb = 0; kb < nkb; ++kb) {
-                        tmem_cp_atom(ta + 4 * kb, sf + kb * kAtom);
-                        tmem_cp_atom(tb + 8 * kb, sf + C::SF_OP + kb * kAtom);
-                        tmem_cp_atom(tb + 8 * kb + 4, sf + 2 * C::SF_OP + kb * kAtom);
+                    if constexpr (!SFST) {
+                        for (int kb = 0; kb < nkb; ++kb) {
+                            tmem_cp_atom(ta + 4 * kb, sf + kb * kAtom);
+                            tmem_cp_atom(tb + 8 * kb, sf + C::SF_OP + kb * kAtom);
+                            tmem_cp_atom(tb + 8 * kb + 4, sf + 2 * C::SF_OP + kb * kAtom);
+                        }
                     }
                     if constexpr (MX8) {
                         // four K = 32 MMAs pick byte kk of the one atom per operand
@@ -262,14 +279,16 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp >= C::EPI_W0 && warp < C::EPI_W0 + 4 * kEpiWG) {
         // ------------------------------------------------- epilogue
-        const int q = warp & 3;               // TMEM lane quarter of this warp
-        const int j = q * 32 + lane;          // token row in the tile
-        const int wg = (warp - 2) >> 2;       // feature half
+        const int q = warp & 3;                   // TMEM lane quarter of this warp
+        const int j = q * 32 + lane;              // token row in the tile
+        const int wg = (warp - C::EPI_W0) >> 2;  // feature half
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
             const Tile tl = decode_tile(t, s_off, s_cs, E, p.m_tiles);
+            const float g0 = MX8 ? 1.0f : P.f.gs0[tl.e];
+            const float g1 = (MX8 || !GATEUP) ? 1.0f : P.f.gs1[tl.e];
             if (!mbar_wait_bounded(tfull_bar, acc_phase, tmo, s_abort, p.status))
                 break;
             tc_fence_after();
@@ -277,39 +296,41 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
             const int row = tl.row0 + j;
             const bool live = j < tl.nrows;
             if constexpr (GATEUP) {
-                // g: columns 64wg.. (gate rows of the weight tile), u: 128 + 64wg..
-                uint32_t g[4][16], u[4][16];
+                // features 64wg + 32c + i: g in column 64wg + 32c + i, u 128 further.
+                // Two halves: h of the first is computed before the second is
+                // loaded; the accumulator is released after the second load.
+                float h[2][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld16(ta + 64 * wg + 16 * c, g[c]);
-                    tmem_ld16(ta + 128 + 64 * wg + 16 * c, u[c]);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t g[2][16], u[2][16];
+                    tmem_ld16(ta + 64 * wg + 32 * c, g[0]);
+                    tmem_ld16(ta + 64 * wg + 32 * c + 16, g[1]);
+                    tmem_ld16(ta + 128 + 64 * wg + 32 * c, u[0]);
+                    tmem_ld16(ta + 128 + 64 * wg + 32 * c + 16, u[1]);
+                    tmem_ld_wait();
+                    if (c == 1) {
+                        tc_fence_before();
+                        mbar_arrive(tempty_bar);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        h[c][i] = silu_mul_f(__fmul_rn(__uint_as_float(g[i / 16][i % 16]), g0),
+                                             __fmul_rn(__uint_as_float(u[i / 16][i % 16]), g1));
                 }
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(tempty_bar);
-                const float g0 = MX8 ? 1.0f : P.f.gs0[tl.e];
-                const float g1 = MX8 ? 1.0f : P.f.gs1[tl.e];
-                float h[4][16];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        h[c][i] = silu_mul_f(__fmul_rn(__uint_as_float(g[c][i]), g0),
-                                             __fmul_rn(__uint_as_float(u[c][i]), g1));
                 if (live) {
                     const int I = p.out_ld;  // h elements per row
                     const int ps = P.row_pos[row];
                     const int jc = ps & 255;
                     uint8_t *hq = static_cast<uint8_t *>(p.out);
                     if constexpr (MX8) {
-                        // two 32-blocks: features 64wg + 32b ..
+                        // half c is the 32-block 2wg + c of the 128-block m
                         uint32_t sc = 0;
 #pragma unroll
-                        for (int b = 0; b < 2; ++b) {
+                        for (int c = 0; c < 2; ++c) {
                             float amax = 0.0f;
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
-                                amax = fmaxf(amax, fabsf(h[2 * b + i / 16][i % 16]));
+                                amax = fmaxf(amax, fabsf(h[c][i]));
                             const int e = mx_shared_exp(amax);
                             uint32_t w[8];
 #pragma unroll
@@ -317,15 +338,14 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
                                 uint32_t x = 0;
 #pragma unroll
                                 for (int i = 0; i < 4; ++i)
-                                    x |= mx_code(h[2 * b + (4 * v + i) / 16][(4 * v + i) % 16], e)
-                                         << (8 * i);
+                                    x |= mx_code(h[c][4 * v + i], e) << (8 * i);
                                 w[v] = x;
                             }
                             uint4 *dst = reinterpret_cast<uint4 *>(
-                                hq + (size_t)row * I + tl.m * 128 + 64 * wg + 32 * b);
+                                hq + (size_t)row * I + tl.m * 128 + 64 * wg + 32 * c);
                             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
                             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                            sc |= (uint32_t)(e + 127) << (8 * b);
+                            sc |= (uint32_t)(e + 127) << (8 * c);
                         }
                         // atom of (chunk, 128-block m): bytes 2wg, 2wg+1 of the row's word
                         *reinterpret_cast<uint16_t *>(
@@ -335,48 +355,122 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
                         // four 16-blocks = the 64-block 2m + wg
                         uint32_t lo[4], hi[4], word = 0;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            word |= nvfp4_quant16(h[c], &lo[c], &hi[c]) << (8 * c);
+                        for (int b = 0; b < 4; ++b) {
+                            float v[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v[i] = h[b / 2][16 * (b % 2) + i];
+                            word |= nvfp4_quant16(v, &lo[b], &hi[b]) << (8 * b);
+                        }
                         uint4 *dst = reinterpret_cast<uint4 *>(hq + (size_t)row * (I / 2) +
                                                                tl.m * 64 + 32 * wg);
                         dst[0] = make_uint4(lo[0], hi[0], lo[1], hi[1]);
                         dst[1] = make_uint4(lo[2], hi[2], lo[3], hi[3]);
-                        // replicated 256-row image of (chunk, 64-block)
-                        uint8_t *img = P.h_sf +
-                                       ((size_t)(ps >> 8) * (I / 64) + 2 * tl.m + wg) * 4096 +
-                                       2048 * (jc >> 7) + nvfp4_atom_offset(jc & 127);
-#pragma unroll
-                        for (int r = 0; r < 4; ++r)
-                            *reinterpret_cast<uint32_t *>(img + 512 * r) = word;
+                        // atom of (chunk, 64-block 2m + wg): the row's word
+                        *reinterpret_cast<uint32_t *>(
+                            P.h_sf + ((size_t)(ps >> 8) * (I / 64) + 2 * tl.m + wg) * kAtom +
+                            nvfp4_atom_offset(jc)) = word;
                     }
                 }
             } else {
-                // y columns 128wg .. 128wg + 127 of the 256-feature tile
-                uint32_t v[8][16];
+                // y columns 128wg .. 128wg + 127 of the 256-feature tile, in
+                // four loads of 32 packed to bf16 pairs; release after the last
+                uint32_t w[4][16];
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    tmem_ld16(ta + 128 * wg + 16 * c, v[c]);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(tempty_bar);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[2][16];
+                    tmem_ld16(ta + 128 * wg + 32 * c, v[0]);
+                    tmem_ld16(ta + 128 * wg + 32 * c + 16, v[1]);
+                    tmem_ld_wait();
+                    if (c == 3) {
+                        tc_fence_before();
+                        mbar_arrive(tempty_bar);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[c][i] = pack_bf16x2(
+                            __fmul_rn(__uint_as_float(v[(2 * i) / 16][(2 * i) % 16]), g0),
+                            __fmul_rn(__uint_as_float(v[(2 * i + 1) / 16][(2 * i + 1) % 16]), g0));
+                }
                 if (live) {
-                    const float g0 = MX8 ? 1.0f : P.f.gs0[tl.e];
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
                                                            (size_t)row * p.out_ld + tl.m * 256 +
                                                            128 * wg);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t w[8];
+                    for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            w[i] = pack_bf16x2(__fmul_rn(__uint_as_float(v[c][2 * i]), g0),
-                                               __fmul_rn(__uint_as_float(v[c][2 * i + 1]), g0));
-                        dst[2 * c] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dst[2 * c + 1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    }
+                        for (int v = 0; v < 4; ++v)
+                            dst[4 * c + v] = make_uint4(w[c][4 * v], w[c][4 * v + 1],
+                                                        w[c][4 * v + 2], w[c][4 * v + 3]);
                 }
             }
             acc_phase ^= 1u;
+        }
+    } else if (SFST && warp >= C::SF_W0) {
+        // --------------------------------------- scale staging (SFST)
+        // Each warp writes its lane quarter: lane 32q + i, column c + w =
+        // word w of row i of the atom placed at column c.
+        const int q = warp & 3;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            for (int k = 0; k < p.ksteps; ++k) {
+                if (!mbar_wait_bounded(full_bar(stage), phase, tmo, s_abort, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *sf = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+                const uint32_t ta =
+                    tmem_base + ((uint32_t)(q * 32) << 16) + C::SF_COL0 + stage * C::SF_COLS;
+                if constexpr (MX8) {
+                    // columns: token atom 0-3, (unused) 4-7, tile 0 8-11, tile 1 12-15
+                    const uint4 a = *reinterpret_cast<const uint4 *>(sf + 16 * lane);
+                    const uint4 b0 = *reinterpret_cast<const uint4 *>(sf + C::SF_OP + 16 * lane);
+                    const uint4 b1 =
+                        *reinterpret_cast<const uint4 *>(sf + 2 * C::SF_OP + 16 * lane);
+                    const uint32_t r[16] = {a.x,  a.y,  a.z,  a.w,  0u,   0u,   0u,   0u,
+                                            b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                    tmem_st16(ta, r);
+                } else {
+                    // columns: token atoms 4kb..4kb+3; weight atoms 16 + 8kb (tile 0)
+                    // and 20 + 8kb (tile 1)
+                    uint32_t r[3][16];
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) {
+                        const uint4 a = *reinterpret_cast<const uint4 *>(sf + kb * kAtom + 16 * lane);
+                        const uint4 b0 = *reinterpret_cast<const uint4 *>(sf + C::SF_OP +
+                                                                          kb * kAtom + 16 * lane);
+                        const uint4 b1 = *reinterpret_cast<const uint4 *>(sf + 2 * C::SF_OP +
+                                                                          kb * kAtom + 16 * lane);
+                        r[0][4 * kb] = a.x;
+                        r[0][4 * kb + 1] = a.y;
+                        r[0][4 * kb + 2] = a.z;
+                        r[0][4 * kb + 3] = a.w;
+                        const int x = 8 * kb;  // column 16 + x of the stage = r[1 + x/16][x%16]
+                        r[1 + x / 16][x % 16] = b0.x;
+                        r[1 + x / 16][x % 16 + 1] = b0.y;
+                        r[1 + x / 16][x % 16 + 2] = b0.z;
+                        r[1 + x / 16][x % 16 + 3] = b0.w;
+                        r[1 + x / 16][x % 16 + 4] = b1.x;
+                        r[1 + x / 16][x % 16 + 5] = b1.y;
+                        r[1 + x / 16][x % 16 + 6] = b1.z;
+                        r[1 + x / 16][x % 16 + 7] = b1.w;
+                    }
+                    tmem_st16(ta, r[0]);
+                    tmem_st16(ta + 16, r[1]);
+                    tmem_st16(ta + 32, r[2]);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(sfready_bar(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
         }
     }
 
@@ -388,12 +482,12 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
 }
 
-template <bool GATEUP, bool MX8, int STAGES>
+template <bool GATEUP, bool MX8, int STAGES, bool SFST>
 cudaError_t launch_tm(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
                       const TmParams &P, int grid, int stage, cudaStream_t s)
 {
-    using C = TmCfg<GATEUP, MX8, STAGES>;
-    auto kern = grouped_gemm_tm_kernel<GATEUP, MX8, STAGES>;
+    using C = TmCfg<GATEUP, MX8, STAGES, SFST>;
+    auto kern = grouped_gemm_tm_kernel<GATEUP, MX8, STAGES, SFST>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -403,7 +497,7 @@ cudaError_t launch_tm(const CUtensorMap &a, const CUtensorMap &b0, const CUtenso
     if (attr_err != cudaSuccess)
         return attr_err;
     stage_begin(stage, s);
-    kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a, b0, b1, P);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, b0, b1, P);
     stage_end(stage, s);
     return cudaGetLastError();
 }
@@ -423,26 +517,31 @@ cudaError_t launch_gateup_tm(bool mx8, const CUtensorMap &wg, const CUtensorMap 
     P.n_tiles_w = a.m_tiles;
     P.h_sf = h_sf;
     P.row_pos = row_pos;
+    // NVFP4 (12 scale atoms per k-step) stages its scales with tcgen05.st;
+    // MXFP8 (3 per k-step) copies them in the tensor pipe, which measured faster
     if (mx8)
-        return launch_tm<true, true, 4>(xq, wg, wu, P, grid, kStGateUp, s);
-    return launch_tm<true, false, 4>(xq, wg, wu, P, grid, kStGateUp, s);
+        return launch_tm<true, true, 4, false>(xq, wg, wu, P, grid, kStGateUp, s);
+    return launch_tm<true, false, 4, true>(xq, wg, wu, P, grid, kStGateUp, s);
 }
 
-cudaError_t launch_down_tm_mx8(const CUtensorMap &wd, const CUtensorMap &hq, const GemmArgs &a,
-                               const Fp4Weights &f, int kblocks, int grid, cudaStream_t s)
+cudaError_t launch_down_tm(bool mx8, const CUtensorMap &wd, const CUtensorMap &hq,
+                           const GemmArgs &a, const Fp4Weights &f, int kblocks, int grid,
+                           cudaStream_t s)
 {
     if (a.m_tiles % 2)
         return cudaErrorInvalidValue;
     TmParams P;
     P.a = a;
     P.a.m_tiles = a.m_tiles / 2;  // 256-feature tiles
-    P.a.ksteps = kblocks;
+    P.a.ksteps = mx8 ? kblocks : (kblocks + 3) / 4;
     P.f = f;
     P.kblocks = kblocks;
     P.n_tiles_w = a.m_tiles;
     P.h_sf = nullptr;
     P.row_pos = nullptr;
-    return launch_tm<false, true, 4>(hq, wd, wd, P, grid, kStDown, s);
+    if (mx8)
+        return launch_tm<false, true, 4, false>(hq, wd, wd, P, grid, kStDown, s);
+    return launch_tm<false, false, 4, true>(hq, wd, wd, P, grid, kStDown, s);
 }
 
 }  // namespace beam

@@ -173,16 +173,17 @@ cudaError_t launch_down_mx8(GemmVariant v, const CUtensorMap &wd, const CUtensor
 // ---- grouped_gemm_tm.cu: token-major prefill-size GEMMs (tokens the
 // M = 128 operand, 256 weight rows the N operand).  Gate/up (NVFP4 or MXFP8,
 // chunks of fp4_chunk_rows(kPrefill) rows, 128-row token boxes) writes h
-// already quantised: codes [R, I] (NVFP4 two per byte) and scales at
-// row_pos in the down GEMM's layout (NVFP4: replicated 256-row images;
-// MXFP8: atoms).  a.out = h codes, a.out_ld = I, a.m_tiles = I/128.
-// Down (MXFP8, a.m_tiles = H/128 even) writes y bf16 [R, H].
+// already quantised: codes [R, I] (NVFP4 two per byte) and scale atoms at
+// row_pos.  a.out = h codes, a.out_ld = I, a.m_tiles = I/128.  Down
+// (a.m_tiles = H/128 even; kblocks = I/64 NVFP4, I/128 MXFP8) writes y
+// bf16 [R, H].
 cudaError_t launch_gateup_tm(bool mx8, const CUtensorMap &wg, const CUtensorMap &wu,
                              const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
                              int kblocks, uint8_t *h_sf, const int32_t *row_pos, int grid,
                              cudaStream_t s);
-cudaError_t launch_down_tm_mx8(const CUtensorMap &wd, const CUtensorMap &hq, const GemmArgs &a,
-                               const Fp4Weights &f, int kblocks, int grid, cudaStream_t s);
+cudaError_t launch_down_tm(bool mx8, const CUtensorMap &wd, const CUtensorMap &hq,
+                           const GemmArgs &a, const Fp4Weights &f, int kblocks, int grid,
+                           cudaStream_t s);
 cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtensorMap &wu,
                               const CUtensorMap &xq, const GemmArgs &a, const Fp4Weights &f,
                               int kblocks, int grid, cudaStream_t s);
