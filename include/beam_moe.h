@@ -303,6 +303,23 @@ int beam_moe_quantize_mxfp8(const void *w, int64_t n_mat, int64_t rows,
                             void *stream);
 
 /*
+ * Activation quantisation: FP32 rows quantised with the rule the layer
+ * applies to x and h when wtype is NVFP4 or MXFP8 (global scale 1), for
+ * callers that want the layer's activation codes outside the layer.
+ *   NVFP4: codes [rows, cols/2] (two E2M1 codes per byte, even element in
+ *          the low nibble), sf [rows, cols/16] E4M3 bytes; cols % 16 == 0.
+ *          Per 16-block: sf = e4m3_rn_satfinite(amax/6), q = e2m1_rn_satfinite(v/sf)
+ *          (0 where sf == 0).
+ *   MXFP8: codes [rows, cols] E4M3 bytes, sf [rows, cols/32] scale bytes
+ *          E + 127; cols % 32 == 0.  The rule of beam_moe_quantize_mxfp8.
+ *   x [rows, cols] float32, device, 16-byte aligned; codes 16-byte aligned.
+ * Returns BEAM_MOE_ERR_INVALID_ARG for any other wtype or a bad size or
+ * pointer (nothing is launched then).  One kernel launch on `stream`.
+ */
+int beam_moe_quantize_act(int wtype, const float *x, int64_t rows,
+                          int64_t cols, void *codes, void *sf, void *stream);
+
+/*
  * Synchronise `stream`, read the device status word of cfg->workspace and
  * clear it.  Returns BEAM_MOE_OK, BEAM_MOE_ERR_TIMEOUT or BEAM_MOE_ERR_DEVICE
  * (or BEAM_MOE_ERR_CUDA if the synchronisation itself failed).

@@ -84,6 +84,8 @@ def lib():
         L.beam_moe_quantize_nvfp4.restype = ctypes.c_int
         L.beam_moe_quantize_mxfp8.argtypes = [vp, i64, i64, i64, vp, vp, vp]
         L.beam_moe_quantize_mxfp8.restype = ctypes.c_int
+        L.beam_moe_quantize_act.argtypes = [ctypes.c_int, vp, i64, i64, vp, vp, vp]
+        L.beam_moe_quantize_act.restype = ctypes.c_int
         L.beam_moe_read_status.argtypes = [cfgp, vp]
         L.beam_moe_read_status.restype = ctypes.c_int
         L.beam_moe_status_string.argtypes = [ctypes.c_int]
@@ -166,6 +168,10 @@ def beam_moe_quantize_nvfp4(w, n_mat, rows, cols, packed, block_sf, global_sf, s
 
 def beam_moe_quantize_mxfp8(w, n_mat, rows, cols, codes, block_sf, stream) -> int:
     return lib().beam_moe_quantize_mxfp8(w, n_mat, rows, cols, codes, block_sf, stream)
+
+
+def beam_moe_quantize_act(wtype, x, rows, cols, codes, sf, stream) -> int:
+    return lib().beam_moe_quantize_act(wtype, x, rows, cols, codes, sf, stream)
 
 
 def beam_moe_read_status(cfg: beam_moe_cfg, stream) -> int:

@@ -41,7 +41,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
     size_t status, scores, ids, wts, local_rank, cta_counts, cta_base, counts, offsets,
-        chunk_start, chunk_start2, row_of, row_src, x_perm, h, h_raw, y, row_pos, x_sf, h_sf,
+        chunk_start, row_of, row_src, x_perm, h, h_raw, y, row_pos, x_sf, h_sf,
         total;
 };
 
@@ -51,17 +51,12 @@ GemmVariant pick_variant(int64_t T, const beam_moe_cfg &c)
     return (T * c.top_k <= 16LL * c.n_experts) ? GemmVariant::kDecode : GemmVariant::kPrefill;
 }
 
-// Rows per token chunk (the N tile of the grouped GEMMs); NVFP4 layers
-// chunk the down GEMM's rows separately (chunk_rows2).
+// Rows per token chunk (the token tile of the grouped GEMMs; both GEMMs of
+// a layer use the same chunking).
 int chunk_rows(int64_t T, const beam_moe_cfg &c)
 {
     const GemmVariant v = pick_variant(T, c);
     return c.wtype != BEAM_MOE_W_BF16 ? fp4_chunk_rows(v) : gemm_chunk_rows(v);
-}
-
-int chunk_rows2(int64_t T, const beam_moe_cfg &c)
-{
-    return fp4_down_chunk_rows(pick_variant(T, c));
 }
 
 Layout make_layout(int64_t T, const beam_moe_cfg &c)
@@ -86,7 +81,6 @@ Layout make_layout(int64_t T, const beam_moe_cfg &c)
     L.counts = take(sizeof(int32_t) * E);
     L.offsets = take(sizeof(int32_t) * (E + 1));
     L.chunk_start = take(sizeof(int32_t) * (E + 1));
-    L.chunk_start2 = take(sizeof(int32_t) * (E + 1));
     L.row_of = take(sizeof(int32_t) * R);
     L.row_src = take(sizeof(int32_t) * R);
     const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4, mx8 = c.wtype == BEAM_MOE_W_MXFP8;
@@ -108,16 +102,14 @@ Layout make_layout(int64_t T, const beam_moe_cfg &c)
         L.total = o;
         return L;
     }
-    // NVFP4: each row's place in the down GEMM's chunking, and the
-    // activations' scales per token chunk: x in atoms [chunk, H/64, 512],
-    // h in atoms or in the replicated 256-row images [chunk2, I/64, 4096]
-    const int64_t cr = chunk_rows(T, c), cr2 = chunk_rows2(T, c);
+    // NVFP4: each row's place in the token chunking (chunk*256 + j), and the
+    // activations' scales per token chunk in atoms: x [chunk, H/64, 512],
+    // h [chunk, I/64, 512]
+    const int64_t cr = chunk_rows(T, c);
     const int64_t chunks = fp4 ? (R + cr - 1) / cr + E : 0;
-    const int64_t chunks2 = fp4 ? (R + cr2 - 1) / cr2 + E : 0;
-    const size_t h_unit = fp4_down_rep(pick_variant(T, c)) ? 4096 : 512;
     L.row_pos = take(fp4 ? 4 * R : 0);
     L.x_sf = take((size_t)chunks * (H / 64) * 512);
-    L.h_sf = take((size_t)chunks2 * (I / 64) * h_unit);
+    L.h_sf = take((size_t)chunks * (I / 64) * 512);
     L.total = o;
     return L;
 }
@@ -241,7 +233,7 @@ int device_sms()
 // Steps 1-6 plus histogram/scan into the workspace.
 int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cfg &c,
               const Layout &L, float *scores, int32_t *ids, float *wts, int rows_per_chunk,
-              int rows_per_chunk2, cudaStream_t s)
+              cudaStream_t s)
 {
     void *ws = c.workspace;
     int *status = at<int>(ws, L.status);
@@ -253,9 +245,8 @@ int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cf
     BEAM_CUDA(launch_hist(ids, (int)T, c.top_k, c.n_experts, at<int32_t>(ws, L.local_rank),
                           at<int32_t>(ws, L.cta_counts), status, s));
     BEAM_CUDA(launch_scan(at<int32_t>(ws, L.cta_counts), n_cta, c.n_experts, rows_per_chunk,
-                          rows_per_chunk2, at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.counts),
-                          at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start),
-                          rows_per_chunk2 > 0 ? at<int32_t>(ws, L.chunk_start2) : nullptr, s));
+                          at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.counts),
+                          at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start), s));
     return BEAM_MOE_OK;
 }
 
@@ -277,7 +268,7 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     const GemmVariant v = pick_variant(T, c);
     const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4, mx8 = c.wtype == BEAM_MOE_W_MXFP8;
     int rc = run_route(x, router_w, T, c, L, at<float>(ws, L.scores), at<int32_t>(ws, L.ids),
-                       at<float>(ws, L.wts), chunk_rows(T, c), fp4 ? chunk_rows2(T, c) : 0, s);
+                       at<float>(ws, L.wts), chunk_rows(T, c), s);
     if (rc != BEAM_MOE_OK)
         return rc;
     const int K = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
@@ -292,7 +283,7 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
         BEAM_CUDA(launch_permute_nvfp4(
             static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids), at<int32_t>(ws, L.local_rank),
             at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start),
-            at<int32_t>(ws, L.chunk_start2), (int)T, K, E, H, at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.row_src),
+            (int)T, K, E, H, at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.row_src),
             at<int32_t>(ws, L.row_pos), at<uint8_t>(ws, L.x_perm), at<uint8_t>(ws, L.x_sf), s));
     else
         BEAM_CUDA(launch_permute(static_cast<const uint16_t *>(x), at<int32_t>(ws, L.ids),
@@ -368,8 +359,7 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
         a.out = at<void>(ws, L.h_raw);
         BEAM_CUDA(launch_gateup_fp4(v, m_wg, m_wu, m_xp, a, f, H / 64, sms, s));
         BEAM_CUDA(launch_quantize_rows(at<float>(ws, L.h_raw), R, I, at<int32_t>(ws, L.row_pos),
-                                       fp4_down_rep(v), at<uint8_t>(ws, L.h),
-                                       at<uint8_t>(ws, L.h_sf), s));
+                                       at<uint8_t>(ws, L.h), at<uint8_t>(ws, L.h_sf), s));
     } else {
         BEAM_CUDA(launch_gateup(v, m_wg, m_wu, m_xp, a, sms, s));
     }
@@ -389,7 +379,6 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     } else if (fp4) {
         Fp4Weights f{static_cast<const uint8_t *>(c.w_down_sf), nullptr, c.w_down_gs, nullptr,
                      at<uint8_t>(ws, L.h_sf)};
-        a.chunk_start = at<int32_t>(ws, L.chunk_start2);  // the down GEMM's own chunking
         if (tm && (H / 128) % 2 == 0)
             BEAM_CUDA(launch_down_tm(false, m_wd, m_h, a, f, I / 64, sms, s));
         else
@@ -539,8 +528,7 @@ int beam_moe_route(const void *x, const float *router_w, int64_t T, const beam_m
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *ws = c.workspace;
     float *sc = scores ? scores : at<float>(ws, L.scores);
-    rc = run_route(x, router_w, T, c, L, sc, topk_ids, topk_w, chunk_rows(T, c), 0,
-                   s);
+    rc = run_route(x, router_w, T, c, L, sc, topk_ids, topk_w, chunk_rows(T, c), s);
     if (rc != BEAM_MOE_OK)
         return rc;
     const int E = c.n_experts;
@@ -652,6 +640,24 @@ int beam_moe_quantize_mxfp8(const void *w, int64_t n_mat, int64_t rows, int64_t 
     BEAM_CUDA(launch_quantize_mxfp8(static_cast<const uint16_t *>(w), n_mat, (int)rows, (int)cols,
                                     static_cast<uint8_t *>(codes), static_cast<uint8_t *>(block_sf),
                                     static_cast<cudaStream_t>(stream)));
+    return BEAM_MOE_OK;
+}
+
+int beam_moe_quantize_act(int wtype, const float *x, int64_t rows, int64_t cols, void *codes,
+                          void *sf, void *stream)
+{
+    if (wtype != BEAM_MOE_W_NVFP4 && wtype != BEAM_MOE_W_MXFP8)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    const bool mx8 = wtype == BEAM_MOE_W_MXFP8;
+    if (rows < 0 || cols <= 0 || cols % (mx8 ? 32 : 16) || cols > (1 << 24) ||
+        rows > (int64_t(1) << 31))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    if (rows == 0)
+        return BEAM_MOE_OK;
+    if (!x || !codes || !sf || !aligned16(x) || !aligned16(codes))
+        return BEAM_MOE_ERR_INVALID_ARG;
+    BEAM_CUDA(launch_quantize_act(mx8, x, rows, (int)cols, static_cast<uint8_t *>(codes),
+                                  static_cast<uint8_t *>(sf), static_cast<cudaStream_t>(stream)));
     return BEAM_MOE_OK;
 }
 

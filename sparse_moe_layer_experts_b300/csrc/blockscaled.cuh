@@ -38,17 +38,6 @@ __device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint32_t saddr)
                  : "memory");
 }
 
-// 128 rows x 256 bits into 8 TMEM columns: the two 2 KB halves of a 4 KB
-// image (128 rows x 16 bytes each) land in columns 0-3 and 4-7.
-__device__ __forceinline__ void tmem_cp_pair(uint32_t taddr, uint32_t saddr)
-{
-    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)(2048u >> 4) << 16;  // between the halves
-    d |= (uint64_t)(128u >> 4) << 32;   // between 8-row groups
-    d |= (uint64_t)1 << 46;
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
-}
-
 // Instruction descriptor: E2M1 x E2M1 (format 1 each), UE4M3 scales, both
 // K-major, FP32 accumulator.
 __device__ __forceinline__ uint32_t idesc_nvf4(uint32_t m, uint32_t n)

@@ -80,14 +80,11 @@ __device__ int block_exclusive_scan_256(int v, int *tmp, int *total)
     return incl - v;
 }
 
-// One CTA of 256 threads, thread e owns expert e.  chunk_start2 (optional)
-// is a second token chunking of the same segments, for a GEMM with another
-// N tile.
+// One CTA of 256 threads, thread e owns expert e.
 __global__ void __launch_bounds__(256)
 scan_kernel(const int32_t *__restrict__ cta_counts, int n_cta, int E, int chunk_rows,
-            int chunk_rows2, int32_t *__restrict__ cta_base, int32_t *__restrict__ counts,
-            int32_t *__restrict__ offsets, int32_t *__restrict__ chunk_start,
-            int32_t *__restrict__ chunk_start2)
+            int32_t *__restrict__ cta_base, int32_t *__restrict__ counts,
+            int32_t *__restrict__ offsets, int32_t *__restrict__ chunk_start)
 {
     __shared__ int tmp[256];
     const int e = threadIdx.x;
@@ -113,30 +110,20 @@ scan_kernel(const int32_t *__restrict__ cta_counts, int n_cta, int E, int chunk_
         chunk_start[e] = cs;
     if (e == 0)
         chunk_start[E] = total_chunks;
-    if (chunk_start2) {
-        const int nchunk2 = (e < E) ? (run + chunk_rows2 - 1) / chunk_rows2 : 0;
-        const int cs2 = block_exclusive_scan_256(nchunk2, tmp, &total_chunks);
-        if (e < E)
-            chunk_start2[e] = cs2;
-        if (e == 0)
-            chunk_start2[E] = total_chunks;
-    }
 }
 
 // CTA per token: place the token's K rows, then read the token's activations
 // once (16-byte vectors) and write them to all K rows.  With QUANT (NVFP4
 // layers) each 16-element block is quantised to NVFP4 (global scale 1) once:
 // its 8 code bytes go to every row, its E4M3 scale into the row's token-chunk
-// scale atom (chunks of <= 128 rows), and row_pos records the row's place in
-// the down GEMM's chunking (chunk * 256 + position) for the pass that
-// quantises h.
+// scale atom (chunks of <= 128 rows), and row_pos records the row's place
+// (chunk * 256 + position) for the kernels that quantise h.
 template <bool QUANT>
 __global__ void __launch_bounds__(256)
 permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
                const int32_t *__restrict__ local_rank, const int32_t *__restrict__ cta_base,
                const int32_t *__restrict__ offsets, const int32_t *__restrict__ chunk_start,
-               const int32_t *__restrict__ chunk_start2, int T, int K, int E, int H,
-               int32_t *__restrict__ row_of,
+               int T, int K, int E, int H, int32_t *__restrict__ row_of,
                int32_t *__restrict__ row_src, int32_t *__restrict__ row_pos,
                void *__restrict__ x_perm, uint8_t *__restrict__ x_sf)
 {
@@ -158,9 +145,7 @@ permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
             int j;
             const int c = nvfp4_chunk_of_row(rank, n, chunk_start[e + 1] - chunk_start[e], &j);
             pos[k] = (chunk_start[e] + c) * 128 + j;
-            // position in the down GEMM's chunking, for the pass that quantises h
-            const int c2 = nvfp4_chunk_of_row(rank, n, chunk_start2[e + 1] - chunk_start2[e], &j);
-            row_pos[row] = (chunk_start2[e] + c2) * 256 + j;
+            row_pos[row] = (chunk_start[e] + c) * 256 + j;
         }
     }
     __syncthreads();
@@ -212,14 +197,8 @@ permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ ids,
 
 // NVFP4 activation quantisation of an FP32 matrix [rows, cols] (global scale
 // 1): codes [rows, cols/2], and the scales at the row's row_pos
-// (chunk * 256 + j) in one of two token-chunk layouts:
-//   REP = false: atoms [chunk, cols/64, 512] (chunks of <= 128 rows)
-//   REP = true:  [chunk, cols/64, 4096] (chunks of <= 256 rows): per 64-block
-//                the atom of rows 0-127 and the atom of rows 128-255, each
-//                written 4 times in a row, the source image of one
-//                128-lane x 256-bit tensor-memory copy
-// One thread per 16-block.
-template <bool REP>
+// (chunk * 256 + j) in token-chunk atoms [chunk, cols/64, 512] (chunks of
+// <= 128 rows).  One thread per 16-block.
 __global__ void __launch_bounds__(256)
 quantize_rows_kernel(const float *__restrict__ in, int64_t n_blocks, int cols,
                      const int32_t *__restrict__ row_pos, uint8_t *__restrict__ codes,
@@ -249,15 +228,7 @@ quantize_rows_kernel(const float *__restrict__ in, int64_t n_blocks, int cols,
     if ((blk & 3) == 0) {
         const int ps = row_pos[b / bpr];
         const size_t unit = (size_t)(ps >> 8) * (cols / 64) + (blk >> 2);
-        const int j = ps & 255;
-        if constexpr (REP) {
-            uint8_t *img = sf + unit * 4096 + 2048 * (j >> 7) + nvfp4_atom_offset(j & 127);
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                *reinterpret_cast<uint32_t *>(img + 512 * r) = word;
-        } else {
-            *reinterpret_cast<uint32_t *>(sf + unit * 512 + nvfp4_atom_offset(j)) = word;
-        }
+        *reinterpret_cast<uint32_t *>(sf + unit * 512 + nvfp4_atom_offset(ps & 255)) = word;
     }
 }
 
@@ -330,13 +301,8 @@ __device__ __forceinline__ uint2 mx_quant8(const float (&v)[8], unsigned live, i
     amax = fmaxf(amax, __shfl_xor_sync(live, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(live, amax, 2));
     *e = mx_shared_exp(amax);
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        lo |= mx_code(v[i], *e) << (8 * i);
-        hi |= mx_code(v[4 + i], *e) << (8 * i);
-    }
-    return make_uint2(lo, hi);
+    const float inv = mx_inv_scale(*e);
+    return make_uint2(mx_code4(v, inv), mx_code4(v + 4, inv));
 }
 
 // CTA per token: place its K rows (as permute_kernel), then quantise x once
@@ -605,12 +571,12 @@ cudaError_t launch_hist(const int32_t *ids, int T, int K, int E, int32_t *local_
 }
 
 cudaError_t launch_scan(const int32_t *cta_counts, int n_cta, int E, int chunk_rows,
-                        int chunk_rows2, int32_t *cta_base, int32_t *counts, int32_t *offsets,
-                        int32_t *chunk_start, int32_t *chunk_start2, cudaStream_t s)
+                        int32_t *cta_base, int32_t *counts, int32_t *offsets,
+                        int32_t *chunk_start, cudaStream_t s)
 {
     stage_begin(kStScan, s);
-    scan_kernel<<<1, 256, 0, s>>>(cta_counts, n_cta, E, chunk_rows, chunk_rows2, cta_base, counts,
-                                  offsets, chunk_start, chunk_start2);
+    scan_kernel<<<1, 256, 0, s>>>(cta_counts, n_cta, E, chunk_rows, cta_base, counts, offsets,
+                                  chunk_start);
     stage_end(kStScan, s);
     return cudaGetLastError();
 }
@@ -621,22 +587,21 @@ cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t 
                            cudaStream_t s)
 {
     stage_begin(kStPermute, s);
-    permute_kernel<false><<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, nullptr, nullptr,
-                                            T, K, E, H, row_of, row_src, nullptr, x_perm, nullptr);
+    permute_kernel<false><<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, nullptr, T, K,
+                                            E, H, row_of, row_src, nullptr, x_perm, nullptr);
     stage_end(kStPermute, s);
     return cudaGetLastError();
 }
 
 cudaError_t launch_permute_nvfp4(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
                                  const int32_t *cta_base, const int32_t *offsets,
-                                 const int32_t *chunk_start, const int32_t *chunk_start2, int T,
-                                 int K, int E, int H, int32_t *row_of, int32_t *row_src,
-                                 int32_t *row_pos, uint8_t *x_codes, uint8_t *x_sf, cudaStream_t s)
+                                 const int32_t *chunk_start, int T, int K, int E, int H,
+                                 int32_t *row_of, int32_t *row_src, int32_t *row_pos,
+                                 uint8_t *x_codes, uint8_t *x_sf, cudaStream_t s)
 {
     stage_begin(kStPermute, s);
-    permute_kernel<true><<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, chunk_start,
-                                           chunk_start2, T, K, E, H, row_of, row_src, row_pos,
-                                           x_codes, x_sf);
+    permute_kernel<true><<<T, 256, 0, s>>>(x, ids, local_rank, cta_base, offsets, chunk_start, T,
+                                           K, E, H, row_of, row_src, row_pos, x_codes, x_sf);
     stage_end(kStPermute, s);
     return cudaGetLastError();
 }
@@ -654,15 +619,12 @@ cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int
 }
 
 cudaError_t launch_quantize_rows(const float *in, int64_t rows, int cols, const int32_t *row_pos,
-                                 bool rep_layout, uint8_t *codes, uint8_t *sf, cudaStream_t s)
+                                 uint8_t *codes, uint8_t *sf, cudaStream_t s)
 {
     const int64_t n_blocks = rows * (int64_t)(cols / 16);
     const unsigned grid = (unsigned)((n_blocks + 255) / 256);
     stage_begin(kStQuantH, s);
-    if (rep_layout)
-        quantize_rows_kernel<true><<<grid, 256, 0, s>>>(in, n_blocks, cols, row_pos, codes, sf);
-    else
-        quantize_rows_kernel<false><<<grid, 256, 0, s>>>(in, n_blocks, cols, row_pos, codes, sf);
+    quantize_rows_kernel<<<grid, 256, 0, s>>>(in, n_blocks, cols, row_pos, codes, sf);
     stage_end(kStQuantH, s);
     return cudaGetLastError();
 }

@@ -21,15 +21,10 @@
 //
 // Activation scales are laid out per token chunk (the N tile of one work
 // unit), written by the kernels that quantise x and h: atoms
-// [chunk, K/64, 512] for chunks of <= 128 rows, or (SFB_REP, chunks of <= 256
-// rows) [chunk, K/64, 4096]: per 64-block the atoms of rows 0-127 and
-// 128-255, each replicated 4 times, which one 128-lane x 256-bit tcgen05.cp
-// turns into the 8 scale columns of an N = 256 MMA.  Every tensor-core
-// instruction costs a roughly fixed number of cycles (about 140 for an MMA of
-// N <= 128, 160 for N = 256, 80-130 for a scale copy), so the N = 256 form
-// does twice the work per MMA with fewer copies.  K must be a multiple of
+// [chunk, K/64, 512] for chunks of <= 128 rows.  K must be a multiple of
 // 64: a last k-step with fewer than four 64-blocks issues fewer MMAs, and its
-// code tiles are zero-filled by TMA past the row end.
+// code tiles are zero-filled by TMA past the row end.  (Prefill-size batches
+// mostly run the token-major kernels of grouped_gemm_tm.cu.)
 //
 // MX8 variants run the MXFP8 experts (E4M3 values, one power-of-two UE8M0
 // scale per 32 elements, no global scale) through the same pipeline: a
@@ -60,8 +55,7 @@ constexpr int kAtom = 512;                        // scales of 128 rows x 64 ele
 constexpr int kSfStep = 4 * kAtom;                // scales of one k-step
 constexpr int kMaxExperts = 256;
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP,
-          bool MX8 = false>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool MX8 = false>
 struct CfgN {
     static constexpr int NA = GATEUP ? 2 : 1;
     static constexpr int THREADS = 64 + 128 * EPI_WG;
@@ -69,14 +63,14 @@ struct CfgN {
     static constexpr int B_BYTES = BN * kRowBytes;
     static constexpr int SFA_MAT = MX8 ? kAtom : kSfStep;  // one weight matrix's scales per stage
     static constexpr int SFA_BYTES = NA * SFA_MAT;
-    static constexpr int SFB_KB_BYTES = SFB_REP ? 4096 : kAtom;  // token scales of one atom unit
+    static constexpr int SFB_KB_BYTES = kAtom;  // token scales of one 64-block
     static constexpr int SFB_BYTES = MX8 ? kAtom : 4 * SFB_KB_BYTES;
     static constexpr int SF_BYTES = ((SFA_BYTES + SFB_BYTES + 1023) / 1024) * 1024;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
     static constexpr int BOX_BYTES = BOX * kRowBytes;
     static constexpr int ACC_COLS = NA * BN;
     static constexpr int SFA_COLS = MX8 ? 4 : 16;  // per weight matrix and stage
-    static constexpr int SFB_COLS = MX8 ? 4 : SFB_REP ? 32 : 16;
+    static constexpr int SFB_COLS = MX8 ? 4 : 16;
     static constexpr int SF_COLS = NA * SFA_COLS + SFB_COLS;
     static constexpr int SF_COL0 = ACC_BUFS * ACC_COLS;
     static constexpr int COLS_NEED = SF_COL0 + STAGES * SF_COLS;
@@ -88,9 +82,7 @@ struct CfgN {
     static constexpr int N_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int AUX_BYTES = N_BARS * 8 + 16 + 2 * (kMaxExperts + 1) * 4;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + ((AUX_BYTES + 127) / 128) * 128;
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= (SFB_REP ? 256 : 128),
-                  "MMA N; token scale atoms per chunk");
-    static_assert(!(MX8 && SFB_REP), "MXFP8 token scales are atoms");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N; token scale atoms per chunk");
     static_assert(BN % BOX == 0 && BOX % 8 == 0, "token boxes tile the B operand");
     static_assert(COLS_NEED <= 512, "TMEM columns");
     static_assert(STAGE_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle-atom alignment");
@@ -103,14 +95,13 @@ struct Fp4Params {
     int kblocks;  // 512-byte scale atoms per operand row tile: K / 64 (NVFP4), K / 128 (MXFP8)
 };
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP,
-          bool MX8>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool MX8>
 __global__ void __launch_bounds__(64 + 128 * EPI_WG, 1)
 grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                          const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB, const Fp4Params P)
 {
-    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP, MX8>;
+    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, MX8>;
     const GemmArgs &p = P.a;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -273,15 +264,12 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                                         ts + 4, tsb, accum);
                         }
                     } else {
-                        constexpr uint32_t kbB = SFB_REP ? 8 : 4;
+                        constexpr uint32_t kbB = 4;
                         for (int kb = 0; kb < nkb; ++kb) {
                             tmem_cp_atom(ts + 4 * kb, sf + kb * kAtom);
                             if (GATEUP)
                                 tmem_cp_atom(ts + 16 + 4 * kb, sf + kSfStep + kb * kAtom);
-                            if constexpr (SFB_REP)
-                                tmem_cp_pair(tsb + kbB * kb, sf + C::SFA_BYTES + kb * C::SFB_KB_BYTES);
-                            else
-                                tmem_cp_atom(tsb + kbB * kb, sf + C::SFA_BYTES + kb * kAtom);
+                            tmem_cp_atom(tsb + kbB * kb, sf + C::SFA_BYTES + kb * kAtom);
                         }
                         for (int kb = 0; kb < nkb; ++kb) {
                             const uint64_t bd = smem_desc_k128(st + C::A_BYTES + kb * 32);
@@ -402,14 +390,13 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
     }
 }
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool SFB_REP = false,
-          bool MX8 = false>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool MX8 = false>
 cudaError_t launch_nvf4_variant(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                                 const GemmArgs &args, const Fp4Weights &f, int kblocks, int grid,
                                 int stage, cudaStream_t s)
 {
-    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP, MX8>;
-    auto kern = grouped_gemm_nvf4_kernel<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, SFB_REP, MX8>;
+    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, MX8>;
+    auto kern = grouped_gemm_nvf4_kernel<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, MX8>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -434,17 +421,6 @@ cudaError_t launch_nvf4_variant(const CUtensorMap &a0, const CUtensorMap &a1, co
 int fp4_chunk_rows(GemmVariant v)
 {
     return v == GemmVariant::kDecode ? 32 : 128;
-}
-
-int fp4_down_chunk_rows(GemmVariant v)
-{
-    return v == GemmVariant::kDecode ? 32 : 128;
-}
-
-bool fp4_down_rep(GemmVariant v)
-{
-    (void)v;
-    return false;
 }
 
 int fp4_box_rows(GemmVariant v)
@@ -482,7 +458,7 @@ cudaError_t launch_gateup_mx8(GemmVariant v, const CUtensorMap &wg, const CUtens
     // prefill-size batches run the token-major kernel (grouped_gemm_tm.cu)
     if (v != GemmVariant::kDecode)
         return cudaErrorInvalidValue;
-    return launch_nvf4_variant<true, 32, 5, 2, 16, 1, false, true>(wg, wu, xq, a, f, kblocks, grid,
+    return launch_nvf4_variant<true, 32, 5, 2, 16, 1, true>(wg, wu, xq, a, f, kblocks, grid,
                                                                    kStGateUp, s);
 }
 
@@ -491,9 +467,9 @@ cudaError_t launch_down_mx8(GemmVariant v, const CUtensorMap &wd, const CUtensor
                             cudaStream_t s)
 {
     if (v == GemmVariant::kDecode)
-        return launch_nvf4_variant<false, 32, 10, 2, 16, 1, false, true>(wd, wd, hq, a, f, kblocks,
+        return launch_nvf4_variant<false, 32, 10, 2, 16, 1, true>(wd, wd, hq, a, f, kblocks,
                                                                          grid, kStDown, s);
-    return launch_nvf4_variant<false, 128, 6, 2, 128, 2, false, true>(wd, wd, hq, a, f, kblocks,
+    return launch_nvf4_variant<false, 128, 6, 2, 128, 2, true>(wd, wd, hq, a, f, kblocks,
                                                                       grid, kStDown, s);
 }
 

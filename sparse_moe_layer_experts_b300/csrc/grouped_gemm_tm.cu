@@ -332,15 +332,11 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
                             for (int i = 0; i < 32; ++i)
                                 amax = fmaxf(amax, fabsf(h[c][i]));
                             const int e = mx_shared_exp(amax);
+                            const float inv = mx_inv_scale(e);
                             uint32_t w[8];
 #pragma unroll
-                            for (int v = 0; v < 8; ++v) {
-                                uint32_t x = 0;
-#pragma unroll
-                                for (int i = 0; i < 4; ++i)
-                                    x |= mx_code(h[c][4 * v + i], e) << (8 * i);
-                                w[v] = x;
-                            }
+                            for (int v = 0; v < 8; ++v)
+                                w[v] = mx_code4(&h[c][4 * v], inv);
                             uint4 *dst = reinterpret_cast<uint4 *>(
                                 hq + (size_t)row * I + tl.m * 128 + 64 * wg + 32 * c);
                             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);

@@ -41,10 +41,10 @@ cudaError_t launch_select(const float *scores, int T, int E, int G, int TG, int 
 constexpr int kHistTokens = 256;  // tokens per histogram CTA
 cudaError_t launch_hist(const int32_t *ids, int T, int K, int E, int32_t *local_rank,
                         int32_t *cta_counts, int *status, cudaStream_t s);
-// chunk_start2 (may be null): a second chunking of chunk_rows2 rows
+// offsets, counts, cta_base, and the token chunks of chunk_rows rows per expert
 cudaError_t launch_scan(const int32_t *cta_counts, int n_cta, int E, int chunk_rows,
-                        int chunk_rows2, int32_t *cta_base, int32_t *counts, int32_t *offsets,
-                        int32_t *chunk_start, int32_t *chunk_start2, cudaStream_t s);
+                        int32_t *cta_base, int32_t *counts, int32_t *offsets,
+                        int32_t *chunk_start, cudaStream_t s);
 cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
                            const int32_t *cta_base, const int32_t *offsets, int T, int K, int E,
                            int H, int32_t *row_of, int32_t *row_src, void *x_perm,
@@ -61,24 +61,22 @@ cudaError_t launch_permute_mx8(const uint16_t *x, const int32_t *ids, const int3
 cudaError_t launch_quantize_rows_mx8(const float *in, int64_t rows, int cols, const int32_t *row_pos,
                                      uint8_t *codes, uint8_t *sf, cudaStream_t s);
 // NVFP4 layers: x rows quantised (global scale 1) into codes [R, H/2] and
-// scale atoms [chunk, H/64, 512] of the gate/up chunking (chunk_start);
-// row_pos[row] = chunk2*256 + j2 in the down GEMM's chunking (chunk_start2)
+// scale atoms [chunk, H/64, 512] of the token chunking (chunk_start);
+// row_pos[row] = chunk*256 + j, the row's place in that chunking
 cudaError_t launch_permute_nvfp4(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
                                  const int32_t *cta_base, const int32_t *offsets,
-                                 const int32_t *chunk_start, const int32_t *chunk_start2, int T,
-                                 int K, int E, int H, int32_t *row_of, int32_t *row_src,
-                                 int32_t *row_pos, uint8_t *x_codes, uint8_t *x_sf,
-                                 cudaStream_t s);
+                                 const int32_t *chunk_start, int T, int K, int E, int H,
+                                 int32_t *row_of, int32_t *row_src, int32_t *row_pos,
+                                 uint8_t *x_codes, uint8_t *x_sf, cudaStream_t s);
 // route-only variant: row_of without moving activations
 cudaError_t launch_rows(const int32_t *ids, const int32_t *local_rank, const int32_t *cta_base,
                         const int32_t *offsets, int T, int K, int E, int32_t *row_of,
                         cudaStream_t s);
 // NVFP4 activations: FP32 [rows, cols] -> codes [rows, cols/2] and scales at
 // the token-chunk positions row_pos names (global scale 1): atoms
-// [chunk, cols/64, 512], or with rep_layout the replicated images
-// [chunk, cols/64, 4096] of 256-row chunks
+// [chunk, cols/64, 512]
 cudaError_t launch_quantize_rows(const float *in, int64_t rows, int cols, const int32_t *row_pos,
-                                 bool rep_layout, uint8_t *codes, uint8_t *sf, cudaStream_t s);
+                                 uint8_t *codes, uint8_t *sf, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t *y, const float *w, const int32_t *row_of, int T, int K,
                            int H, uint16_t *out, cudaStream_t s);
 // fused MoE block: x = bf16(rmsnorm(s_in) * gamma) (FP64 sum of squares,
@@ -121,6 +119,9 @@ struct Fp4Weights {
 };
 
 // ---- nvfp4.cu
+// FP32 activation rows -> codes and row-major scales (global scale 1)
+cudaError_t launch_quantize_act(bool mx8, const float *x, int64_t rows, int cols, uint8_t *codes,
+                                uint8_t *sf, cudaStream_t s);
 cudaError_t launch_quantize_nvfp4(const uint16_t *w, int64_t n_mat, int rows, int cols,
                                   uint8_t *packed, uint8_t *block_sf, float *global_sf,
                                   cudaStream_t s);
@@ -150,13 +151,11 @@ cudaError_t launch_down_pair(const CUtensorMap &wd, const CUtensorMap &hp, const
 // (E2M1 codes of weights and activations via 128-byte TMA rows, block
 // scales via bulk copies).  Gate/up here is the decode-size kernel only
 // (prefill-size batches: launch_gateup_tm); it writes h in FP32 for
-// launch_quantize_rows.  kblocks = K/64.  Gate/up token chunks are fp4_chunk_rows(v) rows at most,
-// down chunks fp4_down_chunk_rows(v); the activation maps use
-// fp4_box_rows(v)-row boxes.  fp4_down_rep(v): the down GEMM takes h's
-// scales in the replicated 256-row layout (launch_quantize_rows rep_layout).
+// launch_quantize_rows.  Down here: decode size, and prefill size with an
+// odd H/128 (else launch_down_tm).  kblocks = K/64.  Token chunks are
+// fp4_chunk_rows(v) rows at most; the activation maps use fp4_box_rows(v)-row
+// boxes; activation scales are atoms [chunk, K/64, 512].
 int fp4_chunk_rows(GemmVariant v);
-int fp4_down_chunk_rows(GemmVariant v);
-bool fp4_down_rep(GemmVariant v);
 int fp4_box_rows(GemmVariant v);
 // MXFP8 experts on the same kernels (kind::mxf8f6f4): E4M3 codes, one
 // UE8M0 scale per 32 elements, scale atoms [.., K/128, 512]; kblocks = K/128;

@@ -83,13 +83,13 @@ nvfp4_quantize_kernel(const uint16_t *__restrict__ w, int64_t n_blocks, int rows
     const uint32_t sc = nvfp4_block_scale(bmax, g, &sfv);
     const float den = __fmul_rn(sfv, g);
     uint32_t lo = 0, hi = 0;
+    if (sfv != 0.0f) {
+        float q[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const uint32_t c = (sfv == 0.0f) ? 0u : e2m1_code(__fdiv_rn(v[i], den));
-        if (i < 8)
-            lo |= c << (4 * i);
-        else
-            hi |= c << (4 * (i - 8));
+        for (int i = 0; i < 16; ++i)
+            q[i] = __fdiv_rn(v[i], den);
+        lo = e2m1x8(q);
+        hi = e2m1x8(q + 8);
     }
     *reinterpret_cast<uint2 *>(packed + elem / 2) = make_uint2(lo, hi);
     const int64_t tile = (mat * (rows / 128) + r / 128) * (cols / 64) + cb / 4;
@@ -127,14 +127,11 @@ mxfp8_quantize_kernel(const uint16_t *__restrict__ w, int64_t n_blocks, int rows
     for (int i = 0; i < 32; ++i)
         amax = fmaxf(amax, fabsf(v[i]));
     const int e = mx_shared_exp(amax);
+    const float inv = mx_inv_scale(e);
     uint32_t out[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        out[q] = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            out[q] |= mx_code(v[4 * q + i], e) << (8 * i);
-    }
+    for (int q = 0; q < 8; ++q)
+        out[q] = mx_code4(v + 4 * q, inv);
     uint4 *dst = reinterpret_cast<uint4 *>(codes + elem);
     dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
     dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
@@ -143,6 +140,78 @@ mxfp8_quantize_kernel(const uint16_t *__restrict__ w, int64_t n_blocks, int rows
 }
 
 }  // namespace
+
+// Activation rows (FP32, global scale 1), the rule the layer applies to x
+// and h: NVFP4 one thread per 16-block, MXFP8 one thread per 32-block;
+// scales row-major [rows, cols/16] (E4M3) or [rows, cols/32] (E8M0).
+__global__ void __launch_bounds__(256)
+quantize_act_nvfp4_kernel(const float *__restrict__ x, int64_t n_blocks, uint8_t *__restrict__ codes,
+                          uint8_t *__restrict__ sf)
+{
+    const int64_t b = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (b >= n_blocks)
+        return;
+    const float4 *src = reinterpret_cast<const float4 *>(x) + 4 * b;
+    float v[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 f = src[q];
+        v[4 * q] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
+    }
+    uint32_t lo, hi;
+    sf[b] = (uint8_t)nvfp4_quant16(v, &lo, &hi);
+    reinterpret_cast<uint2 *>(codes)[b] = make_uint2(lo, hi);
+}
+
+__global__ void __launch_bounds__(256)
+quantize_act_mxfp8_kernel(const float *__restrict__ x, int64_t n_blocks, uint8_t *__restrict__ codes,
+                          uint8_t *__restrict__ sf)
+{
+    const int64_t b = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (b >= n_blocks)
+        return;
+    const float4 *src = reinterpret_cast<const float4 *>(x) + 8 * b;
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 f = src[q];
+        v[4 * q] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        amax = fmaxf(amax, fabsf(v[i]));
+    const int e = mx_shared_exp(amax);
+    const float inv = mx_inv_scale(e);
+    uint32_t out[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        out[q] = mx_code4(v + 4 * q, inv);
+    uint4 *dst = reinterpret_cast<uint4 *>(codes) + 2 * b;
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    sf[b] = (uint8_t)(e + 127);
+}
+
+cudaError_t launch_quantize_act(bool mx8, const float *x, int64_t rows, int cols, uint8_t *codes,
+                                uint8_t *sf, cudaStream_t s)
+{
+    const int64_t n_blocks = rows * (int64_t)(cols / (mx8 ? 32 : 16));
+    const unsigned grid = (unsigned)((n_blocks + 255) / 256);
+    stage_begin(kNumStages, s);
+    if (mx8)
+        quantize_act_mxfp8_kernel<<<grid, 256, 0, s>>>(x, n_blocks, codes, sf);
+    else
+        quantize_act_nvfp4_kernel<<<grid, 256, 0, s>>>(x, n_blocks, codes, sf);
+    stage_end(kNumStages, s);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_mxfp8(const uint16_t *w, int64_t n_mat, int rows, int cols,
                                   uint8_t *codes, uint8_t *block_sf, cudaStream_t s)

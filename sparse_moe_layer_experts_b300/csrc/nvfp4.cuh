@@ -15,41 +15,6 @@
 
 namespace beam {
 
-// Nearest E2M1 code (ties to the even mantissa bit, saturating at 6, sign
-// kept in bit 3).  Thresholds are the midpoints of 0, .5, 1, 1.5, 2, 3, 4, 6.
-__device__ __forceinline__ uint32_t e2m1_code(float v)
-{
-    const float a = fabsf(v);
-    uint32_t c;
-    if (a <= 0.25f)
-        c = 0;
-    else if (a < 0.75f)
-        c = 1;
-    else if (a <= 1.25f)
-        c = 2;
-    else if (a < 1.75f)
-        c = 3;
-    else if (a <= 2.5f)
-        c = 4;
-    else if (a < 3.5f)
-        c = 5;
-    else if (a <= 5.0f)
-        c = 6;
-    else
-        c = 7;
-    return c | (signbit(v) ? 8u : 0u);
-}
-
-__device__ __forceinline__ float e2m1_value(uint32_t c)
-{
-    // magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 built as FP32 bit patterns:
-    // exponent 126 + (m >> 1), mantissa bit (m & 1) for m >= 2
-    const uint32_t m = c & 7u;
-    const uint32_t bits =
-        (m == 0u) ? 0u : ((126u + (m >> 1)) << 23) | ((m >= 2u ? (m & 1u) : 0u) << 22);
-    return __uint_as_float(bits | ((c & 8u) << 28));
-}
-
 __device__ __forceinline__ uint32_t e4m3_code(float v)
 {
     return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
@@ -70,11 +35,36 @@ __device__ __forceinline__ uint32_t nvfp4_block_scale(float bmax, float gs, floa
     return c;
 }
 
-// E2M1 code of one value of a block with scale value sfv (global scale 1):
-// 0 when the block scale is 0.
-__device__ __forceinline__ uint32_t nvfp4_code(float v, float sfv)
+// v / s rounded to nearest FP32 for an E4M3 scale value s > 0, given
+// r = RN(1/s): one correction step after the reciprocal product (Markstein's
+// method: q0 = RN(v r); the FMA gives the exact remainder v - s q0; q =
+// RN(q0 + rem r)).  Over all 126 positive E4M3 values s it equals the
+// correctly rounded quotient wherever that quotient decides an E2M1 code
+// (every FP32 v within 64 ulps of a code boundary, checked exhaustively in
+// exact arithmetic), so codes taken from it match codes from v / s.
+__device__ __forceinline__ float div_by_scale(float v, float s, float r)
 {
-    return sfv == 0.0f ? 0u : e2m1_code(__fdiv_rn(v, sfv));
+    const float q0 = __fmul_rn(v, r);
+    const float rem = __fmaf_rn(-q0, s, v);
+    return __fmaf_rn(rem, r, q0);
+}
+
+// Eight E2M1 codes, element i in bits 4i..4i+3 (sign in the top bit of each
+// code): the hardware conversion rounds to the nearest of 0, 0.5, 1, 1.5, 2,
+// 3, 4, 6 with ties to the even code and saturates at 6.
+__device__ __forceinline__ uint32_t e2m1x8(const float *q)
+{
+    uint32_t out;
+    asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+        "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+        : "=r"(out)
+        : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]),
+          "f"(q[7]));
+    return out;
 }
 
 // Quantise 16 values with global scale 1: 8 code bytes (even element in the
@@ -87,14 +77,18 @@ __device__ __forceinline__ uint32_t nvfp4_quant16(const float (&v)[16], uint32_t
         bmax = fmaxf(bmax, fabsf(v[i]));
     float sfv;
     const uint32_t sc = nvfp4_block_scale(bmax, 1.0f, &sfv);
-    uint32_t a = 0, b = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        a |= nvfp4_code(v[i], sfv) << (4 * i);
-        b |= nvfp4_code(v[i + 8], sfv) << (4 * i);
+    if (sfv == 0.0f) {
+        *lo = 0u;
+        *hi = 0u;
+        return sc;
     }
-    *lo = a;
-    *hi = b;
+    const float r = __frcp_rn(sfv);
+    float q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        q[i] = div_by_scale(v[i], sfv, r);
+    *lo = e2m1x8(q);
+    *hi = e2m1x8(q + 8);
     return sc;
 }
 
@@ -110,10 +104,23 @@ __device__ __forceinline__ int mx_shared_exp(float amax)
     return max(-127, min(127, ex - 1 - 8));
 }
 
-// E4M3 code of v / 2^e (exact scaling), round to nearest even, saturating
-__device__ __forceinline__ uint32_t mx_code(float v, int e)
+// 2^-e for a shared exponent e in [-127, 119] (the range mx_shared_exp
+// gives for finite FP32 blocks): a normal FP32 power of two
+__device__ __forceinline__ float mx_inv_scale(int e)
 {
-    return (uint32_t)__nv_cvt_float_to_fp8(ldexpf(v, -e), __NV_SATFINITE, __NV_E4M3);
+    return __int_as_float((127 - e) << 23);
+}
+
+// Four E4M3 codes of v * 2^-e (an exact power-of-two scaling, correctly
+// rounded where it leaves the normal range), round to nearest even,
+// saturating; element i in byte i.
+__device__ __forceinline__ uint32_t mx_code4(const float *v, float inv)
+{
+    const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv)), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fmul_rn(v[2], inv), __fmul_rn(v[3], inv)), __NV_SATFINITE, __NV_E4M3);
+    return (uint32_t)a | ((uint32_t)b << 16);
 }
 
 // Token chunks: an expert's n rows are split into nc near-equal chunks,

@@ -48,6 +48,23 @@ def quantize_mxfp8(w: torch.Tensor, stream=None):
     return codes, sf
 
 
+def quantize_activations(x: torch.Tensor, wtype: int, stream=None):
+    """Quantise FP32 activation rows [rows, cols] with the layer's activation
+    rule (global scale 1).  wtype B.BEAM_MOE_W_NVFP4: (codes [rows, cols/2]
+    two per byte, E4M3 scales [rows, cols/16]); B.BEAM_MOE_W_MXFP8: (E4M3
+    codes [rows, cols], scale bytes [rows, cols/32])."""
+    if x.dtype != torch.float32 or x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA float32 [rows, cols] tensor")
+    rows, cols = x.shape
+    mx8 = wtype == B.BEAM_MOE_W_MXFP8
+    codes = torch.empty((rows, cols if mx8 else cols // 2), dtype=torch.uint8, device=x.device)
+    sf = torch.empty((rows, cols // (32 if mx8 else 16)), dtype=torch.uint8, device=x.device)
+    B.check(B.beam_moe_quantize_act(wtype, x.data_ptr(), rows, cols, codes.data_ptr(),
+                                    sf.data_ptr(), _stream_handle(stream)),
+            "beam_moe_quantize_act")
+    return codes, sf
+
+
 class BeamMoE:
     """Resident-weight layer.  Weights: w_gate/w_up [E,I,H] bf16, w_down [E,H,I]
     bf16, router_w [H,E] fp32, all contiguous on one CUDA device.  For NVFP4

@@ -148,3 +148,17 @@ def test_block_entry_point_checks(L):
         B.BEAM_MOE_ERR_UNSUPPORTED
     assert B.beam_moe_launch_count() == before
 
+
+
+def test_activation_quantiser_checks(L):
+    before = B.beam_moe_launch_count()
+    nv, mx = B.BEAM_MOE_W_NVFP4, B.BEAM_MOE_W_MXFP8
+    assert B.beam_moe_quantize_act(nv, 16, 0, 64, 16, 16, None) == B.BEAM_MOE_OK
+    assert B.beam_moe_quantize_act(B.BEAM_MOE_W_BF16, 16, 4, 64, 16, 16, None) == \
+        B.BEAM_MOE_ERR_INVALID_ARG
+    assert B.beam_moe_quantize_act(nv, 16, 4, 40, 16, 16, None) == B.BEAM_MOE_ERR_INVALID_ARG
+    assert B.beam_moe_quantize_act(mx, 16, 4, 48, 16, 16, None) == B.BEAM_MOE_ERR_INVALID_ARG
+    assert B.beam_moe_quantize_act(nv, 16, -1, 64, 16, 16, None) == B.BEAM_MOE_ERR_INVALID_ARG
+    assert B.beam_moe_quantize_act(nv, 18, 4, 64, 16, 16, None) == B.BEAM_MOE_ERR_INVALID_ARG
+    assert B.beam_moe_quantize_act(nv, None, 4, 64, 16, 16, None) == B.BEAM_MOE_ERR_INVALID_ARG
+    assert B.beam_moe_launch_count() == before
