@@ -243,9 +243,8 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                     tc_fence_after();
                     const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
                     const uint32_t sf = st + C::A_BYTES + C::B_BYTES;
-                    // this stage's scale columns: A0 | A1 (16 each) | B (16, or
-                    // 32 = 8 per 64-block in the replicated form); every MMA
-                    // scale address is a multiple of 4 columns
+                    // this stage's scale columns: A0 | A1 (16 each) | B (16; MXFP8
+                    // 4 each); every MMA scale address is a multiple of 4 columns
                     const uint32_t ts = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
                     const uint32_t tsb = ts + C::SFA_COLS * C::NA;
                     if constexpr (MX8) {
@@ -264,21 +263,20 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                                         ts + 4, tsb, accum);
                         }
                     } else {
-                        constexpr uint32_t kbB = 4;
                         for (int kb = 0; kb < nkb; ++kb) {
                             tmem_cp_atom(ts + 4 * kb, sf + kb * kAtom);
                             if (GATEUP)
                                 tmem_cp_atom(ts + 16 + 4 * kb, sf + kSfStep + kb * kAtom);
-                            tmem_cp_atom(tsb + kbB * kb, sf + C::SFA_BYTES + kb * kAtom);
+                            tmem_cp_atom(tsb + 4 * kb, sf + C::SFA_BYTES + kb * kAtom);
                         }
                         for (int kb = 0; kb < nkb; ++kb) {
                             const uint64_t bd = smem_desc_k128(st + C::A_BYTES + kb * 32);
                             const uint32_t accum = (k | kb) != 0;
                             mma_nvf4(d, smem_desc_k128(st + kb * 32), bd, idesc, ts + 4 * kb,
-                                     tsb + kbB * kb, accum);
+                                     tsb + 4 * kb, accum);
                             if (GATEUP)
                                 mma_nvf4(d + BN, smem_desc_k128(st + kACodeBytes + kb * 32), bd,
-                                         idesc, ts + 16 + 4 * kb, tsb + kbB * kb, accum);
+                                         idesc, ts + 16 + 4 * kb, tsb + 4 * kb, accum);
                         }
                     }
                     mma_commit(empty_bar(stage));

@@ -86,7 +86,7 @@ struct TmCfg {
 };
 
 struct TmParams {
-    GemmArgs a;      // m_tiles = 256-row weight tile pairs per expert; out = h codes / y
+    GemmArgs a;      // m_tiles = N tiles (256 weight rows) per expert; out = h codes / y
     Fp4Weights f;    // sf0 / sf1 weight atoms, gs0 / gs1 (NVFP4), act_sf token atoms
     int kblocks;     // scale atoms per operand row tile: K/64 (NVFP4), K/128 (MXFP8)
     int n_tiles_w;   // 128-row weight tiles per expert in sf0 / the B maps
