@@ -34,7 +34,12 @@
 // scale-factor ids of the instruction descriptor.
 //
 // Warp roles: warp 0 TMA/bulk-copy producer, warp 1 TMEM allocator and MMA
-// issuer, then EPI_WG epilogue warpgroups splitting a tile's columns.
+// issuer, then EPI_WG epilogue warpgroups splitting a tile's columns, and
+// with SFST a scale warpgroup: it writes each stage's scale atoms into tensor
+// memory with tcgen05.st (each warp its lane quarter, the layout of a
+// 32x128b.warpx4 copy) and signals the MMA thread, so the tensor pipe issues
+// only MMAs.  A stage's scale columns are its atoms in shared-memory order
+// (weights A0, A1, then tokens), column c = word c % 4 of atom c / 4.
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "internal.h"
@@ -55,10 +60,12 @@ constexpr int kAtom = 512;                        // scales of 128 rows x 64 ele
 constexpr int kSfStep = 4 * kAtom;                // scales of one k-step
 constexpr int kMaxExperts = 256;
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool MX8 = false>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool MX8 = false,
+          bool SFST = false>
 struct CfgN {
     static constexpr int NA = GATEUP ? 2 : 1;
-    static constexpr int THREADS = 64 + 128 * EPI_WG;
+    static constexpr int THREADS = 64 + 128 * EPI_WG + (SFST ? 128 : 0);
+    static constexpr int SF_W0 = 2 + 4 * EPI_WG;  // first scale warp (SFST)
     static constexpr int A_BYTES = NA * kACodeBytes;
     static constexpr int B_BYTES = BN * kRowBytes;
     static constexpr int SFA_MAT = MX8 ? kAtom : kSfStep;  // one weight matrix's scales per stage
@@ -79,7 +86,7 @@ struct CfgN {
                                      : COLS_NEED <= 128 ? 128
                                      : COLS_NEED <= 256 ? 256
                                                         : 512;
-    static constexpr int N_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int N_BARS = 3 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int AUX_BYTES = N_BARS * 8 + 16 + 2 * (kMaxExperts + 1) * 4;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + ((AUX_BYTES + 127) / 128) * 128;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N; token scale atoms per chunk");
@@ -87,6 +94,8 @@ struct CfgN {
     static_assert(COLS_NEED <= 512, "TMEM columns");
     static_assert(STAGE_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle-atom alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(!SFST || (!MX8 && SF_COLS % 16 == 0 && SF_COL0 % 16 == 0),
+                  "scale staging: NVFP4, whole 16-column stores");
 };
 
 struct Fp4Params {
@@ -95,13 +104,13 @@ struct Fp4Params {
     int kblocks;  // 512-byte scale atoms per operand row tile: K / 64 (NVFP4), K / 128 (MXFP8)
 };
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool MX8>
-__global__ void __launch_bounds__(64 + 128 * EPI_WG, 1)
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool MX8, bool SFST>
+__global__ void __launch_bounds__(CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, MX8, SFST>::THREADS, 1)
 grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                          const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB, const Fp4Params P)
 {
-    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, MX8>;
+    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, MX8, SFST>;
     const GemmArgs &p = P.a;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -120,6 +129,7 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
     auto tfull_bar = [&](int a) { return bar_u32 + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bar_u32 + 8u * (2 * STAGES + ACC_BUFS + a); };
     const uint32_t drain_bar = bar_u32 + 8u * (2 * STAGES + 2 * ACC_BUFS);
+    auto sfready_bar = [&](int s) { return bar_u32 + 8u * (2 * STAGES + 2 * ACC_BUFS + 1 + s); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
@@ -133,6 +143,9 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
         for (int a = 0; a < ACC_BUFS; ++a) {
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), 128 * EPI_WG);
+        }
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(sfready_bar(s), 4);  // one arrive per scale warp (SFST)
         }
         mbar_init(drain_bar, 1);
         *s_abort = 0;
@@ -236,7 +249,9 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                 const uint32_t d = tmem_base + acc * C::ACC_COLS;
                 for (int k = 0; k < p.ksteps; ++k) {
                     const int nkb = MX8 ? 4 : min(4, KB - 4 * k);  // MMAs of this k-step
-                    if (!mbar_wait_bounded(full_bar(stage), phase, tmo, s_abort, p.status)) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, tmo, s_abort, p.status) ||
+                        (SFST &&
+                         !mbar_wait_bounded(sfready_bar(stage), phase, tmo, s_abort, p.status))) {
                         ok = false;
                         break;
                     }
@@ -263,11 +278,13 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                                         ts + 4, tsb, accum);
                         }
                     } else {
-                        for (int kb = 0; kb < nkb; ++kb) {
-                            tmem_cp_atom(ts + 4 * kb, sf + kb * kAtom);
-                            if (GATEUP)
-                                tmem_cp_atom(ts + 16 + 4 * kb, sf + kSfStep + kb * kAtom);
-                            tmem_cp_atom(tsb + 4 * kb, sf + C::SFA_BYTES + kb * kAtom);
+                        if constexpr (!SFST) {
+                            for (int kb = 0; kb < nkb; ++kb) {
+                                tmem_cp_atom(ts + 4 * kb, sf + kb * kAtom);
+                                if (GATEUP)
+                                    tmem_cp_atom(ts + 16 + 4 * kb, sf + kSfStep + kb * kAtom);
+                                tmem_cp_atom(tsb + 4 * kb, sf + C::SFA_BYTES + kb * kAtom);
+                            }
                         }
                         for (int kb = 0; kb < nkb; ++kb) {
                             const uint64_t bd = smem_desc_k128(st + C::A_BYTES + kb * 32);
@@ -299,7 +316,7 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < C::SF_W0) {
         // ------------------------------------------------- epilogue
         const int q = warp & 3;
         const int i = q * 32 + lane;
@@ -378,6 +395,48 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
                 acc_phase ^= 1u;
             }
         }
+    } else if constexpr (SFST) {
+        // --------------------------------------- scale staging (SFST)
+        // lane i of warp quarter q: column c of the stage = word c % 4 of
+        // row i of atom c / 4 (atoms contiguous in the stage's scale region)
+        const int q = warp & 3;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            for (int k = 0; k < p.ksteps; ++k) {
+                if (!mbar_wait_bounded(full_bar(stage), phase, tmo, s_abort, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *sf = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+                const uint32_t ta =
+                    tmem_base + ((uint32_t)(q * 32) << 16) + C::SF_COL0 + stage * C::SF_COLS;
+#pragma unroll
+                for (int g = 0; g < C::SF_COLS / 16; ++g) {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        const uint4 v =
+                            *reinterpret_cast<const uint4 *>(sf + (4 * g + a) * kAtom + 16 * lane);
+                        r[4 * a] = v.x;
+                        r[4 * a + 1] = v.y;
+                        r[4 * a + 2] = v.z;
+                        r[4 * a + 3] = v.w;
+                    }
+                    tmem_st16(ta + 16 * g, r);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(sfready_bar(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
     }
 
     tc_fence_before();
@@ -388,13 +447,14 @@ grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA0,
     }
 }
 
-template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool MX8 = false>
+template <bool GATEUP, int BN, int STAGES, int ACC_BUFS, int BOX, int EPI_WG, bool MX8 = false,
+          bool SFST = false>
 cudaError_t launch_nvf4_variant(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                                 const GemmArgs &args, const Fp4Weights &f, int kblocks, int grid,
                                 int stage, cudaStream_t s)
 {
-    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, MX8>;
-    auto kern = grouped_gemm_nvf4_kernel<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, MX8>;
+    using C = CfgN<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, MX8, SFST>;
+    auto kern = grouped_gemm_nvf4_kernel<GATEUP, BN, STAGES, ACC_BUFS, BOX, EPI_WG, MX8, SFST>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -433,8 +493,8 @@ cudaError_t launch_gateup_fp4(GemmVariant v, const CUtensorMap &wg, const CUtens
     // prefill-size batches run the token-major kernel (grouped_gemm_tm.cu)
     if (v != GemmVariant::kDecode)
         return cudaErrorInvalidValue;
-    return launch_nvf4_variant<true, 32, 5, 2, 16, 1>(wg, wu, xq, a, f, kblocks, grid, kStGateUp,
-                                                      s);
+    return launch_nvf4_variant<true, 32, 5, 2, 16, 1, false, true>(wg, wu, xq, a, f, kblocks, grid,
+                                                                   kStGateUp, s);
 }
 
 cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensorMap &hq,
@@ -442,8 +502,8 @@ cudaError_t launch_down_fp4(GemmVariant v, const CUtensorMap &wd, const CUtensor
                             cudaStream_t s)
 {
     if (v == GemmVariant::kDecode)
-        return launch_nvf4_variant<false, 32, 9, 2, 16, 1>(wd, wd, hq, a, f, kblocks, grid, kStDown,
-                                                           s);
+        return launch_nvf4_variant<false, 32, 9, 2, 16, 1, false, true>(wd, wd, hq, a, f, kblocks,
+                                                                        grid, kStDown, s);
     // prefill size with an odd H/128 (even H/128 runs token-major)
     return launch_nvf4_variant<false, 128, 6, 2, 128, 2>(wd, wd, hq, a, f, kblocks, grid, kStDown,
                                                          s);
