@@ -2,13 +2,13 @@
 // batches: the expert's token rows are the M = 128 operand and 256 weight
 // rows the N operand, so each block-scaled MMA is 128 x 256.
 //
-// Same computation as the prefill GEMMs of grouped_gemm_fp4.cu (the SwiGLU
-// experts of "Reflection Beam 1.0", section "Mixture of Experts", with NVFP4
-// or MXFP8 operands), laid out for the tensor pipe's cost model: every
-// tcgen05 instruction costs a roughly fixed number of cycles (about 142 for
-// an N <= 128 MMA, 161 for N = 256, plus the scale copies), so one 128 x 256
-// MMA per 64-block does the work of the two 128 x 128 MMAs the weight-major
-// gate/up kernel issues.
+// Same computation as the weight-major GEMMs of grouped_gemm_fp4.cu, which
+// serve decode-size batches (the SwiGLU experts of "Reflection Beam 1.0",
+// section "Mixture of Experts", with NVFP4 or MXFP8 operands), laid out for
+// the tensor pipe's cost model: every tcgen05 instruction costs a roughly
+// fixed number of cycles (about 142 for an N <= 128 MMA, 161 for N = 256,
+// plus the scale copies), so one 128 x 256 MMA per 64-block does the work of
+// the two 128 x 128 MMAs a weight-major gate/up tile issues.
 //
 // Gate/up: the N operand is gate tile m (rows 0-127) stacked on up tile m
 // (rows 128-255), so one accumulator holds g and u side by side for 128
@@ -31,7 +31,8 @@
 // warp its lane quarter: lane 32q + i, columns c..c+3 = words 0-3 of atom
 // row i, the layout a 32x128b.warpx4 copy produces), then signals the MMA
 // thread; the tensor pipe then runs only MMAs.  Without SFST the MMA thread
-// copies the atoms with tcgen05.cp.
+// copies the atoms with tcgen05.cp.  NVFP4 (12 atoms per k-step) uses SFST;
+// MXFP8 (3 atoms per four MMAs) copies, which measured faster there.
 //
 // Warp roles: warp 0 TMA / bulk-copy producer, warp 1 TMEM allocator and MMA
 // issuer, two epilogue warpgroups (features split in halves), and with SFST
