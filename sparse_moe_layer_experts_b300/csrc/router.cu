@@ -262,13 +262,17 @@ router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr
     }
 }
 
-// Small batches (decode): the FMA chain of each output is the critical
-// path, so one thread owns one output and the CTAs spread over the experts.
-// CTA = 32 tokens x 4 experts (128 threads); K chunks of 64 flow through a
-// 4-stage cp.async ring.
-constexpr int kSTM = 32, kSTE = 4, kSKC = 64, kSNS = 4, kSXP = kSKC + 8;
+// Small batches (decode): each output's 5,120-long FMA chain is the critical
+// path and there are few outputs (T x E), so the work is spread thin: a CTA
+// is one warp owning 8 tokens x 8 experts, and lane (tt, ep) runs two
+// independent chains, experts e0 + 2ep and e0 + 2ep + 1 of token t0 + tt
+// (T=32 fills 128 SMs).  Per 8 hidden values a lane issues one 128-bit load
+// of x, eight 64-bit loads of weight pairs and 16 FMAs.  K chunks of 64 flow
+// through a 12-stage cp.async ring (a chunk is ~300 cycles of chain, so the
+// ring runs ~1.5 us ahead of the loads' latency).
+constexpr int kSTM = 8, kSTE = 8, kSKC = 64, kSNS = 12, kSXP = kSKC + 8;
 
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(32)
 router_scores_small(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H,
                     int E, float *__restrict__ scores, int *status)
 {
@@ -276,21 +280,24 @@ router_scores_small(const uint16_t *__restrict__ x, const float *__restrict__ wr
         *status = 0;
     __shared__ __align__(16) uint16_t xs[kSNS][kSTM][kSXP];
     __shared__ __align__(16) float ws[kSNS][kSKC][kSTE];
-    const int tid = threadIdx.x;
-    const int te = tid & 3, tt = tid >> 2;
+    const int lane = threadIdx.x;
+    const int tt = lane >> 2, ep = lane & 3;
     const int t0 = blockIdx.x * kSTM, e0 = blockIdx.y * kSTE;
     const int nk = H / kSKC;
 
     auto load = [&](int st, int k0) {
-        // x: 32 rows x 8 chunks of 16 B; w: 64 rows x one 16-B chunk
-        for (int c = tid; c < kSTM * (kSKC / 8); c += 128) {
+        // x: 8 rows x 8 chunks of 16 B; w: 64 rows x two 16-B chunks (4 experts each)
+#pragma unroll
+        for (int c = lane; c < kSTM * (kSKC / 8); c += 32) {
             const int r = c >> 3, q = c & 7;
             const bool ok = t0 + r < T;
             cp_async16(&xs[st][r][q * 8], x + (size_t)(ok ? t0 + r : 0) * H + k0 + q * 8, ok);
         }
-        if (tid < kSKC) {
-            const bool ok = e0 < E;
-            cp_async16(&ws[st][tid][0], wr + (size_t)(k0 + tid) * E + (ok ? e0 : 0), ok);
+#pragma unroll
+        for (int c = lane; c < kSKC * 2; c += 32) {
+            const int r = c >> 1, h4 = (c & 1) * 4;
+            const bool ok = e0 + h4 < E;
+            cp_async16(&ws[st][r][h4], wr + (size_t)(k0 + r) * E + (ok ? e0 + h4 : 0), ok);
         }
     };
 
@@ -300,21 +307,36 @@ router_scores_small(const uint16_t *__restrict__ x, const float *__restrict__ wr
             load(s, s * kSKC);
         cp_async_commit();
     }
-    float acc = 0.0f;
+    float acc0 = 0.0f, acc1 = 0.0f;
     for (int kc = 0; kc < nk; ++kc) {
         cp_async_wait<kSNS - 2>();
-        __syncthreads();
+        __syncwarp();
         if (kc + kSNS - 1 < nk)
             load((kc + kSNS - 1) % kSNS, (kc + kSNS - 1) * kSKC);
         cp_async_commit();
         const int st = kc % kSNS;
-#pragma unroll 16
-        for (int k = 0; k < kSKC; ++k)
-            acc = __fmaf_rn(bf16_bits_to_f32(xs[st][tt][k]), ws[st][k][te], acc);
+#pragma unroll
+        for (int k8 = 0; k8 < kSKC; k8 += 8) {
+            const uint4 xv = *reinterpret_cast<const uint4 *>(&xs[st][tt][k8]);
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float xf = (i & 1) ? __uint_as_float(xw[i >> 1] & 0xFFFF0000u)
+                                         : __uint_as_float(xw[i >> 1] << 16);
+                const float2 w2 = *reinterpret_cast<const float2 *>(&ws[st][k8 + i][2 * ep]);
+                acc0 = __fmaf_rn(xf, w2.x, acc0);
+                acc1 = __fmaf_rn(xf, w2.y, acc1);
+            }
+        }
+        __syncwarp();
     }
-    const int t = t0 + tt, e = e0 + te;
-    if (t < T && e < E)
-        scores[(size_t)t * E + e] = router_sigmoid(acc);
+    const int t = t0 + tt, e = e0 + 2 * ep;
+    if (t < T) {
+        if (e < E)
+            scores[(size_t)t * E + e] = router_sigmoid(acc0);
+        if (e + 1 < E)
+            scores[(size_t)t * E + e + 1] = router_sigmoid(acc1);
+    }
 }
 
 // One warp per token.  Lane l holds the scores of experts l, l+32, ...
@@ -426,7 +448,7 @@ cudaError_t launch_router_scores(const uint16_t *x, const float *wr, int T, int 
         router_scores_large<4><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
     } else {
         dim3 grid((T + kSTM - 1) / kSTM, (E + kSTE - 1) / kSTE);
-        router_scores_small<<<grid, 128, 0, s>>>(x, wr, T, H, E, scores, status);
+        router_scores_small<<<grid, 32, 0, s>>>(x, wr, T, H, E, scores, status);
     }
     stage_end(kStRouter, s);
     return cudaGetLastError();

@@ -21,6 +21,9 @@ SMALL = {
     "medium": synth.LayerShape(T=3001, H=512, I=384, E=64, G=8, topk_groups=4, top_k=8),
     "wide_groups": synth.LayerShape(T=777, H=256, I=256, E=96, G=4, topk_groups=2, top_k=6,
                                     scale=1.5),
+    # decode-size router with E % 8 == 4 (a half-empty last expert group) and a
+    # ragged last token group
+    "e36_T50": synth.LayerShape(T=50, H=256, I=128, E=36, G=4, topk_groups=2, top_k=4),
 }
 
 
