@@ -246,6 +246,34 @@ rows_kernel(const int32_t *__restrict__ ids, const int32_t *__restrict__ local_r
     row_of[i] = offsets[e] + cta_base[(size_t)(t / kHistTokens) * E + e] + local_rank[i];
 }
 
+// acc[0..7] += w[k] * y[row k][8i .. 8i+8) for k = 0 .. K-1 in ascending
+// order (an FP32 FMA chain per element).  The rows' 16-byte vectors are
+// loaded eight at a time before their FMAs, so a thread waits for one L2
+// round trip per eight rows instead of one per row.
+__device__ __forceinline__ void combine_vec8(const uint16_t *__restrict__ y, const float *ws,
+                                             const int *rs, int K, int H, int i, float (&acc)[8])
+{
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint4 q[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            if (k0 + kk < K)
+                q[kk] = reinterpret_cast<const uint4 *>(y + (size_t)rs[k0 + kk] * H)[i];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            if (k0 + kk < K) {
+                const float wk = ws[k0 + kk];
+                const uint32_t v[4] = {q[kk].x, q[kk].y, q[kk].z, q[kk].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[2 * j] = __fmaf_rn(wk, bf16_bits_to_f32(v[j] & 0xFFFFu), acc[2 * j]);
+                    acc[2 * j + 1] = __fmaf_rn(wk, bf16_bits_to_f32(v[j] >> 16), acc[2 * j + 1]);
+                }
+            }
+        }
+    }
+}
+
 // out[t,:] = bf16( sum_{k=0..K-1} w[t,k] * y[row_of[t,k], :] ), FP32 FMA chain
 // in ascending k over the bf16 expert outputs y.
 __global__ void __launch_bounds__(256)
@@ -266,16 +294,7 @@ combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ w,
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             acc[j] = 0.0f;
-        for (int k = 0; k < K; ++k) {
-            const uint4 q = reinterpret_cast<const uint4 *>(y + (size_t)rs[k] * H)[i];
-            const uint32_t v[4] = {q.x, q.y, q.z, q.w};
-            const float wk = ws[k];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                acc[2 * j] = __fmaf_rn(wk, bf16_bits_to_f32(v[j] & 0xFFFFu), acc[2 * j]);
-                acc[2 * j + 1] = __fmaf_rn(wk, bf16_bits_to_f32(v[j] >> 16), acc[2 * j + 1]);
-            }
-        }
+        combine_vec8(y, ws, rs, K, H, i, acc);
         uint4 o;
         o.x = pack_bf16x2(acc[0], acc[1]);
         o.y = pack_bf16x2(acc[2], acc[3]);
@@ -501,16 +520,7 @@ combine_block_kernel(const uint16_t *__restrict__ y, const float *__restrict__ w
         for (int j = 0; j < 8; ++j)
             o[c][j] = 0.0f;
         if (i < nvec) {
-            for (int k = 0; k < K; ++k) {
-                const uint4 q = reinterpret_cast<const uint4 *>(y + (size_t)rs[k] * H)[i];
-                const uint32_t v[4] = {q.x, q.y, q.z, q.w};
-                const float wk = ws[k];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    o[c][2 * j] = __fmaf_rn(wk, bf16_bits_to_f32(v[j] & 0xFFFFu), o[c][2 * j]);
-                    o[c][2 * j + 1] = __fmaf_rn(wk, bf16_bits_to_f32(v[j] >> 16), o[c][2 * j + 1]);
-                }
-            }
+            combine_vec8(y, ws, rs, K, H, i, o[c]);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const float p = __fmul_rn(o[c][j], o[c][j]);
