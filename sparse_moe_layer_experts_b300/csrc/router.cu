@@ -365,7 +365,31 @@ select_kernel(const float *__restrict__ scores, int T, int E, int G, int TG, int
 
     // group score: the two largest scores of the group, summed in FP32
     float gs = -INFINITY;
-    if (lane < G) {
+    if ((32 % gsize) == 0) {
+        // groups are aligned runs of gsize lanes within each 32-expert row:
+        // reduce (largest, second largest) pairs across the run with xor
+        // shuffles, then lane g fetches group g's pair
+        float gsum[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float m1 = v[j], m2 = -INFINITY;
+            for (int off = 1; off < gsize; off <<= 1) {
+                const float o1 = __shfl_xor_sync(full, m1, off);
+                const float o2 = __shfl_xor_sync(full, m2, off);
+                const float lo = fminf(m1, o1);
+                m1 = fmaxf(m1, o1);
+                m2 = fmaxf(lo, fmaxf(m2, o2));
+            }
+            gsum[j] = (gsize == 1) ? m1 : __fadd_rn(m1, m2);
+        }
+        const int src = (lane * gsize) & 31, row = (lane * gsize) >> 5;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float o = __shfl_sync(full, gsum[j], src);
+            if (lane < G && row == j)
+                gs = o;
+        }
+    } else if (lane < G) {
         float m1 = -INFINITY, m2 = -INFINITY;
         for (int j = 0; j < gsize; ++j) {
             const float q = row_s[warp][lane * gsize + j];
@@ -387,8 +411,18 @@ select_kernel(const float *__restrict__ scores, int T, int E, int G, int TG, int
     }
     const unsigned kept = __ballot_sync(full, lane < G && rank < TG);
 
-    // top-K among the kept groups' experts by repeated warp arg-max
-    unsigned taken = 0;
+    // top-K among the kept groups' experts by repeated warp arg-max under
+    // (score desc, index asc): each lane's best candidate becomes a 32-bit
+    // key (the bits of a score >= +0 order like the score; +1 keeps 0 for
+    // "none", and a NaN score is never a candidate), a warp max picks the
+    // score and a warp min over the lanes holding it picks the lowest index
+    unsigned cand = 0;  // bit j: expert lane + 32j is in a kept group and not yet taken
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && ((kept >> (e / gsize)) & 1u))
+            cand |= 1u << j;
+    }
     int my_e = -1;
     float my_v = 0.0f;
     for (int k = 0; k < K; ++k) {
@@ -397,28 +431,22 @@ select_kernel(const float *__restrict__ scores, int T, int E, int G, int TG, int
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int e = lane + 32 * j;
-            if (e < E && ((kept >> (e / gsize)) & 1u) && !((taken >> j) & 1u) &&
-                (v[j] > bv || (v[j] == bv && e < be))) {
+            if (((cand >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
                 bv = v[j];
                 be = e;
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(full, bv, off);
-            const int oe = __shfl_xor_sync(full, be, off);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if (be == 0x7FFFFFFF) {  // no candidate left (non-finite scores)
+        const unsigned key = (be != 0x7FFFFFFF && bv >= 0.0f) ? __float_as_uint(bv) + 1u : 0u;
+        const unsigned best = __reduce_max_sync(full, key);
+        be = (int)__reduce_min_sync(full, (key == best && best != 0u) ? (unsigned)be : 0xFFFFFFFFu);
+        bv = __uint_as_float(best - 1u);
+        if (best == 0u) {  // no candidate left (non-finite scores)
             if (lane == 0)
                 atomicOr(status, kStatusDevice);
             be = 0;
             bv = 0.0f;
         } else if ((be & 31) == lane) {
-            taken |= 1u << (be >> 5);
+            cand &= ~(1u << (be >> 5));
         }
         if (lane == k) {
             my_e = be;
