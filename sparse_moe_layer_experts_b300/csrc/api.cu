@@ -237,16 +237,15 @@ int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cf
 {
     void *ws = c.workspace;
     int *status = at<int>(ws, L.status);
-    const int n_cta = (int)((T + kHistTokens - 1) / kHistTokens);
     BEAM_CUDA(launch_router_scores(static_cast<const uint16_t *>(x), router_w, (int)T, c.hidden,
                                    c.n_experts, scores, status, s));
     BEAM_CUDA(launch_select(scores, (int)T, c.n_experts, c.n_groups, c.topk_groups, c.top_k,
                             c.routed_scale, ids, wts, status, s));
-    BEAM_CUDA(launch_hist(ids, (int)T, c.top_k, c.n_experts, at<int32_t>(ws, L.local_rank),
-                          at<int32_t>(ws, L.cta_counts), status, s));
-    BEAM_CUDA(launch_scan(at<int32_t>(ws, L.cta_counts), n_cta, c.n_experts, rows_per_chunk,
-                          at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.counts),
-                          at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start), s));
+    BEAM_CUDA(launch_hist_scan(ids, (int)T, c.top_k, c.n_experts, rows_per_chunk,
+                               at<int32_t>(ws, L.local_rank), at<int32_t>(ws, L.cta_counts),
+                               at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.counts),
+                               at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.chunk_start), status,
+                               s));
     return BEAM_MOE_OK;
 }
 

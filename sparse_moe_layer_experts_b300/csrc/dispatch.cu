@@ -15,53 +15,6 @@ namespace beam {
 
 namespace {
 
-// CTA = 8 warps = 256 tokens.  mask[w][e] has bit l set when token
-// (warp w, lane l) routes to expert e; a pair's rank inside its expert and
-// CTA is the number of earlier tokens (lower warp, or lower lane in the same
-// warp) with that expert.
-__global__ void __launch_bounds__(256)
-hist_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int32_t *__restrict__ local_rank,
-            int32_t *__restrict__ cta_counts, int *status)
-{
-    __shared__ uint32_t mask[8][256];
-    __shared__ int32_t prefix[8][256];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int i = tid; i < 8 * 256; i += 256)
-        (&mask[0][0])[i] = 0u;
-    __syncthreads();
-    const int t = blockIdx.x * kHistTokens + tid;
-    if (t < T) {
-        for (int k = 0; k < K; ++k) {
-            const int e = ids[(size_t)t * K + k];
-            if (e < 0 || e >= E) {
-                atomicOr(status, kStatusDevice);
-                continue;
-            }
-            atomicOr(&mask[warp][e], 1u << lane);
-        }
-    }
-    __syncthreads();
-    if (tid < E) {
-        int run = 0;
-        for (int w = 0; w < 8; ++w) {
-            prefix[w][tid] = run;
-            run += __popc(mask[w][tid]);
-        }
-        cta_counts[(size_t)blockIdx.x * E + tid] = run;
-    }
-    __syncthreads();
-    if (t < T) {
-        const uint32_t below = (1u << lane) - 1u;
-        for (int k = 0; k < K; ++k) {
-            const int e = ids[(size_t)t * K + k];
-            int r = 0;
-            if (e >= 0 && e < E)
-                r = prefix[warp][e] + __popc(mask[warp][e] & below);
-            local_rank[(size_t)t * K + k] = r;
-        }
-    }
-}
-
 // Exclusive scan over the E (<= 256) values held one per thread.
 __device__ int block_exclusive_scan_256(int v, int *tmp, int *total)
 {
@@ -80,6 +33,87 @@ __device__ int block_exclusive_scan_256(int v, int *tmp, int *total)
     return incl - v;
 }
 
+// Expert e's row count `run` (thread e) -> counts, offsets (exclusive
+// scan, offsets[E] = total) and chunk_start (exclusive scan of the chunks of
+// chunk_rows rows per expert).  All 256 threads call it.
+__device__ void scan_experts(int run, int E, int chunk_rows, int32_t *__restrict__ counts,
+                             int32_t *__restrict__ offsets, int32_t *__restrict__ chunk_start,
+                             int *tmp)
+{
+    const int e = threadIdx.x;
+    if (e < E)
+        counts[e] = run;
+    int total = 0;
+    const int off = block_exclusive_scan_256(e < E ? run : 0, tmp, &total);
+    if (e < E)
+        offsets[e] = off;
+    if (e == 0)
+        offsets[E] = total;
+    const int nchunk = (e < E) ? (run + chunk_rows - 1) / chunk_rows : 0;
+    int total_chunks = 0;
+    const int cs = block_exclusive_scan_256(nchunk, tmp, &total_chunks);
+    if (e < E)
+        chunk_start[e] = cs;
+    if (e == 0)
+        chunk_start[E] = total_chunks;
+}
+
+// CTA = 8 warps = 256 tokens.  mask[w][e] has bit l set when token
+// (warp w, lane l) routes to expert e; a pair's rank inside its expert and
+// CTA is the number of earlier tokens (lower warp, or lower lane in the same
+// warp) with that expert.
+__global__ void __launch_bounds__(256)
+hist_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int32_t *__restrict__ local_rank,
+            int32_t *__restrict__ cta_counts, int *status, int chunk_rows,
+            int32_t *__restrict__ cta_base, int32_t *__restrict__ counts,
+            int32_t *__restrict__ offsets, int32_t *__restrict__ chunk_start)
+{
+    __shared__ uint32_t mask[8][256];
+    __shared__ int32_t prefix[8][256];
+    __shared__ int tmp[256];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < 8 * 256; i += 256)
+        (&mask[0][0])[i] = 0u;
+    __syncthreads();
+    const int t = blockIdx.x * kHistTokens + tid;
+    if (t < T) {
+        for (int k = 0; k < K; ++k) {
+            const int e = ids[(size_t)t * K + k];
+            if (e < 0 || e >= E) {
+                atomicOr(status, kStatusDevice);
+                continue;
+            }
+            atomicOr(&mask[warp][e], 1u << lane);
+        }
+    }
+    __syncthreads();
+    int run = 0;
+    if (tid < E) {
+        for (int w = 0; w < 8; ++w) {
+            prefix[w][tid] = run;
+            run += __popc(mask[w][tid]);
+        }
+        cta_counts[(size_t)blockIdx.x * E + tid] = run;
+    }
+    if (gridDim.x == 1) {
+        // one histogram CTA (T <= 256 tokens): it also does the scan
+        if (tid < E)
+            cta_base[tid] = 0;
+        scan_experts(run, E, chunk_rows, counts, offsets, chunk_start, tmp);
+    }
+    __syncthreads();
+    if (t < T) {
+        const uint32_t below = (1u << lane) - 1u;
+        for (int k = 0; k < K; ++k) {
+            const int e = ids[(size_t)t * K + k];
+            int r = 0;
+            if (e >= 0 && e < E)
+                r = prefix[warp][e] + __popc(mask[warp][e] & below);
+            local_rank[(size_t)t * K + k] = r;
+        }
+    }
+}
+
 // One CTA of 256 threads, thread e owns expert e.
 __global__ void __launch_bounds__(256)
 scan_kernel(const int32_t *__restrict__ cta_counts, int n_cta, int E, int chunk_rows,
@@ -95,21 +129,8 @@ scan_kernel(const int32_t *__restrict__ cta_counts, int n_cta, int E, int chunk_
             cta_base[(size_t)c * E + e] = run;
             run += v;
         }
-        counts[e] = run;
     }
-    int total = 0;
-    const int off = block_exclusive_scan_256(e < E ? run : 0, tmp, &total);
-    if (e < E)
-        offsets[e] = off;
-    if (e == 0)
-        offsets[E] = total;
-    const int nchunk = (e < E) ? (run + chunk_rows - 1) / chunk_rows : 0;
-    int total_chunks = 0;
-    const int cs = block_exclusive_scan_256(nchunk, tmp, &total_chunks);
-    if (e < E)
-        chunk_start[e] = cs;
-    if (e == 0)
-        chunk_start[E] = total_chunks;
+    scan_experts(run, E, chunk_rows, counts, offsets, chunk_start, tmp);
 }
 
 // CTA per token: place the token's K rows, then read the token's activations
@@ -570,20 +591,19 @@ __global__ void dense_setup_kernel(int T, int chunk_rows, int32_t *__restrict__ 
 }
 }  // namespace
 
-cudaError_t launch_hist(const int32_t *ids, int T, int K, int E, int32_t *local_rank,
-                        int32_t *cta_counts, int *status, cudaStream_t s)
+cudaError_t launch_hist_scan(const int32_t *ids, int T, int K, int E, int chunk_rows,
+                             int32_t *local_rank, int32_t *cta_counts, int32_t *cta_base,
+                             int32_t *counts, int32_t *offsets, int32_t *chunk_start, int *status,
+                             cudaStream_t s)
 {
+    const int n_cta = (T + kHistTokens - 1) / kHistTokens;
     stage_begin(kStHist, s);
-    hist_kernel<<<(T + kHistTokens - 1) / kHistTokens, 256, 0, s>>>(ids, T, K, E, local_rank,
-                                                                    cta_counts, status);
+    hist_kernel<<<n_cta, 256, 0, s>>>(ids, T, K, E, local_rank, cta_counts, status, chunk_rows,
+                                      cta_base, counts, offsets, chunk_start);
     stage_end(kStHist, s);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_scan(const int32_t *cta_counts, int n_cta, int E, int chunk_rows,
-                        int32_t *cta_base, int32_t *counts, int32_t *offsets,
-                        int32_t *chunk_start, cudaStream_t s)
-{
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || n_cta == 1)  // one CTA did the scan as well
+        return e;
     stage_begin(kStScan, s);
     scan_kernel<<<1, 256, 0, s>>>(cta_counts, n_cta, E, chunk_rows, cta_base, counts, offsets,
                                   chunk_start);

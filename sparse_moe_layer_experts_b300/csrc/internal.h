@@ -39,12 +39,14 @@ cudaError_t launch_select(const float *scores, int T, int E, int G, int TG, int 
 
 // ---- dispatch.cu
 constexpr int kHistTokens = 256;  // tokens per histogram CTA
-cudaError_t launch_hist(const int32_t *ids, int T, int K, int E, int32_t *local_rank,
-                        int32_t *cta_counts, int *status, cudaStream_t s);
-// offsets, counts, cta_base, and the token chunks of chunk_rows rows per expert
-cudaError_t launch_scan(const int32_t *cta_counts, int n_cta, int E, int chunk_rows,
-                        int32_t *cta_base, int32_t *counts, int32_t *offsets,
-                        int32_t *chunk_start, cudaStream_t s);
+// Per-CTA histograms (local_rank, cta_counts), then the scan over experts:
+// cta_base, counts, offsets and the token chunks of chunk_rows rows per
+// expert (chunk_start).  With one histogram CTA (T <= 256) that CTA does the
+// scan too and the scan kernel is not launched.
+cudaError_t launch_hist_scan(const int32_t *ids, int T, int K, int E, int chunk_rows,
+                             int32_t *local_rank, int32_t *cta_counts, int32_t *cta_base,
+                             int32_t *counts, int32_t *offsets, int32_t *chunk_start, int *status,
+                             cudaStream_t s);
 cudaError_t launch_permute(const uint16_t *x, const int32_t *ids, const int32_t *local_rank,
                            const int32_t *cta_base, const int32_t *offsets, int T, int K, int E,
                            int H, int32_t *row_of, int32_t *row_src, void *x_perm,
