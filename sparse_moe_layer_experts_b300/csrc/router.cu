@@ -125,8 +125,8 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Large batches: register-tiled FP32 GEMM, 16x16 threads, R x R outputs per
-// thread (CTA tile 16R tokens x 16R experts), K chunks of 16 double-buffered
+// Large batches: register-tiled FP32 GEMM, 16x16 threads, RM x RE outputs per
+// thread (CTA tile 16RM tokens x 16RE experts), K chunks of 16 double-buffered
 // in shared memory.  The next chunk of router weights streams in by cp.async
 // and the next x chunk through registers (bf16 -> FP32); inside a chunk the
 // fragments of step k+1 are loaded while step k's FMAs issue.  Every
@@ -134,13 +134,33 @@ __device__ __forceinline__ void cp_async_wait()
 // result.
 constexpr int kLKC = 16;
 
-template <int R>
+// Q consecutive floats (Q = 4: one 16-byte load, Q = 2: one 8-byte load)
+template <int Q>
+__device__ __forceinline__ void load_quad_or_pair(const float *p, float *dst)
+{
+    if constexpr (Q == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(p);
+        dst[0] = v.x;
+        dst[1] = v.y;
+        dst[2] = v.z;
+        dst[3] = v.w;
+    } else {
+        const float2 v = *reinterpret_cast<const float2 *>(p);
+        dst[0] = v.x;
+        dst[1] = v.y;
+    }
+}
+
+template <int RM, int RE>
 __global__ void __launch_bounds__(256, 2)
 router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H,
                     int E, float *__restrict__ scores, int *status)
 {
-    constexpr int TM = 16 * R, TE = 16 * R, HALF = TM / 2, Q = R / 2;
-    static_assert(R == 4 || R == 8, "thread tile");
+    // a thread's RM tokens (and RE experts) sit in two halves of the tile,
+    // QM (QE) consecutive in each
+    constexpr int TM = 16 * RM, TE = 16 * RE, HM = TM / 2, HE = TE / 2, QM = RM / 2,
+                  QE = RE / 2;
+    static_assert((RM == 4 || RM == 8) && (RE == 4 || RE == 8), "thread tile");
     if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
         *status = 0;
     __shared__ __align__(16) float xs[2][kLKC][TM + 4];
@@ -186,11 +206,11 @@ router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    float acc[R][R];
+    float acc[RM][RE];
 #pragma unroll
-    for (int i = 0; i < R; ++i)
+    for (int i = 0; i < RM; ++i)
 #pragma unroll
-        for (int j = 0; j < R; ++j)
+        for (int j = 0; j < RE; ++j)
             acc[i][j] = 0.0f;
     const int nk = H / kLKC;
     wasync(0, 0);
@@ -204,31 +224,12 @@ router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr
             wasync(b ^ 1, (kc + 1) * kLKC);
             xload((kc + 1) * kLKC);
         }
-        float a[2][R], bb[2][R];
+        float a[2][RM], bb[2][RE];
         auto frag = [&](int s, int k) {
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-                const float *ap = &xs[b][k][h2 * HALF + ty * Q];
-                const float *bp = &ws[b][k][h2 * HALF + tx * Q];
-                if constexpr (Q == 4) {
-                    const float4 av = *reinterpret_cast<const float4 *>(ap);
-                    const float4 bv = *reinterpret_cast<const float4 *>(bp);
-                    a[s][h2 * 4] = av.x;
-                    a[s][h2 * 4 + 1] = av.y;
-                    a[s][h2 * 4 + 2] = av.z;
-                    a[s][h2 * 4 + 3] = av.w;
-                    bb[s][h2 * 4] = bv.x;
-                    bb[s][h2 * 4 + 1] = bv.y;
-                    bb[s][h2 * 4 + 2] = bv.z;
-                    bb[s][h2 * 4 + 3] = bv.w;
-                } else {
-                    const float2 av = *reinterpret_cast<const float2 *>(ap);
-                    const float2 bv = *reinterpret_cast<const float2 *>(bp);
-                    a[s][h2 * 2] = av.x;
-                    a[s][h2 * 2 + 1] = av.y;
-                    bb[s][h2 * 2] = bv.x;
-                    bb[s][h2 * 2 + 1] = bv.y;
-                }
+                load_quad_or_pair<QM>(&xs[b][k][h2 * HM + ty * QM], &a[s][h2 * QM]);
+                load_quad_or_pair<QE>(&ws[b][k][h2 * HE + tx * QE], &bb[s][h2 * QE]);
             }
         };
         frag(0, 0);
@@ -237,9 +238,9 @@ router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr
             if (k + 1 < kLKC)
                 frag((k + 1) & 1, k + 1);
 #pragma unroll
-            for (int i = 0; i < R; ++i)
+            for (int i = 0; i < RM; ++i)
 #pragma unroll
-                for (int j = 0; j < R; ++j)
+                for (int j = 0; j < RE; ++j)
                     acc[i][j] = __fmaf_rn(a[k & 1][i], bb[k & 1][j], acc[i][j]);
         }
         if (kc + 1 < nk) {
@@ -249,13 +250,13 @@ router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr
         __syncthreads();
     }
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-        const int t = t0 + (i / Q) * HALF + ty * Q + (i % Q);
+    for (int i = 0; i < RM; ++i) {
+        const int t = t0 + (i / QM) * HM + ty * QM + (i % QM);
         if (t >= T)
             continue;
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-            const int e = e0 + (j / Q) * HALF + tx * Q + (j % Q);
+        for (int j = 0; j < RE; ++j) {
+            const int e = e0 + (j / QE) * HE + tx * QE + (j % QE);
             if (e < E)
                 scores[(size_t)t * E + e] = router_sigmoid(acc[i][j]);
         }
@@ -468,12 +469,19 @@ cudaError_t launch_router_scores(const uint16_t *x, const float *wr, int T, int 
                                  float *scores, int *status, cudaStream_t s)
 {
     stage_begin(kStRouter, s);
-    if (T >= 8192) {
+    // CTA tiles: 128 x 128 from T = 16384; 128 tokens x 64 experts from
+    // T = 8192 (twice the CTAs of the square tile: 0.58 -> 0.53 ms at
+    // T = 8192); 64 x 64 below (at T = 4096 the 128 x 64 tile leaves too few
+    // CTAs and measured slower)
+    if (T >= 16384) {
         dim3 grid((T + 127) / 128, (E + 127) / 128);
-        router_scores_large<8><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
+        router_scores_large<8, 8><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
+    } else if (T >= 8192) {
+        dim3 grid((T + 127) / 128, (E + 63) / 64);
+        router_scores_large<8, 4><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
     } else if (T >= 128) {
         dim3 grid((T + 63) / 64, (E + 63) / 64);
-        router_scores_large<4><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
+        router_scores_large<4, 4><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
     } else {
         dim3 grid((T + kSTM - 1) / kSTM, (E + kSTE - 1) / kSTE);
         router_scores_small<<<grid, 32, 0, s>>>(x, wr, T, H, E, scores, status);
