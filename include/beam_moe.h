@@ -34,7 +34,8 @@
  *    return before anything is enqueued.
  *  - Device-detected errors (a bounded wait that ran out, a failed debug
  *    check) are written to a status word inside the workspace; read it with
- *    beam_moe_read_status().
+ *    beam_moe_read_status() before the next call on that workspace, whose
+ *    first kernel clears it.
  *  - bf16 tensors are IEEE bfloat16, row-major, densely packed.
  *  - All device pointers must be 16-byte aligned.
  *  - Calls that share a workspace must not overlap on the GPU; calls with
@@ -190,11 +191,16 @@ size_t beam_moe_hostio_extra_bytes(int64_t T, const beam_moe_cfg *cfg);
  *    Beam sizes: T <= 122 tokens); larger calls return BEAM_MOE_ERR_WORKSPACE
  *    with nothing enqueued.  Invalid configurations return
  *    BEAM_MOE_ERR_INVALID_ARG; T = 0 returns BEAM_MOE_OK.
- *  - Memory: every GPU on which this entry point runs keeps the 24 MiB array
- *    until the process exits.
- *  - Set-up: the first call on each device looks up the array's device
- *    address (cudaGetSymbolAddress) with that device current; make that
- *    first call before any stream capture.
+ *  - Memory: the array sits in its own CUDA module.  Under lazy module
+ *    loading (the CUDA default) a GPU holds the 24 MiB from the first call
+ *    of this entry point on it until the process exits; under eager loading
+ *    (CUDA_MODULE_LOADING=EAGER) every GPU on which the process creates a
+ *    context holds it, even if this entry point is never called.
+ *  - Set-up: the first call in each CUDA context (each device's primary
+ *    context, and any context the caller makes current) looks up the
+ *    array's device address (cudaGetSymbolAddress) with that context
+ *    current and caches it under the context's id; make that first call
+ *    before any stream capture.
  *  - Sharing: all calls share the one array and each call overwrites it, so
  *    calls that overlap on the GPU race; serialise them.  The device status
  *    word lives in the shared array and is not readable through
@@ -323,6 +329,10 @@ int beam_moe_quantize_act(int wtype, const float *x, int64_t rows,
  * Synchronise `stream`, read the device status word of cfg->workspace and
  * clear it.  Returns BEAM_MOE_OK, BEAM_MOE_ERR_TIMEOUT or BEAM_MOE_ERR_DEVICE
  * (or BEAM_MOE_ERR_CUDA if the synchronisation itself failed).
+ * The status word is not sticky across calls: the first kernel of every
+ * call that uses the workspace (route, forward, block, dense) clears it, so
+ * a caller that wants a call's status must read it after that call and
+ * before enqueueing the next call on the same workspace.
  */
 int beam_moe_read_status(const beam_moe_cfg *cfg, void *stream);
 

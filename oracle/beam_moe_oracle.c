@@ -32,7 +32,7 @@
  *            "Architecture and memory efficiency": the same routing restated;
  *            FP32 pins restated in the section on residual-stream design.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *  - router logits: l[t,e] = sum_h x[t,h]*Wr[h,e], FP32 fused multiply-add in
  *    ascending h, starting from +0.0f.
  *  - sigmoid: s = 1/(1+E) in FP32 where E is exp(-l) rounded to FP32 (computed

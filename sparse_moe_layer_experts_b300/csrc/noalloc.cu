@@ -9,13 +9,19 @@
 // This entry point keeps its scratch in a fixed array compiled into the
 // library, so it allocates nothing at call time.
 //
-// Cost and limits: every GPU on which this entry point runs holds the array
-// (kNoAllocScratchBytes) until the process exits.  A call is rejected when
-// the layer's workspace for T tokens exceeds the array.  All calls share the
-// one array, so calls that overlap on the GPU (different streams, different
-// host threads) race; serialise them.
+// Cost and limits: the array (kNoAllocScratchBytes) lives in this file's own
+// CUDA module.  Under lazy module loading (the CUDA default) a device holds
+// it from the first call of this entry point on that device until the
+// process exits; under eager loading (CUDA_MODULE_LOADING=EAGER) every
+// device on which the process creates a context holds it, whether or not the
+// entry point is called.  A call is rejected when the layer's workspace for
+// T tokens exceeds the array.  All calls share the one array, so calls that
+// overlap on the GPU (different streams, different host threads) race;
+// serialise them.
 #include "../../include/beam_moe.h"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -23,30 +29,81 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(24) << 20;  // 24 MiB
-constexpr int kMaxDevices = 64;
+constexpr int kCacheSlots = 64;
 
 // The shared scratch.  In host code this name is only a host-side stand-in:
-// its device address comes from cudaGetSymbolAddress, once per device.
+// its device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices];
+// Device addresses of the array, one per CUDA context that has called this
+// entry point.  The key is the driver's context id, which is unique for the
+// life of the process: a context created after cudaDeviceReset, or a
+// non-primary context made current by the caller, gets an id of its own and
+// so a fresh lookup, never a stale address.
+struct Slot {
+    unsigned long long ctx_id;
+    void *addr;
+};
 
-// Device address of the scratch on the current device (looked up on the
-// first call per device, with that device current).
+std::mutex g_mu;
+Slot g_slots[kCacheSlots];
+int g_next_slot = 0;
+
+PFN_cuCtxGetCurrent_v4000 g_get_current = nullptr;
+PFN_cuCtxGetId_v12000 g_get_id = nullptr;
+
+bool driver_entry_points()
+{
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    return g_get_current && g_get_id;
+}
+
+// Device address of the scratch in the current context.  The first call in
+// a context looks it up (cudaGetSymbolAddress, with that context current);
+// later calls in the same context reuse it.
 int scratch_address(void **out)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    if (!driver_entry_points())
         return BEAM_MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
+    CUcontext ctx = nullptr;
+    void *p = nullptr;
+    if (g_get_current(&ctx) != CUDA_SUCCESS)
+        return BEAM_MOE_ERR_CUDA;
+    if (!ctx) {
+        // No context is current on this thread yet: the runtime binds the
+        // current device's primary context on its first call, this lookup.
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
             return BEAM_MOE_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        if (g_get_current(&ctx) != CUDA_SUCCESS || !ctx)
+            return BEAM_MOE_ERR_CUDA;
     }
-    *out = g_scratch_addr[dev];
+    unsigned long long id = 0;
+    if (g_get_id(ctx, &id) != CUDA_SUCCESS)
+        return BEAM_MOE_ERR_CUDA;
+    for (const Slot &s : g_slots)
+        if (s.addr && s.ctx_id == id) {
+            *out = s.addr;
+            return BEAM_MOE_OK;
+        }
+    if (!p && (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p))
+        return BEAM_MOE_ERR_CUDA;
+    g_slots[g_next_slot] = Slot{id, p};
+    g_next_slot = (g_next_slot + 1) % kCacheSlots;
+    *out = p;
     return BEAM_MOE_OK;
 }
 

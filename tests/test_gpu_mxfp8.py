@@ -9,7 +9,8 @@ import torch
 from sparse_moe_layer_experts_b300 import synth
 from sparse_moe_layer_experts_b300.layer import BeamMoE, quantize_mxfp8
 
-from tests._gpu_util import out_bits, rel_l2_per_token, sample_tokens
+from tests._gpu_util import (N_RANDOM_FULL, chunk_rows_of, out_bits, rel_l2_per_token,
+                             sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,8 +66,8 @@ SMALL = {
     "tiny": synth.shape("tiny"),
     "tiny_T200": synth.shape("tiny", T=200),
     "medium": synth.LayerShape(T=1501, H=512, I=384, E=64, G=8, topk_groups=4, top_k=8),
-    # H/128 odd and K = H not a multiple of 256: a short last NVFP4 k-step in
-    # the token-major gate/up, the weight-major MXFP8 down GEMM
+    # H/128 odd: the weight-major MXFP8 down GEMM (the token-major down GEMM
+    # pairs weight tiles, so it needs an even H/128)
     "odd_tiles": synth.LayerShape(T=3001, H=640, I=256, E=32, G=8, topk_groups=4, top_k=8),
 }
 
@@ -98,6 +99,10 @@ def test_mxfp8_deterministic():
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["decode", "prefill"])
 def test_mxfp8_full_size_sampled(oracle_mod, name):
+    """Full-size MXFP8 layer against the oracle with the identical
+    quantisation: routing of every token; outputs of every decode token, and
+    at prefill size of the segment edges of every expert, the chunk edges of
+    the most loaded expert and 256 seeded random tokens."""
     sh = synth.shape(name)
     d = synth.make_inputs(sh, seed=0, device="cuda")
     layer = _layer(sh, d)
@@ -111,9 +116,12 @@ def test_mxfp8_full_size_sampled(oracle_mod, name):
     ids_o, _ = oracle_mod.select(s, sh.G, sh.topk_groups, sh.top_k, sh.scale)
     assert np.array_equal(ids, ids_o)
     _, offsets, _, row_src = oracle_mod.dispatch(ids_o, sh.E)
-    toks = sample_tokens(sh.T, row_src, offsets, n_random=8)[:12]
+    toks = sample_tokens(sh.T, row_src, offsets, n_random=N_RANDOM_FULL,
+                         chunk_rows=chunk_rows_of(sh.T, sh.top_k, sh.E, "mxfp8"))
+    if name == "decode":
+        assert toks == list(range(sh.T))
     q = _oracle_q(oracle_mod, d, experts=np.unique(ids_o[toks]))
     ref, _, _ = oracle_mod.forward_mxfp8(xb, rw, *q, sh.G, sh.topk_groups, sh.top_k, sh.scale,
                                          tokens=toks)
     rel = rel_l2_per_token(out_bits(out)[toks], ref)
-    assert rel.max() <= MXFP8_TOL, (rel.max(), toks[int(rel.argmax())])
+    assert rel.max() <= MXFP8_TOL, (rel.max(), toks[int(rel.argmax())], len(toks))

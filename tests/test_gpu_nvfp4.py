@@ -7,7 +7,8 @@ import torch
 
 from sparse_moe_layer_experts_b300 import synth
 from sparse_moe_layer_experts_b300.layer import BeamMoE, quantize_nvfp4
-from tests._gpu_util import out_bits, rel_l2_per_token, sample_tokens
+from tests._gpu_util import (N_RANDOM_FULL, chunk_rows_of, out_bits, rel_l2_per_token,
+                             sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,8 +73,9 @@ SMALL = {
     "tiny": synth.shape("tiny"),
     "tiny_T200": synth.shape("tiny", T=200),
     "medium": synth.LayerShape(T=1501, H=512, I=384, E=64, G=8, topk_groups=4, top_k=8),
-    # H/128 odd and K = H not a multiple of 256: a short last NVFP4 k-step in
-    # the token-major gate/up, the weight-major MXFP8 down GEMM
+    # H/128 odd and K = H not a multiple of 256: a short last k-step in the
+    # token-major NVFP4 gate/up, and the weight-major NVFP4 down GEMM (the
+    # token-major down GEMM pairs weight tiles, so it needs an even H/128)
     "odd_tiles": synth.LayerShape(T=3001, H=640, I=256, E=32, G=8, topk_groups=4, top_k=8),
 }
 
@@ -105,8 +107,12 @@ def test_nvfp4_deterministic():
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["nvfp4", "decode"])
 def test_nvfp4_full_size_sampled(oracle_mod, name):
-    """Full-size NVFP4 layer in the configuration the benchmark times:
-    sampled tokens against the oracle with the identical quantisation."""
+    """Full-size NVFP4 layer in the configuration the benchmark times, against
+    the oracle with the identical quantisation: routing of every token; layer
+    outputs of every token of the decode batch, and at T=8192 of token 0 and
+    T-1, the first and last row of every non-empty expert segment, the first
+    and last row of every token chunk of the most loaded expert, and 256
+    seeded random tokens."""
     sh = synth.shape(name)
     d = synth.make_inputs(sh, seed=0, device="cuda")
     layer = _nvfp4_layer(sh, d)
@@ -120,9 +126,12 @@ def test_nvfp4_full_size_sampled(oracle_mod, name):
     ids_o, _ = oracle_mod.select(s, sh.G, sh.topk_groups, sh.top_k, sh.scale)
     assert np.array_equal(ids, ids_o)
     _, offsets, _, row_src = oracle_mod.dispatch(ids_o, sh.E)
-    toks = sample_tokens(sh.T, row_src, offsets, n_random=8)[:16]
+    toks = sample_tokens(sh.T, row_src, offsets, n_random=N_RANDOM_FULL,
+                         chunk_rows=chunk_rows_of(sh.T, sh.top_k, sh.E, "nvfp4"))
+    if name == "decode":
+        assert toks == list(range(sh.T))
     q = _oracle_q(oracle_mod, d, experts=np.unique(ids_o[toks]))
     ref, _, _ = oracle_mod.forward_nvfp4(xb, rw, *q, sh.G, sh.topk_groups, sh.top_k, sh.scale,
                                          tokens=toks)
     rel = rel_l2_per_token(out_bits(out)[toks], ref)
-    assert rel.max() <= NVFP4_TOL, (rel.max(), toks[int(rel.argmax())])
+    assert rel.max() <= NVFP4_TOL, (rel.max(), toks[int(rel.argmax())], len(toks))

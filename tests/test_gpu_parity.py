@@ -7,7 +7,8 @@ import torch
 
 from sparse_moe_layer_experts_b300 import synth
 from sparse_moe_layer_experts_b300.layer import BeamMoE
-from tests._gpu_util import REL_L2_TOL, host_inputs, out_bits, rel_l2_per_token, sample_tokens
+from tests._gpu_util import (N_RANDOM_FULL, REL_L2_TOL, chunk_rows_of, host_inputs, out_bits,
+                             rel_l2_per_token, sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -129,8 +130,10 @@ def beam_weights():
 @pytest.mark.parametrize("name", ["decode", "prefill", "skewed", "nvfp4"])
 def test_full_size_route_and_sampled_forward(oracle_mod, beam_weights, name):
     """Full-size workloads in the configuration the benchmark times: every
-    token's routing bit-exact, layer outputs for sampled tokens (first, last,
-    random, and the first/last row of expert segments)."""
+    token's routing bit-exact; layer outputs of every token of the decode
+    batch, and at the larger sizes of token 0 and T-1, the first and last row
+    of every non-empty expert segment, the first and last row of every token
+    chunk of the most loaded expert, and 256 seeded random tokens."""
     sh = synth.shape(name)
     d = synth.make_inputs(sh, seed=0, device="cuda", weights=False)
     d.update(beam_weights)
@@ -140,14 +143,17 @@ def test_full_size_route_and_sampled_forward(oracle_mod, beam_weights, name):
     out = layer.forward(d["x"])
     torch.cuda.synchronize()
     assert layer.status() == 0
-    toks = sample_tokens(sh.T, row_src, offsets, n_random=16)
+    toks = sample_tokens(sh.T, row_src, offsets, n_random=N_RANDOM_FULL,
+                         chunk_rows=chunk_rows_of(sh.T, sh.top_k, sh.E))
+    if name == "decode":
+        assert toks == list(range(sh.T))
     hx = host_inputs(d, experts=np.unique(ids[toks]))
     ref, ref_ids, _ = oracle_mod.forward(hx["x"], hx["router_w"], hx["w_gate"], hx["w_up"],
                                          hx["w_down"], sh.G, sh.topk_groups, sh.top_k, sh.scale,
                                          tokens=toks)
     assert np.array_equal(ref_ids, ids[toks])
     rel = rel_l2_per_token(out_bits(out)[toks], ref)
-    assert rel.max() <= REL_L2_TOL, (rel.max(), toks[int(rel.argmax())])
+    assert rel.max() <= REL_L2_TOL, (rel.max(), toks[int(rel.argmax())], len(toks))
     if name == "skewed":
         # the synthetic Zipf bias makes one expert hot
         assert counts.max() > 4 * counts.mean()

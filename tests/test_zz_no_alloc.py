@@ -39,8 +39,13 @@ def _compare(layer, xs):
         ref = layer.forward(x)                      # caller-allocated workspace
         torch.cuda.synchronize()
         assert layer.status() == 0
-        rel = rel_l2_per_token(out_bits(g), out_bits(ref))
-        assert rel.max() <= REL_L2_TOL, rel.max()
+        # Both entry points run the same deterministic kernels on the same
+        # inputs, so the outputs must agree byte for byte; anything the first
+        # call left in the shared scratch must not change the second.
+        n_diff = int((g.view(torch.int16) != ref.view(torch.int16)).sum())
+        assert n_diff == 0, f"{n_diff} output values differ from beam_moe_forward"
+        # the tolerance of the parity tests holds a fortiori
+        assert rel_l2_per_token(out_bits(g), out_bits(ref)).max() <= REL_L2_TOL
 
 
 @pytest.mark.parametrize("name,T2", [("tiny", 37), ("decode", 32)])
