@@ -6,8 +6,13 @@ down grouped GEMMs, combine) over one batch of T synthetic tokens whose
 activations are already resident in HBM.  The expert weights (20 GB bf16)
 are larger than L2, so no L2 flush is needed between steps.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config all|decode|...]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+The default (--config all) times the decode batch (the headline line) and,
+in the same process with the same resident expert weights, the prefill,
+skewed-routing and NVFP4 workloads, each reported under the line's
+"configs" key with its own clocks, roofline, end-to-end leg and CPU sample.
 
 Multi-GPU (torchrun): every rank runs an independent replica on its own batch
 (the layer is per-token independent; no collective on the data path).
@@ -59,8 +64,11 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="decode",
-                    choices=["tiny", "decode", "prefill", "skewed", "nvfp4", "mxfp8", "dense"])
+    ap.add_argument("--config", default="all",
+                    choices=["all", "tiny", "decode", "prefill", "skewed", "nvfp4", "mxfp8",
+                             "dense"],
+                    help="'all' (default): decode (the headline line) plus prefill, skewed "
+                         "and NVFP4 under the line's 'configs' key, in one process")
     ap.add_argument("--cpu-tokens", type=int, default=16,
                     help="tokens of the batch the CPU oracle baseline computes")
     ap.add_argument("--override", default="",
@@ -70,9 +78,12 @@ def parse_args():
                          "are allocated); prints a diagnostic line, not a bench line")
     ap.add_argument("--block", action="store_true",
                     help="time the fused block (pre-norm, MoE, post-norm, residual at step 9) "
-                         "instead of the bare layer (bf16 configs)")
+                         "instead of the bare layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-library-peaks", action="store_true",
+                    help="skip timing cuBLASLt's FP4/FP8 GEMMs (their peaks then come from the "
+                         "bf16 peak times the nominal ratio)")
     return ap.parse_args()
 
 
@@ -208,8 +219,8 @@ class ClockSampler:
 
 
 KERNEL_SOURCES = {
-    "router_scores": ("router.cu", "common.cuh"),
-    "select": ("router.cu", "common.cuh"),
+    "router_scores": ("router.cu", "router_tc.cu", "router_math.cuh", "common.cuh"),
+    "select": ("router.cu", "router_math.cuh", "common.cuh"),
     "hist": ("dispatch.cu", "common.cuh"),
     "scan": ("dispatch.cu", "common.cuh"),
     "permute": ("dispatch.cu", "common.cuh", "nvfp4.cuh"),
@@ -376,7 +387,8 @@ def run_reference(args, world, rank):
     if args.config == "dense":
         run_reference_dense(args)
         return
-    sh = synth.shape(args.config)
+    name = DEFAULT_SET[0] if args.config == "all" else args.config
+    sh = synth.shape(name)
     # the inputs are drawn exactly as the GPU arm draws them
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     d = synth.make_inputs(sh, seed=0, device=dev, weights=True)
@@ -384,7 +396,7 @@ def run_reference(args, world, rank):
     toks = sorted(np.random.default_rng(0).choice(sh.T, size=ntok, replace=False).tolist())
     host = host_sample(sh, d, toks)
     del d
-    fmt = weight_format(args.config)
+    fmt = weight_format(name)
     q = oracle_quantize_sample(host, fmt)
     times = [oracle_step(sh, host, toks, fmt, q) for _ in range(args.warmup + args.steps)]
     total = sum(times[args.warmup:])
@@ -395,8 +407,9 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32/f64", "data": "synthetic",
-        "config": {"workload": f"{args.config}: T={sh.T} tokens, hidden {sh.H}, "
-                               f"intermediate {sh.I}, {sh.E} experts",
+        "config": {"workload": f"{name}: T={sh.T} tokens, hidden {sh.H}, intermediate {sh.I}, "
+                               f"{sh.E} experts in {sh.G} groups, top-{sh.topk_groups} groups, "
+                               f"top-{sh.top_k}, {fmt} experts",
                    "sample": f"{ntok} seeded tokens of the batch per step"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{ntok} seeded tokens per step, {args.steps} steps"},
@@ -441,47 +454,129 @@ def run_reference_dense(args):
     }), flush=True)
 
 
-def run_ours(args, world, rank, local):
-    import numpy as np
-    import torch
-    from sparse_moe_layer_experts_b300 import binding as B
-    from sparse_moe_layer_experts_b300 import build as build_mod
+# Workloads a default run measures, in this order; the first is the headline
+# (the decode batch, whose step streams the active experts' weights).
+DEFAULT_SET = ("decode", "prefill", "skewed", "nvfp4")
+# the skewed workload's target: the hottest expert takes about 8x the mean load
+SKEW_TARGET = 8.0
+
+
+def make_layer(name, sh, weights, qcache, dev, rank):
+    """Resident layer of one workload (its own router and batch; the expert
+    weights are shared across the Beam-size workloads and quantised once)."""
     from sparse_moe_layer_experts_b300 import synth
     from sparse_moe_layer_experts_b300.layer import BeamMoE, quantize_mxfp8, quantize_nvfp4
-
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
-    build_mod.build()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    sh = synth.shape(args.config, **parse_override(args.override))
-    fmt = weight_format(args.config)
-    nvfp4, mx8 = fmt == "nvfp4", fmt == "mxfp8"
-    d = synth.make_inputs(sh, seed=0, device=dev, weights=True)
+    fmt = weight_format(name)
+    d = synth.make_inputs(sh, seed=0, device=dev, weights=False)
     if rank > 0:  # each replica routes its own batch
         d["x"] = synth.make_inputs(sh, seed=rank, device=dev, weights=False)["x"]
-    if mx8:
-        q = [quantize_mxfp8(d[k]) for k in ("w_gate", "w_up", "w_down")]
-        layer = BeamMoE.mxfp8(d["router_w"], *q, n_groups=sh.G, topk_groups=sh.topk_groups,
-                              top_k=sh.top_k, routed_scale=sh.scale)
-    elif nvfp4:
-        q = [quantize_nvfp4(d[k]) for k in ("w_gate", "w_up", "w_down")]
-        layer = BeamMoE.nvfp4(d["router_w"], *q, n_groups=sh.G, topk_groups=sh.topk_groups,
-                              top_k=sh.top_k, routed_scale=sh.scale)
+    d.update(weights)
+    kw = dict(n_groups=sh.G, topk_groups=sh.topk_groups, top_k=sh.top_k, routed_scale=sh.scale)
+    if fmt == "mxfp8":
+        if "mxfp8" not in qcache:
+            qcache["mxfp8"] = [quantize_mxfp8(weights[k]) for k in ("w_gate", "w_up", "w_down")]
+        layer = BeamMoE.mxfp8(d["router_w"], *qcache["mxfp8"], **kw)
+    elif fmt == "nvfp4":
+        if "nvfp4" not in qcache:
+            qcache["nvfp4"] = [quantize_nvfp4(weights[k]) for k in ("w_gate", "w_up", "w_down")]
+        layer = BeamMoE.nvfp4(d["router_w"], *qcache["nvfp4"], **kw)
     else:
-        layer = BeamMoE(d["router_w"], d["w_gate"], d["w_up"], d["w_down"], n_groups=sh.G,
-                        topk_groups=sh.topk_groups, top_k=sh.top_k, routed_scale=sh.scale)
+        layer = BeamMoE(d["router_w"], weights["w_gate"], weights["w_up"], weights["w_down"], **kw)
+    return layer, d
+
+
+def tensor_peak(fmt, peaks, lib_peaks):
+    """(dense tensor peak in TFLOP/s for the path's MMA type, its source).
+    bf16: the measured cuBLAS rate.  NVFP4 / MXFP8: the cuBLASLt
+    block-scaled GEMM measured in this run when that ran, else the bf16 rate
+    times the nominal dense ratio (13.5/2.25 for FP4, 4.5/2.25 for FP8)."""
+    if fmt == "bf16":
+        return peaks["bf16_tflops"], "measured bf16 cuBLAS GEMM (MEASURED_PEAKS.json)"
+    key = f"{fmt}_tflops"
+    if lib_peaks and lib_peaks.get(key):
+        return lib_peaks[key], (f"measured in this run: cuBLASLt {fmt} block-scaled GEMM "
+                                f"{lib_peaks['shape']} via torch._scaled_mm, best of "
+                                f"{lib_peaks['reps']}")
+    ratio = NVFP4_OVER_BF16 if fmt == "nvfp4" else FP8_OVER_BF16
+    return peaks["bf16_tflops"] * ratio, ("bf16 measured (MEASURED_PEAKS.json) x nominal dense "
+                                          + ("13.5/2.25" if fmt == "nvfp4" else "4.5/2.25"))
+
+
+def measure_library_peaks(dev, reps=20, warm_s=0.5):
+    """Dense FP4 and FP8 tensor peaks of this GPU as the vendor library
+    reaches them: cuBLASLt's block-scaled GEMMs (NVFP4: E2M1 with an E4M3
+    scale per 16; MXFP8: E4M3 with a UE8M0 scale per 32) on 8192^3 through
+    torch._scaled_mm, best of `reps` CUDA-event timings after `warm_s`
+    seconds of back-to-back warm-up calls.  Returns None entries for formats
+    the installed torch cannot run."""
+    import torch
+    M = N = K = 8192
+    out = {"shape": f"{M}x{N}x{K}", "reps": reps, "nvfp4_tflops": None, "mxfp8_tflops": None}
+
+    def best_ms(fn):
+        t_end = time.time() + warm_s
+        while time.time() < t_end:
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = float("inf")
+        for _ in range(reps):
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return best
+
+    flops = 2.0 * M * N * K
+    try:
+        g = torch.Generator(device=dev).manual_seed(0)
+        a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev, generator=g)
+        b = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev, generator=g)
+        one = 0x38  # 1.0 in E4M3
+        sa = torch.full((M, K // 16), one, dtype=torch.uint8, device=dev)
+        sb = torch.full((N, K // 16), one, dtype=torch.uint8, device=dev)
+        a4, b4 = a.view(torch.float4_e2m1fn_x2), b.view(torch.float4_e2m1fn_x2)
+        sa4, sb4 = sa.view(torch.float8_e4m3fn), sb.view(torch.float8_e4m3fn)
+        fn = lambda: torch._scaled_mm(a4, b4.t(), sa4, sb4, out_dtype=torch.bfloat16)
+        out["nvfp4_tflops"] = flops / best_ms(fn) / 1e9
+        del a, b, sa, sb
+    except Exception as ex:  # noqa: BLE001 - reported, not fatal
+        out["nvfp4_error"] = repr(ex)[:200]
+    try:
+        g = torch.Generator(device=dev).manual_seed(1)
+        a = torch.randn(M, K, device=dev, generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn(N, K, device=dev, generator=g).to(torch.float8_e4m3fn)
+        sa = torch.full((M, K // 32), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+        sb = torch.full((N, K // 32), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+        fn = lambda: torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16)
+        out["mxfp8_tflops"] = flops / best_ms(fn) / 1e9
+        del a, b, sa, sb
+    except Exception as ex:  # noqa: BLE001
+        out["mxfp8_error"] = repr(ex)[:200]
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure(name, sh, layer, d, args, world, rank, local, dev, peaks, lib_peaks):
+    """Time one workload: warm-up, K timed steps (device events on the launch
+    stream, per-kernel events through the library's hook, clocks sampled in
+    the region), the host-I/O end-to-end leg, and the roofline figures."""
+    import torch
+    from sparse_moe_layer_experts_b300 import binding as B
+    from sparse_moe_layer_experts_b300 import synth
+    fmt = weight_format(name)
     x = d["x"]
     out = torch.empty_like(x)
     if args.block:
-        if fmt != "bf16":
-            raise SystemExit("--block runs the bf16 configs")
         gp, gq = synth.make_block_gains(sh.H, seed=0, device=dev)
         step_fn = lambda: layer.block_forward(x, BLOCK_STEP, gp, gq, BLOCK_EPS, out=out)
     else:
         step_fn = lambda: layer.forward(x, out)
     r = layer.route(x, want_scores=False)
     counts = r["counts"].cpu().numpy()
+    del r
     n_active = int((counts > 0).sum())
     stream = torch.cuda.current_stream()
 
@@ -489,7 +584,7 @@ def run_ours(args, world, rank, local):
         step_fn()
     torch.cuda.synchronize()
     if layer.status() != 0:
-        raise SystemExit("device status word reports an error during warm-up")
+        raise SystemExit(f"{name}: device status word reports an error during warm-up")
 
     # per-kernel events: one (start, stop) pair per stage per step
     nst = len(B.KERNEL_STAGES)
@@ -519,12 +614,13 @@ def run_ours(args, world, rank, local):
     ms = start.elapsed_time(stop)
     ms_max = max_over_ranks(ms, world, dev)
     if layer.status() != 0:
-        raise SystemExit("device status word reports an error in the timed region")
+        raise SystemExit(f"{name}: device status word reports an error in the timed region")
     # stages the path launched: their events were recorded inside the timed
     # region (the others keep their setup records from before `start`)
     ran = [start.elapsed_time(ev[-1][j][0]) >= 0.0 for j in range(nst)]
-    per_kernel_ms = {name: sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps))
-                     / args.steps for j, name in enumerate(B.KERNEL_STAGES) if ran[j]}
+    per_kernel_ms = {kn: sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps))
+                     / args.steps for j, kn in enumerate(B.KERNEL_STAGES) if ran[j]}
+    del ev
 
     # end to end through the host-I/O entry point (pinned host buffers)
     e2e = None
@@ -549,13 +645,10 @@ def run_ours(args, world, rank, local):
         nbytes = sh.T * sh.H * 2
         e2e = {"value": world * sh.T * args.steps / dt, "unit": UNIT,
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+        del xh, oh
 
     value = world * sh.T * args.steps / (ms_max / 1e3)
-    peaks, peak_src = load_peaks()
-    # tensor peak of the path's MMA type: bf16, or FP4 (measured bf16 x the
-    # nominal fp4/bf16 ratio)
-    t_peak = peaks["bf16_tflops"] * {"bf16": 1.0, "nvfp4": NVFP4_OVER_BF16,
-                                     "mxfp8": FP8_OVER_BF16}[fmt]
+    t_peak, t_peak_src = tensor_peak(fmt, peaks, lib_peaks)
     alg = workload_algorithmic(sh, n_active, fmt)
     dom = max(per_kernel_ms, key=per_kernel_ms.get)
     a = alg[dom]
@@ -566,18 +659,15 @@ def run_ours(args, world, rank, local):
         achieved = a["flops"] / t_dom / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": t_peak,
                 "unit": "TFLOP/s", "frac": achieved / t_peak}
+        roof["peak_source"] = t_peak_src
     else:
         achieved = a["bytes"] / t_dom / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"]}
-    roof["traffic"] = ncu_traffic(dom, args.config)
+        roof["peak_source"] = "measured HBM copy (MEASURED_PEAKS.json)" \
+            if peaks.get("_src") == "measured" else "fallback"
+    roof["traffic"] = ncu_traffic(dom, name)
     roof["kernel"] = dom
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else \
-        "fallback"
-    if nvfp4 and roof["bound"] == "tensor":
-        roof["peak_source"] += ", bf16 x 13.5/2.25 (nominal dense fp4/bf16)"
-    if mx8 and roof["bound"] == "tensor":
-        roof["peak_source"] += ", bf16 x 4.5/2.25 (nominal dense fp8/bf16)"
     roof["algorithmic_bytes_per_launch"] = a["bytes"]
     roof["algorithmic_flops_per_launch"] = a["flops"]
     lay = alg["layer"]
@@ -585,43 +675,95 @@ def run_ours(args, world, rank, local):
     layer_roof = {
         "hbm_frac": lay["bytes"] / t_step / 1e9 / peaks["hbm_gbs"],
         "tensor_frac": lay["flops"] / t_step / 1e12 / t_peak,
+        "tensor_peak": t_peak, "tensor_peak_source": t_peak_src,
         "attainable_frac": max(lay["bytes"] / (peaks["hbm_gbs"] * 1e9),
                                lay["flops"] / (t_peak * 1e12)) / t_step,
     }
+    if fmt == "bf16":
+        sus = peaks.get("bf16_tflops_sustained")
+        if sus:
+            layer_roof["tensor_frac_of_sustained"] = lay["flops"] / t_step / 1e12 / sus
+            layer_roof["attainable_frac_sustained"] = max(
+                lay["bytes"] / (peaks["hbm_gbs"] * 1e9), lay["flops"] / (sus * 1e12)) / t_step
+    elif fmt == "nvfp4":
+        layer_roof["tensor_frac_of_nominal_ratio_peak"] = (
+            lay["flops"] / t_step / 1e12 / (peaks["bf16_tflops"] * NVFP4_OVER_BF16))
 
-    cpu = None
+    load = float(counts.max() / counts.mean())
+    config = {"workload": f"{name}{'(' + args.override + ')' if args.override else ''}: "
+                          f"T={sh.T} tokens, hidden {sh.H}, intermediate {sh.I}, {sh.E} experts "
+                          f"in {sh.G} groups, top-{sh.topk_groups} groups, top-{sh.top_k}, "
+                          f"{fmt} experts"
+                          + (f"; fused block: RMS pre-norm, the layer, RMS post-norm, "
+                             f"residual step {BLOCK_STEP}" if args.block else ""),
+              "tokens_per_step_per_gpu": sh.T, "active_experts": n_active,
+              "max_expert_load_over_mean": load,
+              "l2": "no flush: expert weights read per step exceed the 126 MB L2",
+              "parallelism": f"replicas x{world}"}
+    if sh.routing == "zipf":
+        config["skew_target_load_over_mean"] = SKEW_TARGET
+    res = {"value": value, "unit": UNIT, "ms_per_step": ms_max / args.steps,
+           "dtype": DTYPES[fmt], "config": config, "roofline": roof,
+           "layer_roofline": layer_roof, "kernels_ms": per_kernel_ms, "e2e": e2e,
+           "gpu_launches": launches, "clocks": clk.summary()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, n, dt = cpu_oracle_run(sh, d, args.cpu_tokens, fmt=fmt)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{n} seeded tokens of the {args.config} batch ({dt:.1f} s)"}
+        res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": f"{n} seeded tokens of the {name} batch ({dt:.1f} s)"}
+    else:
+        res["cpu_baseline"] = None
+    return res
+
+
+DTYPES = {"bf16": "bf16",
+          "nvfp4": "nvfp4 weights+activations, fp4 MMA (kind::mxf4nvf4), f32 accumulate",
+          "mxfp8": "mxfp8 weights+activations, fp8 MMA (kind::mxf8f6f4), f32 accumulate"}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from sparse_moe_layer_experts_b300 import build as build_mod
+    from sparse_moe_layer_experts_b300 import synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    build_mod.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    names = list(DEFAULT_SET) if args.config == "all" else [args.config]
+    shapes = {n: synth.shape(n, **parse_override(args.override)) for n in names}
+    sh0 = shapes[names[0]]
+    weights = synth.make_inputs(sh0, seed=0, device=dev, weights=True)
+    weights = {k: weights[k] for k in ("w_gate", "w_up", "w_down")}
+    peaks, peak_src = load_peaks()
+    peaks["_src"] = peak_src
+    lib_peaks = None
+    if any(weight_format(n) != "bf16" for n in names) and not args.no_library_peaks:
+        lib_peaks = measure_library_peaks(dev)
+    qcache = {}
+    results = {}
+    for n in names:
+        sh = shapes[n]
+        assert (sh.H, sh.I, sh.E) == (sh0.H, sh0.I, sh0.E), "workloads share the expert weights"
+        layer, d = make_layer(n, sh, weights, qcache, dev, rank)
+        results[n] = measure(n, sh, layer, d, args, world, rank, local, dev, peaks, lib_peaks)
+        del layer, d
+        torch.cuda.empty_cache()
 
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"bf16": "bf16",
-                      "nvfp4": "nvfp4 weights+activations, fp4 MMA (kind::mxf4nvf4), f32 accumulate",
-                      "mxfp8": "mxfp8 weights+activations, fp8 MMA (kind::mxf8f6f4), f32 accumulate"
-                      }[fmt],
-            "data": "synthetic (seeded N(0,1) activations, N(0,0.02) bf16 weights)",
-            "config": {"workload": f"{args.config}{'(' + args.override + ')' if args.override else ''}: T={sh.T} tokens, hidden {sh.H}, "
-                                   f"intermediate {sh.I}, {sh.E} experts in {sh.G} groups, "
-                                   f"top-{sh.topk_groups} groups, top-{sh.top_k}"
-                                   + (f"; fused block: RMS pre-norm, the layer, RMS post-norm, "
-                                      f"residual step {BLOCK_STEP}" if args.block else ""),
-                       "tokens_per_step_per_gpu": sh.T, "active_experts": n_active,
-                       "max_expert_load_over_mean": float(counts.max() / counts.mean()),
-                       "l2": "no flush: expert weights read per step exceed the 126 MB L2",
-                       "parallelism": f"replicas x{world}"},
-            "roofline": roof,
-            "layer_roofline": layer_roof,
-            "kernels_ms": per_kernel_ms,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": launches,
-            "clocks": clk.summary(),
-        }
+        head = results[names[0]]
+        line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": head["dtype"],
+                "data": "synthetic (seeded N(0,1) activations, N(0,0.02) bf16 weights)"}
+        for k in ("config", "roofline", "layer_roofline", "kernels_ms", "cpu_baseline", "e2e",
+                  "gpu_launches", "clocks"):
+            line[k] = head[k]
+        if len(names) > 1:
+            line["configs"] = {n: results[n] for n in names[1:]}
+        if lib_peaks is not None:
+            line["library_tensor_peaks"] = lib_peaks
         print(json.dumps(line), flush=True)
 
 
@@ -633,7 +775,8 @@ def run_route_only(args):
     from sparse_moe_layer_experts_b300 import synth
     from sparse_moe_layer_experts_b300.layer import BeamMoE
     build_mod.build()
-    sh = synth.shape(args.config, **parse_override(args.override))
+    name = DEFAULT_SET[0] if args.config == "all" else args.config
+    sh = synth.shape(name, **parse_override(args.override))
     d = synth.make_inputs(sh, seed=0, device="cuda", weights=False)
     w = torch.zeros(1, dtype=torch.bfloat16, device="cuda")
     layer = BeamMoE.__new__(BeamMoE)
@@ -659,7 +802,7 @@ def run_route_only(args):
     ms = {n: sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps)) / args.steps
           for j, n in enumerate(names)}
     gflop = 2 * sh.T * sh.H * sh.E / 1e9
-    print(json.dumps({"route_only": True, "config": args.config, "T": sh.T, "kernels_ms": ms,
+    print(json.dumps({"route_only": True, "config": name, "T": sh.T, "kernels_ms": ms,
                       "router_tflops": gflop / ms["router_scores"]}), flush=True)
 
 

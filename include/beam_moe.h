@@ -22,8 +22,9 @@
  *
  * Readings taken where the pages are silent: ties go to the lower group or
  * expert index; the selected slots are ordered by score descending, index
- * ascending; the router sums h = 0..H-1 in order with FP32 fused
- * multiply-adds; sigmoid(l) = 1/(1 + fp32(exp(-l))).
+ * ascending; the router logits are FP32 sums of exact products (a sequential
+ * FMA chain for small batches, tensor cores for large ones: see
+ * beam_moe_router_arith); sigmoid(l) = 1/(1 + fp32(exp(-l))).
  *
  * Conventions shared by every call:
  *  - Pointers named as device pointers are CUDA device memory owned by the
@@ -133,6 +134,28 @@ int beam_moe_route(const void *x, const float *router_w, int64_t T,
                    const beam_moe_cfg *cfg, int32_t *topk_ids, float *topk_w,
                    float *scores, int32_t *counts, int32_t *offsets,
                    int32_t *row_of, void *stream);
+
+/*
+ * How the router logits of a batch of T tokens are computed (the pages pin
+ * only "router in FP32": "Reflection Beam 1.0", section "Residual stream",
+ * last paragraph).  Returns one of:
+ *   BEAM_MOE_ROUTER_FMA_CHAIN  each logit is the FP32 fused multiply-add
+ *                              chain over h = 0..H-1 from +0, i.e. exactly a
+ *                              sequential FP32 dot product (T < 256);
+ *   BEAM_MOE_ROUTER_TENSOR     tensor cores: router_w is split into three
+ *                              bf16 parts whose sum is router_w exactly, so
+ *                              every product x*w is exact, and the products
+ *                              are summed in FP32 in the tensor cores' order
+ *                              (T >= 256).  A logit then differs from the
+ *                              sequential FP32 dot product only by FP32
+ *                              accumulation rounding.
+ * In both cases sigmoid(l) = 1/(1 + fp32(exp(-l))) is applied to the FP32
+ * logit, and the selection uses those FP32 scores.  Returns
+ * BEAM_MOE_ERR_INVALID_ARG for an invalid configuration or T < 0.
+ */
+#define BEAM_MOE_ROUTER_FMA_CHAIN 0
+#define BEAM_MOE_ROUTER_TENSOR 1
+int beam_moe_router_arith(int64_t T, const beam_moe_cfg *cfg);
 
 /*
  * The whole layer forward (steps 1-7).
@@ -275,9 +298,12 @@ int beam_moe_dense_forward(const void *x, const void *w_gate, const void *w_up,
  *   norm_pre, norm_post [H] fp32, device;  eps in [0, 1]
  *   stream_out [T,H] bf16, device, written; may be stream_in (in place), must
  *              not partly overlap it
- * Routing and experts as beam_moe_forward on x (bf16 weights only:
- * BEAM_MOE_ERR_UNSUPPORTED for NVFP4; H <= 8192).  Workspace:
- * beam_moe_block_workspace_size.  step >= 1.  Asynchronous; deterministic.
+ * Routing and experts as beam_moe_forward on x, with any expert format of
+ * cfg->wtype (bf16, NVFP4 or MXFP8 weights and their scales, as for
+ * beam_moe_forward; the quantised formats quantise x and h the same way, and
+ * o is their FP32 combine); H <= 8192 (else BEAM_MOE_ERR_UNSUPPORTED).
+ * Workspace: beam_moe_block_workspace_size.  step >= 1.  Asynchronous;
+ * deterministic.
  */
 size_t beam_moe_block_workspace_size(int64_t T, const beam_moe_cfg *cfg);
 int beam_moe_block_forward(const void *stream_in, int step, const float *norm_pre,

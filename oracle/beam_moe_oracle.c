@@ -309,17 +309,37 @@ void oracle_expert_row(const uint16_t *xrow, const uint16_t *wg,
 /* ----------------------------------------------------------- whole layer */
 
 /*
+ * The router's scores for one token: computed from x and wr (the router
+ * step), or, when the caller gives scores_in [T,E], that token's given row.
+ * The given-scores form is the layer from the selection step on, applied to
+ * FP32 scores produced elsewhere (the pages fix the selection, weights,
+ * experts and combine as functions of the FP32 scores).
+ */
+static void token_scores(const uint16_t *xrow, const float *wr, const float *scores_in,
+                         int64_t t, int H, int E, float *scores)
+{
+    if (scores_in)
+        memcpy(scores, scores_in + t * E, sizeof(float) * (size_t)E);
+    else
+        oracle_router_scores(xrow, wr, 1, H, E, NULL, scores);
+}
+
+/*
  * The layer forward for a list of tokens (all tokens when tokens == NULL):
  * router -> group-limited top-k -> experts -> weighted combine.
  *   x [T,H] bf16; wr [H,E] fp32; wg, wu [E,I,H] bf16; wd [E,H,I] bf16
  *   out [n,H] bf16 bits (row r is token tokens[r]);
- *   ids_out [n,top_k], w_out [n,top_k] may be NULL.
+ *   ids_out [n,top_k], w_out [n,top_k] may be NULL;
+ *   scores_in [T,E] fp32 or NULL: the router's scores, used instead of the
+ *   router step when given (wr is then not read);
+ *   o_out [n,H] fp32 or NULL: the FP32 combine before the bf16 rounding of
+ *   out (the input of the fused block's post-norm).
  */
 int oracle_forward(const uint16_t *x, const float *wr, const uint16_t *wg,
                    const uint16_t *wu, const uint16_t *wd, int64_t T, int H,
                    int I, int E, int G, int topk_groups, int top_k, float scale,
                    const int64_t *tokens, int64_t n_tokens, uint16_t *out,
-                   int32_t *ids_out, float *w_out)
+                   int32_t *ids_out, float *w_out, const float *scores_in, float *o_out)
 {
     if (E % G != 0 || top_k > topk_groups * (E / G))
         return -1;
@@ -340,7 +360,7 @@ int oracle_forward(const uint16_t *x, const float *wr, const uint16_t *wg,
         double *y = (double *)malloc(sizeof(double) * (size_t)H);
         double *acc = (double *)calloc((size_t)H, sizeof(double));
 
-        oracle_router_scores(xrow, wr, 1, H, E, NULL, scores);
+        token_scores(xrow, wr, scores_in, t, H, E, scores);
         if (oracle_select(scores, 1, E, G, topk_groups, top_k, scale, ids, w) != 0)
             bad = 1;
         for (int k = 0; k < top_k && !bad; ++k) {
@@ -350,8 +370,13 @@ int oracle_forward(const uint16_t *x, const float *wr, const uint16_t *wg,
             for (int j = 0; j < H; ++j)
                 acc[j] += (double)w[k] * y[j];
         }
-        for (int j = 0; j < H; ++j)
-            out[r * H + j] = float_to_bf16_bits_rne((float)acc[j]);
+        {
+            for (int j = 0; j < H; ++j) {
+                if (o_out)
+                    o_out[r * H + j] = (float)acc[j];
+                out[r * H + j] = float_to_bf16_bits_rne((float)acc[j]);
+            }
+        }
         if (ids_out)
             memcpy(ids_out + r * top_k, ids, sizeof(int32_t) * (size_t)top_k);
         if (w_out)
@@ -425,14 +450,16 @@ static float rms_inv(const float *v, int n, float eps)
  *   z  = rmsnorm(o) * gamma_post               FP32
  *   s' = bf16( a*s + b*z ),  a = sqrt((k-1)/k), b = 1/sqrt(k) (FP32)
  *   s  [T,H] bf16 bits (the residual stream at step k-1); out [n,H] bf16
- *   bits (row r is token tokens[r], all tokens when tokens == NULL).
+ *   bits (row r is token tokens[r], all tokens when tokens == NULL);
+ *   scores_in [T,E] fp32 or NULL: the router's scores of the pre-normed x,
+ *   used instead of the router step when given.
  */
 int oracle_block_forward(const uint16_t *s, int step, const float *gamma_pre,
                          const float *gamma_post, float eps, const float *wr,
                          const uint16_t *wg, const uint16_t *wu, const uint16_t *wd,
                          int64_t T, int H, int I, int E, int G, int topk_groups,
                          int top_k, float scale, const int64_t *tokens, int64_t n_tokens,
-                         uint16_t *out)
+                         uint16_t *out, const float *scores_in)
 {
     if (step < 1 || E % G != 0 || top_k > topk_groups * (E / G))
         return -1;
@@ -464,7 +491,7 @@ int oracle_block_forward(const uint16_t *s, int step, const float *gamma_pre,
             const float v = sv[h] * rp;
             xb[h] = float_to_bf16_bits_rne(v * gamma_pre[h]);
         }
-        oracle_router_scores(xb, wr, 1, H, E, NULL, scores);
+        token_scores(xb, wr, scores_in, t, H, E, scores);
         if (oracle_select(scores, 1, E, G, topk_groups, top_k, scale, ids, w) != 0)
             bad = 1;
         for (int k = 0; k < top_k && !bad; ++k) {
@@ -489,6 +516,42 @@ int oracle_block_forward(const uint16_t *s, int step, const float *gamma_pre,
         free(hbuf);
         free(y);
         free(acc);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * The fused block's post-norm and residual update on a given FP32 layer
+ * combine ([P1-RES]): for row r (token t = tokens[r], or r when tokens is
+ * NULL), out[r] = bf16( a*s[t] + b*(rmsnorm(o[r]) * gamma_post) ), with a, b,
+ * the norm and the roundings exactly as in oracle_block_forward.  With o the
+ * o_out of a layer oracle applied to the pre-normed stream, this is the block
+ * for any expert format.
+ */
+int oracle_block_tail(const uint16_t *s, int step, const float *gamma_post, float eps,
+                      const float *o, int64_t T, int H, const int64_t *tokens, int64_t n_tokens,
+                      uint16_t *out)
+{
+    if (step < 1)
+        return -1;
+    const float a = (float)sqrt((double)(step - 1) / (double)step);
+    const float b = (float)(1.0 / sqrt((double)step));
+    const int64_t n = tokens ? n_tokens : T;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t t = tokens ? tokens[r] : r;
+        if (t < 0 || t >= T) {
+            bad = 1;
+            continue;
+        }
+        const float *orow = o + r * H;
+        const float rq = rms_inv(orow, H, eps);
+        for (int j = 0; j < H; ++j) {
+            const float sv = bf16_bits_to_float(s[t * H + j]);
+            const float z = (orow[j] * rq) * gamma_post[j];
+            out[r * H + j] = float_to_bf16_bits_rne(a * sv + b * z);
+        }
     }
     return bad ? -1 : 0;
 }
@@ -651,13 +714,16 @@ static double deq(const uint8_t *codes, const uint8_t *sf, float g, int64_t row,
  *   y    = h . deq(Wd)^T                     (FP64)
  * where xq = fakequant(x).  Weight arrays are the outputs of
  * oracle_quantize_nvfp4: codes [E,I,H] / [E,H,I], sf [.., /16], gs [E].
+ * scores_in [T,E] fp32 or NULL: given router scores, and o_out [n,H] fp32 or
+ * NULL: the FP32 combine, both as in oracle_forward.
  */
 int oracle_forward_nvfp4(const uint16_t *x, const float *wr, const uint8_t *gc, const uint8_t *gsf,
                          const float *ggs, const uint8_t *uc, const uint8_t *usf,
                          const float *ugs, const uint8_t *dc, const uint8_t *dsf,
                          const float *dgs, int64_t T, int H, int I, int E, int G,
                          int topk_groups, int top_k, float scale, const int64_t *tokens,
-                         int64_t n_tokens, uint16_t *out, int32_t *ids_out, float *w_out)
+                         int64_t n_tokens, uint16_t *out, int32_t *ids_out, float *w_out,
+                         const float *scores_in, float *o_out)
 {
     if (E % G != 0 || top_k > topk_groups * (E / G) || H % 16 || I % 16)
         return -1;
@@ -678,7 +744,7 @@ int oracle_forward_nvfp4(const uint16_t *x, const float *wr, const uint8_t *gc, 
         float *hq = (float *)malloc(sizeof(float) * (size_t)I);
         double *acc = (double *)calloc((size_t)H, sizeof(double));
 
-        oracle_router_scores(xrow, wr, 1, H, E, NULL, scores);
+        token_scores(xrow, wr, scores_in, t, H, E, scores);
         if (oracle_select(scores, 1, E, G, topk_groups, top_k, scale, ids, w) != 0)
             bad = 1;
         for (int h = 0; h < H; ++h)
@@ -705,8 +771,13 @@ int oracle_forward_nvfp4(const uint16_t *x, const float *wr, const uint8_t *gc, 
                 acc[j] += (double)w[k] * yd;
             }
         }
-        for (int j = 0; j < H; ++j)
-            out[r * H + j] = float_to_bf16_bits_rne((float)acc[j]);
+        {
+            for (int j = 0; j < H; ++j) {
+                if (o_out)
+                    o_out[r * H + j] = (float)acc[j];
+                out[r * H + j] = float_to_bf16_bits_rne((float)acc[j]);
+            }
+        }
         if (ids_out)
             memcpy(ids_out + r * top_k, ids, sizeof(int32_t) * (size_t)top_k);
         if (w_out)
@@ -852,12 +923,15 @@ void oracle_fake_quant_mxfp8_rows(float *v, int64_t n_rows, int64_t n)
  * The layer forward with MXFP8 experts: routing as oracle_forward (FP32 on
  * the bf16 x); x and h quantised to MXFP8 as above; FP64 dot products of
  * the dequantised values; h = silu(g)*u in FP32 from g, u rounded to FP32.
+ * scores_in [T,E] fp32 or NULL: given router scores, and o_out [n,H] fp32 or
+ * NULL: the FP32 combine, both as in oracle_forward.
  */
 int oracle_forward_mxfp8(const uint16_t *x, const float *wr, const uint8_t *gc, const uint8_t *gsf,
                          const uint8_t *uc, const uint8_t *usf, const uint8_t *dc,
                          const uint8_t *dsf, int64_t T, int H, int I, int E, int G,
                          int topk_groups, int top_k, float scale, const int64_t *tokens,
-                         int64_t n_tokens, uint16_t *out, int32_t *ids_out, float *w_out)
+                         int64_t n_tokens, uint16_t *out, int32_t *ids_out, float *w_out,
+                         const float *scores_in, float *o_out)
 {
     if (E % G != 0 || top_k > topk_groups * (E / G) || H % 32 || I % 32)
         return -1;
@@ -879,7 +953,7 @@ int oracle_forward_mxfp8(const uint16_t *x, const float *wr, const uint8_t *gc, 
         float *hq = (float *)malloc(sizeof(float) * (size_t)I);
         double *acc = (double *)calloc((size_t)H, sizeof(double));
 
-        oracle_router_scores(xrow, wr, 1, H, E, NULL, scores);
+        token_scores(xrow, wr, scores_in, t, H, E, scores);
         if (oracle_select(scores, 1, E, G, topk_groups, top_k, scale, ids, w) != 0)
             bad = 1;
         for (int h = 0; h < H; ++h)
@@ -906,8 +980,13 @@ int oracle_forward_mxfp8(const uint16_t *x, const float *wr, const uint8_t *gc, 
                 acc[j] += (double)w[k] * yd;
             }
         }
-        for (int j = 0; j < H; ++j)
-            out[r * H + j] = float_to_bf16_bits_rne((float)acc[j]);
+        {
+            for (int j = 0; j < H; ++j) {
+                if (o_out)
+                    o_out[r * H + j] = (float)acc[j];
+                out[r * H + j] = float_to_bf16_bits_rne((float)acc[j]);
+            }
+        }
         if (ids_out)
             memcpy(ids_out + r * top_k, ids, sizeof(int32_t) * (size_t)top_k);
         if (w_out)

@@ -56,12 +56,12 @@ def lib():
         L.oracle_expert_row.argtypes = [p, p, p, p, i32, i32, p]
         L.oracle_expert_row.restype = None
         L.oracle_forward.argtypes = [p, p, p, p, p, i64, i32, i32, i32, i32, i32, i32,
-                                     f32, p, i64, p, p, p]
+                                     f32, p, i64, p, p, p, p, p]
         L.oracle_forward.restype = i32
         L.oracle_dense_forward.argtypes = [p, p, p, p, i64, i32, i32, p, i64, p]
         L.oracle_dense_forward.restype = i32
         L.oracle_block_forward.argtypes = [p, i32, p, p, f32, p, p, p, p, i64, i32, i32, i32,
-                                           i32, i32, i32, f32, p, i64, p]
+                                           i32, i32, i32, f32, p, i64, p, p]
         L.oracle_block_forward.restype = i32
         L.oracle_rmsnorm_bf16.argtypes = [p, p, f32, i64, i32, p]
         L.oracle_rmsnorm_bf16.restype = None
@@ -72,7 +72,7 @@ def lib():
         L.oracle_fake_quant_mxfp8_rows.argtypes = [p, i64, i64]
         L.oracle_fake_quant_mxfp8_rows.restype = None
         L.oracle_forward_mxfp8.argtypes = [p, p, p, p, p, p, p, p, i64, i32, i32, i32, i32, i32,
-                                           i32, f32, p, i64, p, p, p]
+                                           i32, f32, p, i64, p, p, p, p, p]
         L.oracle_forward_mxfp8.restype = i32
         L.oracle_e2m1_value.argtypes = [i32]
         L.oracle_e2m1_value.restype = f32
@@ -87,7 +87,9 @@ def lib():
         L.oracle_fake_quant_rows.argtypes = [p, i64, i64]
         L.oracle_fake_quant_rows.restype = None
         L.oracle_forward_nvfp4.argtypes = [p, p, p, p, p, p, p, p, p, p, p, i64, i32, i32, i32, i32,
-                                           i32, i32, f32, p, i64, p, p, p]
+                                           i32, i32, f32, p, i64, p, p, p, p, p]
+        L.oracle_block_tail.argtypes = [p, i32, p, f32, p, i64, i32, p, i64, p]
+        L.oracle_block_tail.restype = i32
         L.oracle_forward_nvfp4.restype = i32
         _lib = L
     return _lib
@@ -162,11 +164,23 @@ def expert_row(x_row_bits, wg_bits, wu_bits, wd_bits):
     return y
 
 
-def forward(x_bits, router_w, wg_bits, wu_bits, wd_bits, n_groups, topk_groups, top_k,
-            scale, tokens=None):
-    """Layer output for `tokens` (all when None).
+def _scores_in(scores, T, E):
+    """Given router scores [T,E] fp32 (or None: the oracle's router runs)."""
+    if scores is None:
+        return None
+    scores = _c(scores, np.float32)
+    if scores.shape != (T, E):
+        raise ValueError(f"scores must be [T,E] = {(T, E)}")
+    return scores
 
-    Returns (out_bits [n,H] uint16, ids [n,K] int32, w [n,K] fp32).
+
+def forward(x_bits, router_w, wg_bits, wu_bits, wd_bits, n_groups, topk_groups, top_k,
+            scale, tokens=None, scores=None, combine=False):
+    """Layer output for `tokens` (all when None).  With `scores` ([T,E] fp32)
+    the given router scores replace the router step (selection onward).
+
+    Returns (out_bits [n,H] uint16, ids [n,K] int32, w [n,K] fp32), and with
+    combine=True also the FP32 combine o [n,H] before the bf16 rounding.
     """
     x_bits = _c(x_bits, np.uint16)
     router_w = _c(router_w, np.float32)
@@ -182,12 +196,15 @@ def forward(x_bits, router_w, wg_bits, wu_bits, wd_bits, n_groups, topk_groups, 
     out = np.empty((n, H), np.uint16)
     ids = np.empty((n, top_k), np.int32)
     w = np.empty((n, top_k), np.float32)
+    sc = _scores_in(scores, T, E)  # kept alive for the call
+    o = np.empty((n, H), np.float32) if combine else None
     rc = lib().oracle_forward(_ptr(x_bits), _ptr(router_w), _ptr(wg_bits), _ptr(wu_bits),
                               _ptr(wd_bits), T, H, I, E, n_groups, topk_groups, top_k,
-                              float(scale), _ptr(tok), n, _ptr(out), _ptr(ids), _ptr(w))
+                              float(scale), _ptr(tok), n, _ptr(out), _ptr(ids), _ptr(w),
+                              _ptr(sc), _ptr(o))
     if rc != 0:
         raise ValueError("oracle_forward failed (bad configuration or token index)")
-    return out, ids, w
+    return (out, ids, w, o) if combine else (out, ids, w)
 
 
 def dense_forward(x_bits, wg_bits, wu_bits, wd_bits, tokens=None):
@@ -211,9 +228,11 @@ def dense_forward(x_bits, wg_bits, wu_bits, wd_bits, tokens=None):
 
 
 def block_forward(s_bits, step, gamma_pre, gamma_post, eps, router_w, wg_bits, wu_bits, wd_bits,
-                  n_groups, topk_groups, top_k, scale, tokens=None):
+                  n_groups, topk_groups, top_k, scale, tokens=None, scores=None):
     """MoE sublayer with pre-norm, post-norm and the constant-scale residual
-    at step `step`: the new stream rows (bf16 bits [n,H]) for `tokens`."""
+    at step `step`: the new stream rows (bf16 bits [n,H]) for `tokens`.
+    With `scores` ([T,E] fp32, the router scores of the pre-normed x) the
+    given scores replace the router step."""
     s_bits = _c(s_bits, np.uint16)
     gp = _c(gamma_pre, np.float32)
     gq = _c(gamma_post, np.float32)
@@ -227,12 +246,31 @@ def block_forward(s_bits, step, gamma_pre, gamma_post, eps, router_w, wg_bits, w
     tok = None if tokens is None else _c(np.asarray(tokens, np.int64), np.int64)
     n = T if tok is None else tok.shape[0]
     out = np.empty((n, H), np.uint16)
+    sc = _scores_in(scores, T, E)  # kept alive for the call
     rc = lib().oracle_block_forward(_ptr(s_bits), int(step), _ptr(gp), _ptr(gq), float(eps),
                                     _ptr(router_w), _ptr(wg_bits), _ptr(wu_bits), _ptr(wd_bits),
                                     T, H, I, E, n_groups, topk_groups, top_k, float(scale),
-                                    _ptr(tok), n, _ptr(out))
+                                    _ptr(tok), n, _ptr(out), _ptr(sc))
     if rc != 0:
         raise ValueError("oracle_block_forward failed (bad configuration, step or token)")
+    return out
+
+
+def block_tail(s_bits, step, gamma_post, eps, o, tokens=None):
+    """The fused block's post-norm and residual on a given FP32 layer combine
+    o [n,H] (rows of `tokens`, all when None): bf16 bits [n,H]."""
+    s_bits = _c(s_bits, np.uint16)
+    gq = _c(gamma_post, np.float32)
+    o = _c(o, np.float32)
+    T, H = s_bits.shape
+    tok = None if tokens is None else _c(np.asarray(tokens, np.int64), np.int64)
+    n = T if tok is None else tok.shape[0]
+    assert o.shape == (n, H) and gq.shape == (H,)
+    out = np.empty((n, H), np.uint16)
+    rc = lib().oracle_block_tail(_ptr(s_bits), int(step), _ptr(gq), float(eps), _ptr(o), T, H,
+                                 _ptr(tok), n, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_block_tail failed (bad step or token)")
     return out
 
 
@@ -298,8 +336,9 @@ def dequantize_nvfp4(codes, sf, gs) -> np.ndarray:
 
 
 def forward_nvfp4(x_bits, router_w, q_gate, q_up, q_down, n_groups, topk_groups, top_k,
-                  scale, tokens=None):
-    """NVFP4 layer for `tokens`; q_* = (codes, sf, gs) from quantize_nvfp4."""
+                  scale, tokens=None, scores=None, combine=False):
+    """NVFP4 layer for `tokens`; q_* = (codes, sf, gs) from quantize_nvfp4;
+    `scores` as in forward()."""
     x_bits = _c(x_bits, np.uint16)
     router_w = _c(router_w, np.float32)
     (gc, gsf, ggs), (uc, usf, ugs), (dc, dsf, dgs) = [
@@ -313,13 +352,16 @@ def forward_nvfp4(x_bits, router_w, q_gate, q_up, q_down, n_groups, topk_groups,
     out = np.empty((n, H), np.uint16)
     ids = np.empty((n, top_k), np.int32)
     w = np.empty((n, top_k), np.float32)
+    sc = _scores_in(scores, T, E)  # kept alive for the call
+    o = np.empty((n, H), np.float32) if combine else None
     rc = lib().oracle_forward_nvfp4(_ptr(x_bits), _ptr(router_w), _ptr(gc), _ptr(gsf), _ptr(ggs),
                                     _ptr(uc), _ptr(usf), _ptr(ugs), _ptr(dc), _ptr(dsf),
                                     _ptr(dgs), T, H, I, E, n_groups, topk_groups, top_k,
-                                    float(scale), _ptr(tok), n, _ptr(out), _ptr(ids), _ptr(w))
+                                    float(scale), _ptr(tok), n, _ptr(out), _ptr(ids), _ptr(w),
+                                    _ptr(sc), _ptr(o))
     if rc != 0:
         raise ValueError("oracle_forward_nvfp4 failed")
-    return out, ids, w
+    return (out, ids, w, o) if combine else (out, ids, w)
 
 
 # ---------------------------------------------------------------- MXFP8
@@ -361,8 +403,9 @@ def dequantize_mxfp8(codes, sf) -> np.ndarray:
 
 
 def forward_mxfp8(x_bits, router_w, q_gate, q_up, q_down, n_groups, topk_groups, top_k, scale,
-                  tokens=None):
-    """Layer output with MXFP8 experts; q_* = quantize_mxfp8(w_*) (codes, sf)."""
+                  tokens=None, scores=None, combine=False):
+    """Layer output with MXFP8 experts; q_* = quantize_mxfp8(w_*) (codes, sf);
+    `scores` as in forward()."""
     x_bits = _c(x_bits, np.uint16)
     router_w = _c(router_w, np.float32)
     T, H = x_bits.shape
@@ -375,11 +418,13 @@ def forward_mxfp8(x_bits, router_w, q_gate, q_up, q_down, n_groups, topk_groups,
     out = np.empty((n, H), np.uint16)
     ids = np.empty((n, top_k), np.int32)
     w = np.empty((n, top_k), np.float32)
+    sc = _scores_in(scores, T, E)  # kept alive for the call
+    o = np.empty((n, H), np.float32) if combine else None
     rc = lib().oracle_forward_mxfp8(_ptr(x_bits), _ptr(router_w), _ptr(gc), _ptr(gsf), _ptr(uc),
                                     _ptr(usf), _ptr(dc), _ptr(dsf), T, H, I, E, n_groups,
                                     topk_groups, top_k, float(scale), _ptr(tok), n, _ptr(out),
-                                    _ptr(ids), _ptr(w))
+                                    _ptr(ids), _ptr(w), _ptr(sc), _ptr(o))
     if rc != 0:
         raise ValueError("oracle_forward_mxfp8 failed")
-    return out, ids, w
+    return (out, ids, w, o) if combine else (out, ids, w)
 

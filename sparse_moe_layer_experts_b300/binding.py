@@ -20,6 +20,9 @@ BEAM_MOE_ERR_WORKSPACE = -4
 BEAM_MOE_ERR_TIMEOUT = -5
 BEAM_MOE_ERR_DEVICE = -6
 
+BEAM_MOE_ROUTER_FMA_CHAIN = 0
+BEAM_MOE_ROUTER_TENSOR = 1
+
 BEAM_MOE_W_BF16 = 0
 BEAM_MOE_W_NVFP4 = 1
 BEAM_MOE_W_MXFP8 = 2
@@ -74,6 +77,8 @@ def lib():
         L.beam_moe_workspace_size.restype = sz
         L.beam_moe_hostio_extra_bytes.argtypes = [i64, cfgp]
         L.beam_moe_hostio_extra_bytes.restype = sz
+        L.beam_moe_router_arith.argtypes = [i64, cfgp]
+        L.beam_moe_router_arith.restype = ctypes.c_int
         L.beam_moe_route.argtypes = [vp, vp, i64, cfgp, vp, vp, vp, vp, vp, vp, vp]
         L.beam_moe_route.restype = ctypes.c_int
         L.beam_moe_forward.argtypes = [vp, vp, vp, vp, vp, i64, cfgp, vp, vp]
@@ -120,6 +125,10 @@ def beam_moe_cfg_init_beam(cfg: beam_moe_cfg) -> None:
 
 def beam_moe_workspace_size(T: int, cfg: beam_moe_cfg) -> int:
     return int(lib().beam_moe_workspace_size(T, ctypes.byref(cfg)))
+
+
+def beam_moe_router_arith(T: int, cfg: beam_moe_cfg) -> int:
+    return int(lib().beam_moe_router_arith(T, ctypes.byref(cfg)))
 
 
 def beam_moe_hostio_extra_bytes(T: int, cfg: beam_moe_cfg) -> int:

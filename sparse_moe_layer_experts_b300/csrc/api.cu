@@ -9,6 +9,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -32,6 +33,8 @@ void stage_end(int stage, cudaStream_t s)
         cudaEventRecord(g_ev_stop[stage], s);
 }
 
+void count_launch() { ++g_launches; }
+
 namespace {
 
 constexpr size_t kAlign = 1024;
@@ -40,10 +43,23 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-    size_t status, scores, ids, wts, local_rank, cta_counts, cta_base, counts, offsets,
+    size_t status, wr_parts, router_partials, scores, ids, wts, local_rank, cta_counts, cta_base, counts, offsets,
         chunk_start, row_of, row_src, x_perm, h, h_raw, y, row_pos, x_sf, h_sf,
         total;
 };
+
+// Prefill-size batches route on the tensor cores (router_tc.cu); smaller
+// ones keep the FP32 FMA-chain router, whose logits follow the h order.
+bool tc_router(int64_t T) { return T >= kTcRouterMinTokens; }
+
+// The workspace holds the tensor-core router's partial logits for as many
+// hidden-dimension splits as a GPU of up to kLayoutSms SMs would take; the
+// launch never takes more.
+constexpr int kLayoutSms = 256;
+int tc_router_layout_splits(int64_t T, const beam_moe_cfg &c)
+{
+    return tc_router(T) ? router_tc_splits(T, c.n_experts, c.hidden, kLayoutSms) : 0;
+}
 
 GemmVariant pick_variant(int64_t T, const beam_moe_cfg &c)
 {
@@ -72,6 +88,11 @@ Layout make_layout(int64_t T, const beam_moe_cfg &c)
         return at;
     };
     L.status = take(256);
+    L.wr_parts = take(tc_router(T) ? (size_t)3 * E * H * 2 : 0);
+    // partial logits of split hidden ranges (none when one range: the
+    // logits then go straight into the scores buffer)
+    const int splits = tc_router_layout_splits(T, c);
+    L.router_partials = take(splits > 1 ? sizeof(float) * splits * T * E : 0);
     L.scores = take(sizeof(float) * T * E);
     L.ids = take(sizeof(int32_t) * R);
     L.wts = take(sizeof(float) * R);
@@ -142,6 +163,25 @@ int check_cfg(const beam_moe_cfg *c)
     if (c->wtype != BEAM_MOE_W_BF16 && c->wtype != BEAM_MOE_W_NVFP4 &&
         c->wtype != BEAM_MOE_W_MXFP8)
         return BEAM_MOE_ERR_INVALID_ARG;
+    return BEAM_MOE_OK;
+}
+
+// The block and global scales that NVFP4 / MXFP8 weights need.
+int check_scale_ptrs(const beam_moe_cfg *c)
+{
+    if (c->wtype == BEAM_MOE_W_NVFP4) {
+        const void *p[6] = {c->w_gate_sf, c->w_up_sf, c->w_down_sf,
+                            c->w_gate_gs, c->w_up_gs, c->w_down_gs};
+        for (const void *q : p)
+            if (!q || !aligned16(q))
+                return BEAM_MOE_ERR_INVALID_ARG;
+    }
+    if (c->wtype == BEAM_MOE_W_MXFP8) {
+        const void *p[3] = {c->w_gate_sf, c->w_up_sf, c->w_down_sf};
+        for (const void *q : p)
+            if (!q || !aligned16(q))
+                return BEAM_MOE_ERR_INVALID_ARG;
+    }
     return BEAM_MOE_OK;
 }
 
@@ -237,10 +277,30 @@ int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cf
 {
     void *ws = c.workspace;
     int *status = at<int>(ws, L.status);
-    BEAM_CUDA(launch_router_scores(static_cast<const uint16_t *>(x), router_w, (int)T, c.hidden,
-                                   c.n_experts, scores, status, s));
-    BEAM_CUDA(launch_select(scores, (int)T, c.n_experts, c.n_groups, c.topk_groups, c.top_k,
-                            c.routed_scale, ids, wts, status, s));
+    int nsplit = 0;  // 0: the FMA-chain router wrote the scores
+    float *partials = scores;
+    if (tc_router(T)) {
+        const int sms = device_sms();
+        if (sms <= 0)
+            return BEAM_MOE_ERR_CUDA;
+        nsplit = std::min(router_tc_splits(T, c.n_experts, c.hidden, sms),
+                          tc_router_layout_splits(T, c));
+        if (nsplit > 1)
+            partials = at<float>(ws, L.router_partials);
+        CUtensorMap mw, mx;
+        if (!make_map(&mw, at<void>(ws, L.wr_parts), c.hidden, (uint64_t)3 * c.n_experts, 128) ||
+            !make_map(&mx, x, c.hidden, (uint64_t)T, 256))
+            return BEAM_MOE_ERR_CUDA;
+        const unsigned long long tmo =
+            c.wait_timeout_ns > 0 ? (unsigned long long)c.wait_timeout_ns : kDefaultTimeoutNs;
+        BEAM_CUDA(launch_router_tc(router_w, at<void>(ws, L.wr_parts), mw, mx, (int)T, c.hidden,
+                                   c.n_experts, nsplit, partials, status, tmo, s));
+    } else {
+        BEAM_CUDA(launch_router_scores(static_cast<const uint16_t *>(x), router_w, (int)T,
+                                       c.hidden, c.n_experts, scores, status, s));
+    }
+    BEAM_CUDA(launch_select(scores, partials, nsplit, (int)T, c.n_experts, c.n_groups,
+                            c.topk_groups, c.top_k, c.routed_scale, ids, wts, status, s));
     BEAM_CUDA(launch_hist_scan(ids, (int)T, c.top_k, c.n_experts, rows_per_chunk,
                                at<int32_t>(ws, L.local_rank), at<int32_t>(ws, L.cta_counts),
                                at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.counts),
@@ -500,6 +560,13 @@ size_t beam_moe_workspace_size(int64_t T, const beam_moe_cfg *cfg)
     return make_layout(T, *cfg).total;
 }
 
+int beam_moe_router_arith(int64_t T, const beam_moe_cfg *cfg)
+{
+    if (check_cfg(cfg) != BEAM_MOE_OK || T < 0)
+        return BEAM_MOE_ERR_INVALID_ARG;
+    return tc_router(T) ? BEAM_MOE_ROUTER_TENSOR : BEAM_MOE_ROUTER_FMA_CHAIN;
+}
+
 size_t beam_moe_hostio_extra_bytes(int64_t T, const beam_moe_cfg *cfg)
 {
     if (check_cfg(cfg) != BEAM_MOE_OK || T < 0)
@@ -556,19 +623,8 @@ int beam_moe_forward(const void *x, const float *router_w, const void *w_gate, c
         return BEAM_MOE_OK;
     if (!x || !router_w || !w_gate || !w_up || !w_down || !out)
         return BEAM_MOE_ERR_INVALID_ARG;
-    if (cfg->wtype == BEAM_MOE_W_NVFP4) {
-        const void *p[6] = {cfg->w_gate_sf, cfg->w_up_sf, cfg->w_down_sf,
-                            cfg->w_gate_gs, cfg->w_up_gs, cfg->w_down_gs};
-        for (const void *q : p)
-            if (!q || !aligned16(q))
-                return BEAM_MOE_ERR_INVALID_ARG;
-    }
-    if (cfg->wtype == BEAM_MOE_W_MXFP8) {
-        const void *p[3] = {cfg->w_gate_sf, cfg->w_up_sf, cfg->w_down_sf};
-        for (const void *q : p)
-            if (!q || !aligned16(q))
-                return BEAM_MOE_ERR_INVALID_ARG;
-    }
+    if ((rc = check_scale_ptrs(cfg)) != BEAM_MOE_OK)
+        return rc;
     if (!aligned16(x) || !aligned16(router_w) || !aligned16(w_gate) || !aligned16(w_up) ||
         !aligned16(w_down) || !aligned16(out))
         return BEAM_MOE_ERR_INVALID_ARG;
@@ -752,8 +808,6 @@ int beam_moe_block_forward(const void *stream_in, int step, const float *norm_pr
     int rc = check_cfg(cfg);
     if (rc != BEAM_MOE_OK)
         return rc;
-    if (cfg->wtype != BEAM_MOE_W_BF16)
-        return BEAM_MOE_ERR_UNSUPPORTED;
     if (cfg->hidden > 8192)
         return BEAM_MOE_ERR_UNSUPPORTED;
     if ((rc = check_T(T, cfg)) != BEAM_MOE_OK)
@@ -765,6 +819,8 @@ int beam_moe_block_forward(const void *stream_in, int step, const float *norm_pr
     if (!stream_in || !norm_pre || !norm_post || !router_w || !w_gate || !w_up || !w_down ||
         !stream_out)
         return BEAM_MOE_ERR_INVALID_ARG;
+    if ((rc = check_scale_ptrs(cfg)) != BEAM_MOE_OK)
+        return rc;
     if (!aligned16(stream_in) || !aligned16(norm_pre) || !aligned16(norm_post) ||
         !aligned16(router_w) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
         !aligned16(stream_out))

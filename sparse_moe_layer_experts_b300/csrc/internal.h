@@ -26,6 +26,8 @@ enum Stage {
 // the stage (if any are set) and counts the launch.
 void stage_begin(int stage, cudaStream_t s);
 void stage_end(int stage, cudaStream_t s);
+// Count a launch that shares its stage's events with the stage's last kernel.
+void count_launch();
 
 // ---- router.cu
 // scores[t,e] = sigmoid(sum_h x[t,h] * wr[h,e]) with an FP32 FMA chain in
@@ -33,9 +35,30 @@ void stage_end(int stage, cudaStream_t s);
 // Also resets *status (the call's device status word) to 0.
 cudaError_t launch_router_scores(const uint16_t *x, const float *wr, int T, int H, int E,
                                  float *scores, int *status, cudaStream_t s);
-// Group-limited top-k over scores -> ids [T,K], w [T,K].
-cudaError_t launch_select(const float *scores, int T, int E, int G, int TG, int K, float scale,
-                          int32_t *ids, float *w, int *status, cudaStream_t s);
+// ---- router_tc.cu
+// Batches of at least kTcRouterMinTokens tokens take the tensor-core router:
+// wr is split into three exact bf16 parts [3][E][H] (`parts`, 3*E*H*2 bytes
+// of workspace), then the FP32 tensor-core sums of the exact products
+// x[t,h]*part[e,h] over nsplit ranges of h go to partials [nsplit][T][E]
+// (nsplit a power of two <= kRouterMaxSplits; router_tc_splits picks it from
+// the tile count and the SM count).  w_map: parts as [3E, H] bf16, box 64 x
+// 128 rows; x_map: x [T,H] bf16, box 64 x 256 rows (both 128-byte
+// swizzled).  Two launches; the first resets *status.  launch_select then
+// turns the partials into scores.
+constexpr int kTcRouterMinTokens = 256;
+constexpr int kRouterMaxSplits = 8;
+int router_tc_splits(int64_t T, int E, int H, int sms);
+cudaError_t launch_router_tc(const float *wr, void *parts, const CUtensorMap &w_map,
+                             const CUtensorMap &x_map, int T, int H, int E, int nsplit,
+                             float *partials, int *status, unsigned long long timeout_ns,
+                             cudaStream_t s);
+// Group-limited top-k over scores -> ids [T,K], w [T,K].  With nsplit > 0
+// the scores are computed first from the router's partial logits
+// [nsplit][T][E] (summed in order, then the sigmoid) and written to scores
+// (partials may equal scores when nsplit == 1).
+cudaError_t launch_select(float *scores, const float *partials, int nsplit, int T, int E, int G,
+                          int TG, int K, float scale, int32_t *ids, float *w, int *status,
+                          cudaStream_t s);
 
 // ---- dispatch.cu
 constexpr int kHistTokens = 256;  // tokens per histogram CTA

@@ -89,3 +89,97 @@ def chunk_rows_of(T, K, E, fmt="bf16"):
 # Random tokens every full-size test checks on top of the segment and chunk
 # edges (the oracle runs about 25 tokens/s on 16 host cores).
 N_RANDOM_FULL = 256
+
+
+# ------------------------------------------------------------------ routing
+#
+# Router logits come from one of two FP32 evaluations (beam_moe_router_arith):
+#  - the FMA chain (T < 256): the oracle's own arithmetic, so scores must match
+#    the oracle bit for bit;
+#  - the tensor cores (T >= 256): every product x*w is exact (x is bf16, the
+#    FP32 router weight is split exactly into three bf16 parts), and the
+#    products are added in FP32 in the tensor cores' order, over up to 8
+#    ranges of h whose partial sums are then added in order.  Any FP32
+#    summation of n exact terms with a longest chain of d roundings satisfies
+#        |l - l_exact| <= ((1 + u)^d - 1) * sum|terms| ~ d * u * sum|x*w|
+#    with u = 2^-23 even for round-toward-zero.  The chain here is at most
+#    d = 3*H/16 + 16 + 8 (one accumulator addition per 16-deep MMA for each
+#    of the three parts, up to 16 inside an MMA, up to 8 partial sums).
+#    sigmoid has slope <= 1/4, and the FP32 exp/add/divide of the score add
+#    at most 4 * 2^-24.
+# Given the same FP32 scores, the selection is a pure function of them, so the
+# GPU's ids and weights must equal the oracle's selection on the GPU's scores
+# bit for bit (the comparison rule for routing); the oracle's own scores may
+# select differently only on near-ties, which are counted and must be rare.
+
+def tc_score_bound(x_bits, router_w):
+    """(exact fp64 sigmoid scores [T,E], per-element bound on |s_gpu - s_exact|)."""
+    x = (np.asarray(x_bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(
+        np.float64)
+    w = np.asarray(router_w, np.float64)
+    logits = x @ w                     # products exact in fp64; sum error ~2^-53 * A
+    A = np.abs(x) @ np.abs(w)
+    d = 3 * x.shape[1] // 16 + 16 + 8
+    bound = d * 2.0 ** -23 * A / 4.0 + 4 * 2.0 ** -24
+    return 1.0 / (1.0 + np.exp(-logits)), bound
+
+
+def check_tc_scores(g_scores, x_bits, router_w):
+    s_exact, bound = tc_score_bound(x_bits, router_w)
+    err = np.abs(np.asarray(g_scores, np.float64) - s_exact)
+    bad = int((err > bound).sum())
+    assert bad == 0, f"{bad} tensor-core router scores outside the FP32 accumulation bound " \
+                     f"(max err {err.max():.3e}, max err/bound {(err / bound).max():.3f})"
+    return float(err.max()), float(np.sqrt((err ** 2).mean()))
+
+
+def check_route(oracle_mod, sh, r, x_bits, router_w, arith):
+    """Check the GPU routing outputs `r` (BeamMoE.route with scores) of a batch
+    against the oracle.  Returns a dict with the checked ids, counts, offsets,
+    row_src, the GPU scores and the set of near-tie tokens on which the
+    oracle's own scores select differently."""
+    from sparse_moe_layer_experts_b300 import binding as B
+    g = {k: v.cpu().numpy() for k, v in r.items() if v is not None}
+    _, s_o = oracle_mod.router_scores(x_bits, router_w)
+    if arith == B.BEAM_MOE_ROUTER_FMA_CHAIN:
+        n_diff = int((g["scores"].view(np.uint32) != s_o.view(np.uint32)).sum())
+        assert n_diff == 0, f"{n_diff} scores differ from the oracle's"
+    else:
+        assert arith == B.BEAM_MOE_ROUTER_TENSOR
+        check_tc_scores(g["scores"], x_bits, router_w)
+    ids, w = oracle_mod.select(g["scores"], sh.G, sh.topk_groups, sh.top_k, sh.scale)
+    assert np.array_equal(g["ids"], ids)
+    assert np.array_equal(g["w"].view(np.uint32), w.view(np.uint32))
+    counts, offsets, row_of, row_src = oracle_mod.dispatch(ids, sh.E)
+    assert np.array_equal(g["counts"], counts)
+    assert np.array_equal(g["offsets"], offsets)
+    assert np.array_equal(g["row_of"], row_of)
+    ids_o, _ = oracle_mod.select(s_o, sh.G, sh.topk_groups, sh.top_k, sh.scale)
+    flipped = set(int(t) for t in np.nonzero((ids_o != ids).any(axis=1))[0])
+    if arith == B.BEAM_MOE_ROUTER_FMA_CHAIN:
+        assert not flipped
+    else:
+        assert len(flipped) <= max(4, sh.T // 1000), f"{len(flipped)} near-tie flips"
+    return dict(ids=ids, w=w, counts=counts, offsets=offsets, row_src=row_src,
+                scores=g["scores"], flipped=flipped)
+
+
+def oracle_rows(fwd, toks, route, *args, **kw):
+    """The oracle's layer rows for tokens `toks` (a list): its own router for
+    every token whose selection agrees with the GPU's, and the GPU's checked
+    scores for the near-tie tokens where two valid FP32 evaluations of the
+    router select different experts."""
+    res = fwd(*args, tokens=toks, **kw)
+    ref = res[0] if isinstance(res, tuple) else res
+    flip = [i for i, t in enumerate(toks) if t in route["flipped"]]
+    if flip:
+        sub = fwd(*args, tokens=[toks[i] for i in flip], scores=route["scores"], **kw)
+        ref[flip] = sub[0] if isinstance(sub, tuple) else sub
+    return ref
+
+
+def router_arith(layer, T):
+    from sparse_moe_layer_experts_b300 import binding as B
+    a = B.beam_moe_router_arith(T, layer.cfg)
+    assert a >= 0
+    return a

@@ -143,7 +143,17 @@ def test_block_entry_point_checks(L):
         B.BEAM_MOE_ERR_INVALID_ARG
     assert B.beam_moe_block_forward(16, 9, 16, 16, 1e-6, 16, 16, 16, 16, 4, c, 16, None) == \
         B.BEAM_MOE_ERR_WORKSPACE
-    c.wtype = B.BEAM_MOE_W_NVFP4
+    # quantised experts are accepted, but need their scale pointers
+    for wt in (B.BEAM_MOE_W_NVFP4, B.BEAM_MOE_W_MXFP8):
+        c.wtype = wt
+        c.w_gate_sf = c.w_up_sf = c.w_down_sf = None
+        assert B.beam_moe_block_forward(16, 9, 16, 16, 1e-6, 16, 16, 16, 16, 4, c, 16, None) == \
+            B.BEAM_MOE_ERR_INVALID_ARG
+        c.w_gate_sf = c.w_up_sf = c.w_down_sf = 16
+        c.w_gate_gs = c.w_up_gs = c.w_down_gs = 16
+        assert B.beam_moe_block_forward(16, 9, 16, 16, 1e-6, 16, 16, 16, 16, 4, c, 16, None) == \
+            B.BEAM_MOE_ERR_WORKSPACE
+    c.hidden = 8192 + 128
     assert B.beam_moe_block_forward(16, 9, 16, 16, 1e-6, 16, 16, 16, 16, 4, c, 16, None) == \
         B.BEAM_MOE_ERR_UNSUPPORTED
     assert B.beam_moe_launch_count() == before
@@ -162,3 +172,20 @@ def test_activation_quantiser_checks(L):
     assert B.beam_moe_quantize_act(nv, 18, 4, 64, 16, 16, None) == B.BEAM_MOE_ERR_INVALID_ARG
     assert B.beam_moe_quantize_act(nv, None, 4, 64, 16, 16, None) == B.BEAM_MOE_ERR_INVALID_ARG
     assert B.beam_moe_launch_count() == before
+
+
+def test_router_arith_by_batch_size():
+    # Small batches keep the sequential FP32 FMA-chain router; from 256 tokens
+    # the tensor-core router runs, and its split router weight (three bf16
+    # parts of [E,H]) is carved from the workspace.
+    c = B.beam_moe_cfg()
+    B.beam_moe_cfg_init_beam(c)
+    assert B.beam_moe_router_arith(1, c) == B.BEAM_MOE_ROUTER_FMA_CHAIN
+    assert B.beam_moe_router_arith(255, c) == B.BEAM_MOE_ROUTER_FMA_CHAIN
+    assert B.beam_moe_router_arith(256, c) == B.BEAM_MOE_ROUTER_TENSOR
+    assert B.beam_moe_router_arith(1 << 20, c) == B.BEAM_MOE_ROUTER_TENSOR
+    assert B.beam_moe_router_arith(-1, c) == B.BEAM_MOE_ERR_INVALID_ARG
+    grow = B.beam_moe_workspace_size(256, c) - B.beam_moe_workspace_size(255, c)
+    assert grow >= 3 * c.n_experts * c.hidden * 2
+    c.top_k = 0
+    assert B.beam_moe_router_arith(256, c) == B.BEAM_MOE_ERR_INVALID_ARG

@@ -9,8 +9,8 @@ import torch
 from sparse_moe_layer_experts_b300 import synth
 from sparse_moe_layer_experts_b300.layer import BeamMoE, quantize_mxfp8
 
-from tests._gpu_util import (N_RANDOM_FULL, chunk_rows_of, out_bits, rel_l2_per_token,
-                             sample_tokens)
+from tests._gpu_util import (N_RANDOM_FULL, check_route, chunk_rows_of, oracle_rows, out_bits,
+                             rel_l2_per_token, router_arith, sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -77,12 +77,13 @@ def test_mxfp8_forward_small_all_tokens(oracle_mod, name):
     sh = SMALL[name]
     d = synth.make_inputs(sh, seed=13, device="cuda")
     layer = _layer(sh, d)
+    xb, rw = synth.to_bits(d["x"]), synth.to_f32(d["router_w"])
+    route = check_route(oracle_mod, sh, layer.route(d["x"]), xb, rw, router_arith(layer, sh.T))
     out = layer.forward(d["x"])
     torch.cuda.synchronize()
     assert layer.status() == 0
-    ref, _, _ = oracle_mod.forward_mxfp8(synth.to_bits(d["x"]), synth.to_f32(d["router_w"]),
-                                         *_oracle_q(oracle_mod, d), sh.G, sh.topk_groups,
-                                         sh.top_k, sh.scale)
+    ref = oracle_rows(oracle_mod.forward_mxfp8, list(range(sh.T)), route, xb, rw,
+                      *_oracle_q(oracle_mod, d), sh.G, sh.topk_groups, sh.top_k, sh.scale)
     rel = rel_l2_per_token(out_bits(out), ref)
     assert rel.max() <= MXFP8_TOL, (rel.max(), int(rel.argmax()))
 
@@ -100,28 +101,26 @@ def test_mxfp8_deterministic():
 @pytest.mark.parametrize("name", ["decode", "prefill"])
 def test_mxfp8_full_size_sampled(oracle_mod, name):
     """Full-size MXFP8 layer against the oracle with the identical
-    quantisation: routing of every token; outputs of every decode token, and
+    quantisation: routing of every token checked; outputs of every decode
+    token, and
     at prefill size of the segment edges of every expert, the chunk edges of
     the most loaded expert and 256 seeded random tokens."""
     sh = synth.shape(name)
     d = synth.make_inputs(sh, seed=0, device="cuda")
     layer = _layer(sh, d)
     out = layer.forward(d["x"])
-    r = layer.route(d["x"], want_scores=False)
+    r = layer.route(d["x"])
     torch.cuda.synchronize()
     assert layer.status() == 0
-    ids = r["ids"].cpu().numpy()
     xb, rw = synth.to_bits(d["x"]), synth.to_f32(d["router_w"])
-    _, s = oracle_mod.router_scores(xb, rw)
-    ids_o, _ = oracle_mod.select(s, sh.G, sh.topk_groups, sh.top_k, sh.scale)
-    assert np.array_equal(ids, ids_o)
-    _, offsets, _, row_src = oracle_mod.dispatch(ids_o, sh.E)
-    toks = sample_tokens(sh.T, row_src, offsets, n_random=N_RANDOM_FULL,
+    route = check_route(oracle_mod, sh, r, xb, rw, router_arith(layer, sh.T))
+    del r
+    toks = sample_tokens(sh.T, route["row_src"], route["offsets"], n_random=N_RANDOM_FULL,
                          chunk_rows=chunk_rows_of(sh.T, sh.top_k, sh.E, "mxfp8"))
     if name == "decode":
         assert toks == list(range(sh.T))
-    q = _oracle_q(oracle_mod, d, experts=np.unique(ids_o[toks]))
-    ref, _, _ = oracle_mod.forward_mxfp8(xb, rw, *q, sh.G, sh.topk_groups, sh.top_k, sh.scale,
-                                         tokens=toks)
+    q = _oracle_q(oracle_mod, d, experts=np.unique(route["ids"][toks]))
+    ref = oracle_rows(oracle_mod.forward_mxfp8, toks, route, xb, rw, *q, sh.G, sh.topk_groups,
+                      sh.top_k, sh.scale)
     rel = rel_l2_per_token(out_bits(out)[toks], ref)
     assert rel.max() <= MXFP8_TOL, (rel.max(), toks[int(rel.argmax())], len(toks))

@@ -7,8 +7,8 @@ import torch
 
 from sparse_moe_layer_experts_b300 import synth
 from sparse_moe_layer_experts_b300.layer import BeamMoE, quantize_nvfp4
-from tests._gpu_util import (N_RANDOM_FULL, chunk_rows_of, out_bits, rel_l2_per_token,
-                             sample_tokens)
+from tests._gpu_util import (N_RANDOM_FULL, check_route, chunk_rows_of, oracle_rows, out_bits,
+                             rel_l2_per_token, router_arith, sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -85,12 +85,14 @@ def test_nvfp4_forward_small_all_tokens(oracle_mod, name):
     sh = SMALL[name]
     d = synth.make_inputs(sh, seed=11, device="cuda")
     layer = _nvfp4_layer(sh, d)
+    xb, rw = synth.to_bits(d["x"]), synth.to_f32(d["router_w"])
+    route = check_route(oracle_mod, sh, layer.route(d["x"]), xb, rw, router_arith(layer, sh.T))
     out = layer.forward(d["x"])
     torch.cuda.synchronize()
     assert layer.status() == 0
     q = _oracle_q(oracle_mod, d)
-    ref, _, _ = oracle_mod.forward_nvfp4(synth.to_bits(d["x"]), synth.to_f32(d["router_w"]), *q,
-                                         sh.G, sh.topk_groups, sh.top_k, sh.scale)
+    ref = oracle_rows(oracle_mod.forward_nvfp4, list(range(sh.T)), route, xb, rw, *q, sh.G,
+                      sh.topk_groups, sh.top_k, sh.scale)
     rel = rel_l2_per_token(out_bits(out), ref)
     assert rel.max() <= NVFP4_TOL, (rel.max(), int(rel.argmax()))
 
@@ -108,7 +110,8 @@ def test_nvfp4_deterministic():
 @pytest.mark.parametrize("name", ["nvfp4", "decode"])
 def test_nvfp4_full_size_sampled(oracle_mod, name):
     """Full-size NVFP4 layer in the configuration the benchmark times, against
-    the oracle with the identical quantisation: routing of every token; layer
+    the oracle with the identical quantisation: routing of every token
+    checked; layer
     outputs of every token of the decode batch, and at T=8192 of token 0 and
     T-1, the first and last row of every non-empty expert segment, the first
     and last row of every token chunk of the most loaded expert, and 256
@@ -117,21 +120,18 @@ def test_nvfp4_full_size_sampled(oracle_mod, name):
     d = synth.make_inputs(sh, seed=0, device="cuda")
     layer = _nvfp4_layer(sh, d)
     out = layer.forward(d["x"])
-    r = layer.route(d["x"], want_scores=False)
+    r = layer.route(d["x"])
     torch.cuda.synchronize()
     assert layer.status() == 0
-    ids = r["ids"].cpu().numpy()
     xb, rw = synth.to_bits(d["x"]), synth.to_f32(d["router_w"])
-    _, s = oracle_mod.router_scores(xb, rw)
-    ids_o, _ = oracle_mod.select(s, sh.G, sh.topk_groups, sh.top_k, sh.scale)
-    assert np.array_equal(ids, ids_o)
-    _, offsets, _, row_src = oracle_mod.dispatch(ids_o, sh.E)
-    toks = sample_tokens(sh.T, row_src, offsets, n_random=N_RANDOM_FULL,
+    route = check_route(oracle_mod, sh, r, xb, rw, router_arith(layer, sh.T))
+    del r
+    toks = sample_tokens(sh.T, route["row_src"], route["offsets"], n_random=N_RANDOM_FULL,
                          chunk_rows=chunk_rows_of(sh.T, sh.top_k, sh.E, "nvfp4"))
     if name == "decode":
         assert toks == list(range(sh.T))
-    q = _oracle_q(oracle_mod, d, experts=np.unique(ids_o[toks]))
-    ref, _, _ = oracle_mod.forward_nvfp4(xb, rw, *q, sh.G, sh.topk_groups, sh.top_k, sh.scale,
-                                         tokens=toks)
+    q = _oracle_q(oracle_mod, d, experts=np.unique(route["ids"][toks]))
+    ref = oracle_rows(oracle_mod.forward_nvfp4, toks, route, xb, rw, *q, sh.G, sh.topk_groups,
+                      sh.top_k, sh.scale)
     rel = rel_l2_per_token(out_bits(out)[toks], ref)
     assert rel.max() <= NVFP4_TOL, (rel.max(), toks[int(rel.argmax())], len(toks))

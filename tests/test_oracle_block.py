@@ -89,3 +89,40 @@ def test_block_large_step_keeps_the_stream(oracle_mod):
     dev = np.linalg.norm(got - sv, axis=1)
     bound = 2 ** -8 * np.linalg.norm(sv, axis=1) + 2 ** -10 * np.sqrt(sh.H) * np.abs(gq).max()
     assert np.all(dev <= bound) and np.all(dev > 0)
+
+
+def test_block_tail_composes_to_the_block(oracle_mod):
+    # pre-norm -> layer (its FP32 combine) -> tail == the block oracle, bit
+    # for bit; and the combine rounds to the layer's bf16 output
+    sh = synth.shape("tiny", T=40)
+    d = synth.make_inputs(sh, seed=31, device="cpu")
+    h = {k: (synth.to_bits(v) if v.dtype == torch.bfloat16 else synth.to_f32(v))
+         for k, v in d.items()}
+    gp, gq = (g.numpy() for g in synth.make_block_gains(sh.H, seed=31))
+    for step, toks in ((9, None), (1, [3, 0, 39]), (400, [7])):
+        blk = oracle_mod.block_forward(h["x"], step, gp, gq, 1e-6, h["router_w"], h["w_gate"],
+                                       h["w_up"], h["w_down"], sh.G, sh.topk_groups, sh.top_k,
+                                       sh.scale, tokens=toks)
+        xn = oracle_mod.rmsnorm_bf16(h["x"], gp, 1e-6)
+        out, _, _, o = oracle_mod.forward(xn, h["router_w"], h["w_gate"], h["w_up"], h["w_down"],
+                                          sh.G, sh.topk_groups, sh.top_k, sh.scale, tokens=toks,
+                                          combine=True)
+        assert np.array_equal(out, torch.from_numpy(o).to(torch.bfloat16).view(torch.int16)
+                              .numpy().view(np.uint16))
+        tail = oracle_mod.block_tail(h["x"], step, gq, 1e-6, o, tokens=toks)
+        assert np.array_equal(tail, blk), step
+
+
+def test_quantised_layers_expose_their_combine(oracle_mod):
+    sh = synth.shape("tiny", T=16)
+    d = synth.make_inputs(sh, seed=32, device="cpu")
+    xb, rw = synth.to_bits(d["x"]), synth.to_f32(d["router_w"])
+    for quant, fwd in ((oracle_mod.quantize_nvfp4, oracle_mod.forward_nvfp4),
+                       (oracle_mod.quantize_mxfp8, oracle_mod.forward_mxfp8)):
+        q = [quant(synth.to_bits(d[k])) for k in ("w_gate", "w_up", "w_down")]
+        out, ids, w = fwd(xb, rw, *q, sh.G, sh.topk_groups, sh.top_k, sh.scale)
+        out2, ids2, w2, o = fwd(xb, rw, *q, sh.G, sh.topk_groups, sh.top_k, sh.scale,
+                                combine=True)
+        assert np.array_equal(out, out2) and np.array_equal(ids, ids2)
+        assert np.array_equal(out, torch.from_numpy(o).to(torch.bfloat16).view(torch.int16)
+                              .numpy().view(np.uint16))
