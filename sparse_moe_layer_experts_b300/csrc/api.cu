@@ -270,10 +270,11 @@ int device_sms()
             return BEAM_MOE_ERR_CUDA;            \
     } while (0)
 
-// Steps 1-6 plus histogram/scan into the workspace.
+// Steps 1-6 plus histogram/scan into the workspace.  want_scores: the
+// caller reads `scores` afterwards (else the selection may skip writing them).
 int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cfg &c,
-              const Layout &L, float *scores, int32_t *ids, float *wts, int rows_per_chunk,
-              cudaStream_t s)
+              const Layout &L, float *scores, bool want_scores, int32_t *ids, float *wts,
+              int rows_per_chunk, cudaStream_t s)
 {
     void *ws = c.workspace;
     int *status = at<int>(ws, L.status);
@@ -299,8 +300,9 @@ int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cf
         BEAM_CUDA(launch_router_scores(static_cast<const uint16_t *>(x), router_w, (int)T,
                                        c.hidden, c.n_experts, scores, status, s));
     }
-    BEAM_CUDA(launch_select(scores, partials, nsplit, (int)T, c.n_experts, c.n_groups,
-                            c.topk_groups, c.top_k, c.routed_scale, ids, wts, status, s));
+    BEAM_CUDA(launch_select(scores, partials, nsplit, want_scores, (int)T, c.n_experts,
+                            c.n_groups, c.topk_groups, c.top_k, c.routed_scale, ids, wts, status,
+                            s));
     BEAM_CUDA(launch_hist_scan(ids, (int)T, c.top_k, c.n_experts, rows_per_chunk,
                                at<int32_t>(ws, L.local_rank), at<int32_t>(ws, L.cta_counts),
                                at<int32_t>(ws, L.cta_base), at<int32_t>(ws, L.counts),
@@ -326,8 +328,8 @@ int run_forward(const void *x, const float *router_w, const void *w_gate, const 
     void *ws = c.workspace;
     const GemmVariant v = pick_variant(T, c);
     const bool fp4 = c.wtype == BEAM_MOE_W_NVFP4, mx8 = c.wtype == BEAM_MOE_W_MXFP8;
-    int rc = run_route(x, router_w, T, c, L, at<float>(ws, L.scores), at<int32_t>(ws, L.ids),
-                       at<float>(ws, L.wts), chunk_rows(T, c), s);
+    int rc = run_route(x, router_w, T, c, L, at<float>(ws, L.scores), false,
+                       at<int32_t>(ws, L.ids), at<float>(ws, L.wts), chunk_rows(T, c), s);
     if (rc != BEAM_MOE_OK)
         return rc;
     const int K = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
@@ -594,7 +596,8 @@ int beam_moe_route(const void *x, const float *router_w, int64_t T, const beam_m
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *ws = c.workspace;
     float *sc = scores ? scores : at<float>(ws, L.scores);
-    rc = run_route(x, router_w, T, c, L, sc, topk_ids, topk_w, chunk_rows(T, c), s);
+    rc = run_route(x, router_w, T, c, L, sc, scores != nullptr, topk_ids, topk_w,
+                   chunk_rows(T, c), s);
     if (rc != BEAM_MOE_OK)
         return rc;
     const int E = c.n_experts;

@@ -285,6 +285,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N)
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// 256-bit global store (8 words; the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *p, uint32_t w0, uint32_t w1, uint32_t w2,
+                                             uint32_t w3, uint32_t w4, uint32_t w5, uint32_t w6,
+                                             uint32_t w7)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w0),
+                 "r"(w1), "r"(w2), "r"(w3), "r"(w4), "r"(w5), "r"(w6), "r"(w7)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------ numerics
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b)

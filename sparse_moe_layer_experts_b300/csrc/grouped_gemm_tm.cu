@@ -390,15 +390,21 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
                             __fmul_rn(__uint_as_float(v[(2 * i + 1) / 16][(2 * i + 1) % 16]), g0));
                 }
                 if (live) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
-                                                           (size_t)row * p.out_ld + tl.m * 256 +
-                                                           128 * wg);
+                    // 256 contiguous bytes of the row in eight 256-bit stores
+                    // (the row's 32 lanes each write another row, so fewer,
+                    // wider stores keep the load/store pipe free for the
+                    // scale staging); 32-byte aligned: H * 2, the tile offset
+                    // (multiples of 256 bytes) and the 1 KB-aligned y region
+                    uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                                               (size_t)row * p.out_ld +
+                                                               tl.m * 256 + 128 * wg);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[4 * c + v] = make_uint4(w[c][4 * v], w[c][4 * v + 1],
-                                                        w[c][4 * v + 2], w[c][4 * v + 3]);
+                        for (int v = 0; v < 2; ++v)
+                            st_global_v8(dst + 64 * c + 32 * v, w[c][8 * v], w[c][8 * v + 1],
+                                         w[c][8 * v + 2], w[c][8 * v + 3], w[c][8 * v + 4],
+                                         w[c][8 * v + 5], w[c][8 * v + 6], w[c][8 * v + 7]);
                 }
             }
             acc_phase ^= 1u;

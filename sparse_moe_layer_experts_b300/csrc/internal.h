@@ -53,12 +53,14 @@ cudaError_t launch_router_tc(const float *wr, void *parts, const CUtensorMap &w_
                              float *partials, int *status, unsigned long long timeout_ns,
                              cudaStream_t s);
 // Group-limited top-k over scores -> ids [T,K], w [T,K].  With nsplit > 0
-// the scores are computed first from the router's partial logits
-// [nsplit][T][E] (summed in order, then the sigmoid) and written to scores
-// (partials may equal scores when nsplit == 1).
-cudaError_t launch_select(float *scores, const float *partials, int nsplit, int T, int E, int G,
-                          int TG, int K, float scale, int32_t *ids, float *w, int *status,
-                          cudaStream_t s);
+// the logits are first summed from the router's partials [nsplit][T][E] (in
+// order); with write_scores every score is then computed and written to
+// scores (partials may equal scores when nsplit == 1), without it only the
+// scores the selection needs are evaluated and scores is not written.  The
+// selection is the same either way.
+cudaError_t launch_select(float *scores, const float *partials, int nsplit, bool write_scores,
+                          int T, int E, int G, int TG, int K, float scale, int32_t *ids, float *w,
+                          int *status, cudaStream_t s);
 
 // ---- dispatch.cu
 constexpr int kHistTokens = 256;  // tokens per histogram CTA

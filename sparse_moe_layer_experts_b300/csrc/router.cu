@@ -257,15 +257,68 @@ router_scores_small(const uint16_t *__restrict__ x, const float *__restrict__ wr
     }
 }
 
-// One warp per token.  Lane l holds the scores of experts l, l+32, ...
-// With nsplit > 0 the scores are first made from the tensor-core router's
-// partial logits [nsplit][T][E] (l = p_0 + p_1 + ... in FP32, in that
-// order; then the sigmoid) and written to `scores`, which may be the
-// partials buffer itself when nsplit == 1 (each element is read and written
-// by the same lane).
+// Key of a float under the warp's max/min reductions: larger float, larger
+// key.  0 means "no candidate"; a NaN is never a candidate.
+__device__ __forceinline__ unsigned order_key(float f)
+{
+    if (f != f)
+        return 0u;
+    const unsigned u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(unsigned k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// One round of the warp arg-max under (value desc, index asc) over the
+// candidate bits `cand` of this lane's experts lane + 32j.  Returns the key
+// of the best value (0 if none is left) and its expert in *be; the lane
+// holding it clears its bit.
+__device__ __forceinline__ unsigned warp_argmax(const float (&val)[8], unsigned &cand, int lane,
+                                                int *be_out)
+{
+    const unsigned full = 0xFFFFFFFFu;
+    unsigned bk = 0u;
+    int be = 0x7FFFFFFF;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const unsigned k = ((cand >> j) & 1u) ? order_key(val[j]) : 0u;
+        if (k > bk) {  // j ascending: the first of equal keys has the lowest index
+            bk = k;
+            be = lane + 32 * j;
+        }
+    }
+    const unsigned best = __reduce_max_sync(full, bk);
+    be = (int)__reduce_min_sync(full, (bk == best && best != 0u) ? (unsigned)be : 0xFFFFFFFFu);
+    if (best != 0u && (be & 31) == lane)
+        cand &= ~(1u << (be >> 5));
+    *be_out = best != 0u ? be : 0;
+    return best;
+}
+
+// One warp per token.  Lane l holds the values of experts l, l+32, ...
+// Three sources of the router's scores:
+//  - nsplit == 0: the FMA-chain router wrote the FP32 scores;
+//  - nsplit > 0, write_scores: the tensor-core router's partial logits
+//    [nsplit][T][E] are added in order p = 0..nsplit-1 (FP32), the sigmoid
+//    applied to every one and the scores written (`partials` may be
+//    `scores` when nsplit == 1: each element is read and written by the
+//    same lane);
+//  - nsplit > 0, !write_scores: the same logits, but the sigmoid is
+//    evaluated only where the selection needs it.  sigmoid is monotone
+//    (non-decreasing in FP32), so a group's two largest scores are the
+//    sigmoids of its two largest logits, and the top-K experts by (score
+//    desc, index asc) are the top-K by (logit desc, index asc) re-ranked by
+//    (score, index) -- unless the next candidate's score equals the K-th
+//    (a plateau of the FP32 sigmoid, or tied logits), in which case every
+//    candidate's score is evaluated and the plain selection runs.
+// Both tensor-core modes therefore select exactly what the scores select.
 __global__ void __launch_bounds__(256)
-select_kernel(float *scores, const float *partials, int nsplit, int T, int E, int G, int TG, int K,
-              float scale, int32_t *__restrict__ ids, float *__restrict__ wts, int *status)
+select_kernel(float *scores, const float *partials, int nsplit, int write_scores, int T, int E,
+              int G, int TG, int K, float scale, int32_t *__restrict__ ids,
+              float *__restrict__ wts, int *status)
 {
     __shared__ float row_s[8][256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -275,58 +328,73 @@ select_kernel(float *scores, const float *partials, int nsplit, int T, int E, in
     const unsigned full = 0xFFFFFFFFu;
     float *s = scores + (size_t)t * E;
     const int gsize = E / G;
+    const bool lazy = nsplit > 0 && !write_scores;
 
+    // v: scores, or logits in the lazy mode.  Each pass over j issues its
+    // eight loads together (one round trip per partial, not per element).
     float v[8];
+    const float *src = nsplit > 0 ? partials + (size_t)t * E : s;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int e = lane + 32 * j;
-        if (e < E) {
-            if (nsplit > 0) {
-                const float *pl = partials + (size_t)t * E + e;
-                float l = pl[0];
-                for (int p = 1; p < nsplit; ++p)
-                    l = __fadd_rn(l, pl[(size_t)p * T * E]);
-                v[j] = router_sigmoid(l);
-                s[e] = v[j];
-            } else {
-                v[j] = s[e];
-            }
-        } else {
-            v[j] = -INFINITY;
+        v[j] = (e < E) ? src[e] : -INFINITY;
+    }
+    for (int p = 1; p < nsplit; ++p) {
+        const float *pl = partials + ((size_t)p * T + t) * E;
+        float q[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane + 32 * j;
+            q[j] = (e < E) ? pl[e] : 0.0f;
         }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = __fadd_rn(v[j], q[j]);
+    }
+    if (nsplit > 0 && !lazy) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E) {
+                v[j] = router_sigmoid(v[j]);
+                s[e] = v[j];
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e = lane + 32 * j;
         if (e < E)
             row_s[warp][e] = v[j];
     }
     __syncwarp();
 
-    // group score: the two largest scores of the group, summed in FP32
-    float gs = -INFINITY;
+    // group score: the two largest scores of the group, summed in FP32 (in
+    // the lazy mode: the sigmoids of the two largest logits)
+    float m1 = -INFINITY, m2 = -INFINITY;  // lane g < G: group g's two largest values
     if ((32 % gsize) == 0) {
         // groups are aligned runs of gsize lanes within each 32-expert row:
         // reduce (largest, second largest) pairs across the run with xor
         // shuffles, then lane g fetches group g's pair
-        float gsum[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float m1 = v[j], m2 = -INFINITY;
-            for (int off = 1; off < gsize; off <<= 1) {
-                const float o1 = __shfl_xor_sync(full, m1, off);
-                const float o2 = __shfl_xor_sync(full, m2, off);
-                const float lo = fminf(m1, o1);
-                m1 = fmaxf(m1, o1);
-                m2 = fmaxf(lo, fmaxf(m2, o2));
-            }
-            gsum[j] = (gsize == 1) ? m1 : __fadd_rn(m1, m2);
-        }
         const int src = (lane * gsize) & 31, row = (lane * gsize) >> 5;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float o = __shfl_sync(full, gsum[j], src);
-            if (lane < G && row == j)
-                gs = o;
+            float a1 = v[j], a2 = -INFINITY;
+            for (int off = 1; off < gsize; off <<= 1) {
+                const float o1 = __shfl_xor_sync(full, a1, off);
+                const float o2 = __shfl_xor_sync(full, a2, off);
+                const float lo = fminf(a1, o1);
+                a1 = fmaxf(a1, o1);
+                a2 = fmaxf(lo, fmaxf(a2, o2));
+            }
+            const float b1 = __shfl_sync(full, a1, src);
+            const float b2 = __shfl_sync(full, a2, src);
+            if (lane < G && row == j) {
+                m1 = b1;
+                m2 = b2;
+            }
         }
     } else if (lane < G) {
-        float m1 = -INFINITY, m2 = -INFINITY;
         for (int j = 0; j < gsize; ++j) {
             const float q = row_s[warp][lane * gsize + j];
             if (q > m1) {
@@ -336,7 +404,11 @@ select_kernel(float *scores, const float *partials, int nsplit, int T, int E, in
                 m2 = q;
             }
         }
-        gs = (gsize == 1) ? m1 : __fadd_rn(m1, m2);
+    }
+    float gs = -INFINITY;
+    if (lane < G) {
+        const float s1 = lazy ? router_sigmoid(m1) : m1;
+        gs = (gsize == 1) ? s1 : __fadd_rn(s1, lazy ? router_sigmoid(m2) : m2);
     }
     // rank of my group under (score desc, index asc)
     int rank = 0;
@@ -347,54 +419,85 @@ select_kernel(float *scores, const float *partials, int nsplit, int T, int E, in
     }
     const unsigned kept = __ballot_sync(full, lane < G && rank < TG);
 
-    // top-K among the kept groups' experts by repeated warp arg-max under
-    // (score desc, index asc): each lane's best candidate becomes a 32-bit
-    // key (the bits of a score >= +0 order like the score; +1 keeps 0 for
-    // "none", and a NaN score is never a candidate), a warp max picks the
-    // score and a warp min over the lanes holding it picks the lowest index
-    unsigned cand = 0;  // bit j: expert lane + 32j is in a kept group and not yet taken
+    unsigned cand0 = 0;  // bit j: expert lane + 32j is in a kept group
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int e = lane + 32 * j;
         if (e < E && ((kept >> (e / gsize)) & 1u))
-            cand |= 1u << j;
+            cand0 |= 1u << j;
     }
-    int my_e = -1;
-    float my_v = 0.0f;
-    for (int k = 0; k < K; ++k) {
-        float bv = -INFINITY;
-        int be = 0x7FFFFFFF;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = lane + 32 * j;
-            if (((cand >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
-                bv = v[j];
-                be = e;
+    int my_e = -1;     // lane k < K: the expert of slot k
+    float my_v = 0.0f;  // and its score
+    bool done = false;
+    if (lazy) {
+        // top-K candidates by (logit desc, index asc), and the next one
+        unsigned cand = cand0;
+        float my_l = 0.0f;
+        bool ok = true;
+        for (int k = 0; k < K; ++k) {
+            int be;
+            const unsigned best = warp_argmax(v, cand, lane, &be);
+            ok = ok && best != 0u;
+            if (lane == k) {
+                my_e = be;
+                my_l = key_value(best);
             }
         }
-        const unsigned key = (be != 0x7FFFFFFF && bv >= 0.0f) ? __float_as_uint(bv) + 1u : 0u;
-        const unsigned best = __reduce_max_sync(full, key);
-        be = (int)__reduce_min_sync(full, (key == best && best != 0u) ? (unsigned)be : 0xFFFFFFFFu);
-        bv = __uint_as_float(best - 1u);
-        if (best == 0u) {  // no candidate left (non-finite scores)
-            if (lane == 0)
-                atomicOr(status, kStatusDevice);
-            be = 0;
-            bv = 0.0f;
-        } else if ((be & 31) == lane) {
-            cand &= ~(1u << (be >> 5));
+        int be_next;
+        const unsigned next = warp_argmax(v, cand, lane, &be_next);
+        if (ok) {
+            if (lane < K)
+                my_v = router_sigmoid(my_l);
+            const float vK = __shfl_sync(full, my_v, K - 1);
+            // the K-th score is not shared with any later candidate
+            if (next == 0u || router_sigmoid(key_value(next)) < vK) {
+                // slot = rank under (score desc, index asc)
+                int slot = 0;
+                for (int j = 0; j < K; ++j) {
+                    const float oj = __shfl_sync(full, my_v, j);
+                    const int ej = __shfl_sync(full, my_e, j);
+                    if (oj > my_v || (oj == my_v && ej < my_e))
+                        ++slot;
+                }
+                float S = 0.0f;
+                for (int k = 0; k < K; ++k) {
+                    const unsigned m = __ballot_sync(full, lane < K && slot == k);
+                    S = __fadd_rn(S, __shfl_sync(full, my_v, __ffs(m) - 1));
+                }
+                if (lane < K) {
+                    ids[(size_t)t * K + slot] = my_e;
+                    wts[(size_t)t * K + slot] = __fmul_rn(__fdiv_rn(my_v, S), scale);
+                }
+                done = true;
+            }
         }
-        if (lane == k) {
-            my_e = be;
-            my_v = bv;
+        if (!done) {  // a plateau or tie at the boundary: every candidate's score
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = ((cand0 >> j) & 1u) ? router_sigmoid(v[j]) : -INFINITY;
         }
     }
-    float S = 0.0f;
-    for (int k = 0; k < K; ++k)
-        S = __fadd_rn(S, __shfl_sync(full, my_v, k));
-    if (lane < K) {
-        ids[(size_t)t * K + lane] = my_e;
-        wts[(size_t)t * K + lane] = __fmul_rn(__fdiv_rn(my_v, S), scale);
+    if (!done) {
+        // top-K among the kept groups' experts by repeated warp arg-max under
+        // (score desc, index asc)
+        unsigned cand = cand0;
+        for (int k = 0; k < K; ++k) {
+            int be;
+            const unsigned best = warp_argmax(v, cand, lane, &be);
+            if (best == 0u && lane == 0)  // no candidate left (non-finite scores)
+                atomicOr(status, kStatusDevice);
+            if (lane == k) {
+                my_e = be;
+                my_v = best != 0u ? key_value(best) : 0.0f;
+            }
+        }
+        float S = 0.0f;
+        for (int k = 0; k < K; ++k)
+            S = __fadd_rn(S, __shfl_sync(full, my_v, k));
+        if (lane < K) {
+            ids[(size_t)t * K + lane] = my_e;
+            wts[(size_t)t * K + lane] = __fmul_rn(__fdiv_rn(my_v, S), scale);
+        }
     }
 }
 
@@ -425,13 +528,13 @@ cudaError_t launch_router_scores(const uint16_t *x, const float *wr, int T, int 
     return cudaGetLastError();
 }
 
-cudaError_t launch_select(float *scores, const float *partials, int nsplit, int T, int E, int G,
-                          int TG, int K, float scale, int32_t *ids, float *w, int *status,
-                          cudaStream_t s)
+cudaError_t launch_select(float *scores, const float *partials, int nsplit, bool write_scores,
+                          int T, int E, int G, int TG, int K, float scale, int32_t *ids, float *w,
+                          int *status, cudaStream_t s)
 {
     stage_begin(kStSelect, s);
-    select_kernel<<<(T + 7) / 8, 256, 0, s>>>(scores, partials, nsplit, T, E, G, TG, K, scale, ids,
-                                             w, status);
+    select_kernel<<<(T + 7) / 8, 256, 0, s>>>(scores, partials, nsplit, write_scores ? 1 : 0, T, E,
+                                             G, TG, K, scale, ids, w, status);
     stage_end(kStSelect, s);
     return cudaGetLastError();
 }

@@ -91,3 +91,57 @@ def test_deterministic_across_calls_and_streams():
     s.synchronize()
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def _route_both(layer, x):
+    a = layer.route(x, want_scores=True)    # every score evaluated and written
+    b = layer.route(x, want_scores=False)   # only the scores the selection needs
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    for k in ("ids", "w", "counts", "offsets", "row_of"):
+        ua, ub = a[k].cpu().numpy(), b[k].cpu().numpy()
+        assert np.array_equal(ua.view(np.uint32), ub.view(np.uint32)), k
+    return a
+
+
+@pytest.mark.parametrize("case", ["prefill", "one_hot", "zero_x", "saturated", "e36", "g4_24"])
+def test_lazy_sigmoid_selection_equals_full(oracle_mod, case):
+    """The selection without written scores evaluates the sigmoid only for
+    each group's two largest logits and the top-K candidates, falling back
+    to every candidate on a plateau of the FP32 sigmoid or tied logits.  It
+    must select exactly what the full evaluation selects, and that must be
+    the oracle's selection on the same scores."""
+    if case == "prefill":
+        sh = synth.shape("prefill")
+        d = synth.make_inputs(sh, seed=9, device="cuda", weights=False)
+        x, w = d["x"], d["router_w"]
+    elif case == "one_hot":
+        sh = synth.LayerShape(T=4096, H=512, I=128, E=256, G=8, topk_groups=4, top_k=8)
+        xc, wc = _one_hot_inputs(sh.T, sh.H, sh.E, seed=5)
+        x, w = xc.cuda().contiguous(), wc.cuda().contiguous()
+    elif case == "zero_x":
+        # every logit 0: every score 0.5, all ties resolved by index
+        sh = synth.LayerShape(T=512, H=256, I=128, E=256, G=8, topk_groups=4, top_k=8)
+        x = torch.zeros(sh.T, sh.H, dtype=torch.bfloat16, device="cuda")
+        w = torch.randn(sh.H, sh.E, device="cuda") * 0.02
+    elif case == "saturated":
+        # logits of +-20..60: most scores round to exactly 1.0 or to tiny values
+        sh = synth.LayerShape(T=1024, H=256, I=128, E=256, G=8, topk_groups=4, top_k=8)
+        g = torch.Generator(device="cuda").manual_seed(3)
+        x = torch.randn(sh.T, sh.H, generator=g, device="cuda").to(torch.bfloat16)
+        w = torch.randn(sh.H, sh.E, generator=g, device="cuda") * 2.5
+    elif case == "e36":
+        sh = synth.LayerShape(T=700, H=256, I=128, E=36, G=4, topk_groups=2, top_k=4)
+        d = synth.make_inputs(sh, seed=2, device="cuda", weights=False)
+        x, w = d["x"], d["router_w"]
+    else:  # groups of 24 experts: the group stage's non-shuffle branch
+        sh = synth.LayerShape(T=900, H=256, I=128, E=96, G=4, topk_groups=2, top_k=6, scale=1.5)
+        d = synth.make_inputs(sh, seed=4, device="cuda", weights=False)
+        x, w = d["x"], d["router_w"]
+    layer = _router_only_layer(sh, w)
+    assert B.beam_moe_router_arith(sh.T, layer.cfg) == B.BEAM_MOE_ROUTER_TENSOR
+    a = _route_both(layer, x)
+    g = a["scores"].cpu().numpy()
+    ids, wts = oracle_mod.select(g, sh.G, sh.topk_groups, sh.top_k, sh.scale)
+    assert np.array_equal(a["ids"].cpu().numpy(), ids)
+    assert np.array_equal(a["w"].cpu().numpy().view(np.uint32), wts.view(np.uint32))
