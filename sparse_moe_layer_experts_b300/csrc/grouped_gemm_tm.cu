@@ -30,7 +30,10 @@
 // shared memory and writes them into tensor memory with tcgen05.st (each
 // warp its lane quarter: lane 32q + i, columns c..c+3 = words 0-3 of atom
 // row i, the layout a 32x128b.warpx4 copy produces), then signals the MMA
-// thread; the tensor pipe then runs only MMAs.  Without SFST the MMA thread
+// thread; the tensor pipe then runs only MMAs.  The producer issues a
+// stage's scale atoms before its operand tiles and counts them on a barrier
+// of their own, so the staging overlaps the operand copies instead of
+// following them.  Without SFST the MMA thread
 // copies the atoms with tcgen05.cp.  NVFP4 (12 atoms per k-step) uses SFST;
 // MXFP8 (3 atoms per four MMAs) copies, which measured faster there.
 //
@@ -76,7 +79,8 @@ struct TmCfg {
     static constexpr int SF_COL0 = ACC_COLS;
     static constexpr int COLS_NEED = SF_COL0 + STAGES * SF_COLS;
     static constexpr int TMEM_COLS = COLS_NEED <= 256 ? 256 : 512;
-    static constexpr int N_BARS = 3 * STAGES + 3;
+    // full, empty, sfready per stage; tfull, tempty, drain; sffull per stage
+    static constexpr int N_BARS = 4 * STAGES + 3;
     static constexpr int AUX_BYTES = N_BARS * 8 + 16 + 2 * (kMaxExperts + 1) * 4;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + ((AUX_BYTES + 127) / 128) * 128;
     static_assert(SF_COL0 % 8 == 0 && SF_COLS % 8 == 0 && SFA_COLS % 8 == 0,
@@ -121,6 +125,9 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint32_t tfull_bar = bar_u32 + 8u * (3 * STAGES);
     const uint32_t tempty_bar = bar_u32 + 8u * (3 * STAGES + 1);
     const uint32_t drain_bar = bar_u32 + 8u * (3 * STAGES + 2);
+    // SFST: the stage's scale atoms complete on their own barrier, so the
+    // scale warpgroup stages them while the operand tiles are still landing
+    auto sffull_bar = [&](int s) { return bar_u32 + 8u * (3 * STAGES + 3 + s); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
@@ -131,6 +138,7 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
             mbar_init(sfready_bar(s), 4);  // one arrive per scale warp
+            mbar_init(sffull_bar(s), 1);
         }
         mbar_init(tfull_bar, 1);
         mbar_init(tempty_bar, 128 * kEpiWG);
@@ -186,22 +194,28 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(stage),
-                                          (uint32_t)(C::A_BYTES + C::B_BYTES + 3 * nkb * kAtom));
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                     const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
                     const uint32_t sb = st + C::A_BYTES;
                     const uint32_t sf = sb + C::B_BYTES;
+                    // scales first (on their own barrier with SFST), then the
+                    // operand tiles
+                    const uint32_t sbar = SFST ? sffull_bar(stage) : full_bar(stage);
+                    if (SFST) {
+                        mbar_arrive_expect_tx(sbar, (uint32_t)(3 * nkb * kAtom));
+                        mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(C::A_BYTES + C::B_BYTES));
+                    } else {
+                        mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(C::A_BYTES + C::B_BYTES +
+                                                                          3 * nkb * kAtom));
+                    }
+                    bulk_g2s(sf, sfa + (size_t)atom0 * kAtom, nkb * kAtom, sbar);
+                    bulk_g2s(sf + C::SF_OP, sfb0 + (size_t)atom0 * kAtom, nkb * kAtom, sbar);
+                    bulk_g2s(sf + 2 * C::SF_OP, sfb1 + (size_t)atom0 * kAtom, nkb * kAtom, sbar);
                     tma_load_2d(st, &tmA, k * kRowBytes, tl.row0, full_bar(stage));
                     tma_load_2d(sb, &tmB0, k * kRowBytes, w0 * kBlockM, full_bar(stage));
                     tma_load_2d(sb + 128 * kRowBytes, GATEUP ? &tmB1 : &tmB0, k * kRowBytes,
                                 w1 * kBlockM, full_bar(stage));
-                    bulk_g2s(sf, sfa + (size_t)atom0 * kAtom, nkb * kAtom, full_bar(stage));
-                    bulk_g2s(sf + C::SF_OP, sfb0 + (size_t)atom0 * kAtom, nkb * kAtom,
-                             full_bar(stage));
-                    bulk_g2s(sf + 2 * C::SF_OP, sfb1 + (size_t)atom0 * kAtom, nkb * kAtom,
-                             full_bar(stage));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -210,8 +224,11 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             if (!ok)
                 for (int s = 0; s < STAGES; ++s)
-                    if ((armed >> s) & 1u)
+                    if ((armed >> s) & 1u) {
                         mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, tmo);
+                        if (SFST)
+                            mbar_wait_drain(sffull_bar(s), (armed_par >> s) & 1u, tmo);
+                    }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -419,7 +436,7 @@ grouped_gemm_tm_kernel(const __grid_constant__ CUtensorMap tmA,
         bool ok = true;
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
             for (int k = 0; k < p.ksteps; ++k) {
-                if (!mbar_wait_bounded(full_bar(stage), phase, tmo, s_abort, p.status)) {
+                if (!mbar_wait_bounded(sffull_bar(stage), phase, tmo, s_abort, p.status)) {
                     ok = false;
                     break;
                 }
