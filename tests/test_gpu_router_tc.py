@@ -145,3 +145,24 @@ def test_lazy_sigmoid_selection_equals_full(oracle_mod, case):
     ids, wts = oracle_mod.select(g, sh.G, sh.topk_groups, sh.top_k, sh.scale)
     assert np.array_equal(a["ids"].cpu().numpy(), ids)
     assert np.array_equal(a["w"].cpu().numpy().view(np.uint32), wts.view(np.uint32))
+
+
+@pytest.mark.parametrize("T", [255, 256, 300, 1000, 2304])
+def test_beam_router_around_the_threshold_and_eight_way_split(oracle_mod, T):
+    """Beam sizes (H=5120, E=256) at small batches: T=255 takes the FMA-chain
+    router (scores bit-exact); from T=256 the tensor cores with the hidden
+    dimension split 8 ways (one or a few 256-token tiles leave most SMs
+    free), checked against the FP32 accumulation bound, the selection
+    bit-exact given the scores, and the near-tie count."""
+    from tests._gpu_util import check_route
+    sh = synth.shape("decode", T=T)
+    d = synth.make_inputs(sh, seed=T, device="cuda", weights=False)
+    layer = _router_only_layer(sh, d["router_w"])
+    arith = B.beam_moe_router_arith(T, layer.cfg)
+    assert arith == (B.BEAM_MOE_ROUTER_TENSOR if T >= 256 else B.BEAM_MOE_ROUTER_FMA_CHAIN)
+    r = layer.route(d["x"])
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    check_route(oracle_mod, sh, r, synth.to_bits(d["x"]), synth.to_f32(d["router_w"]), arith)
+    # the lazy selection (no scores written) agrees
+    _route_both(layer, d["x"])
