@@ -24,8 +24,9 @@
 // so the hidden dimension is split into S ranges (S a power of two chosen
 // on the host): CTA (tile, s) sums its range and stores FP32 partial
 // logits [S][T][E]; the selection kernel adds the S partials in order
-// s = 0..S-1 and applies the sigmoid.  With S = 1 the partials are the
-// logits themselves, stored straight into the scores buffer.
+// s = 0..S-1 and applies the sigmoid where the selection needs it (to every
+// logit when the caller asks for the scores).  With S = 1 the partials are
+// the logits themselves, stored straight into the scores buffer.
 // Warp 0 produces, warp 1 owns tensor memory and issues the MMAs, warps 2-5
 // read the accumulator and store it.
 #include "common.cuh"
