@@ -273,10 +273,10 @@ __device__ __forceinline__ float key_value(unsigned k)
 }
 
 // One round of the warp arg-max under (value desc, index asc) over the
-// candidate bits `cand` of this lane's experts lane + 32j.  Returns the key
-// of the best value (0 if none is left) and its expert in *be; the lane
-// holding it clears its bit.
-__device__ __forceinline__ unsigned warp_argmax(const float (&val)[8], unsigned &cand, int lane,
+// candidate bits `cand` of this lane's experts lane + 32j, whose order keys
+// are key[j].  Returns the key of the best value (0 if none is left) and its
+// expert in *be; the lane holding it clears its bit.
+__device__ __forceinline__ unsigned warp_argmax(const unsigned (&key)[8], unsigned &cand, int lane,
                                                 int *be_out)
 {
     const unsigned full = 0xFFFFFFFFu;
@@ -284,7 +284,7 @@ __device__ __forceinline__ unsigned warp_argmax(const float (&val)[8], unsigned 
     int be = 0x7FFFFFFF;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const unsigned k = ((cand >> j) & 1u) ? order_key(val[j]) : 0u;
+        const unsigned k = ((cand >> j) & 1u) ? key[j] : 0u;
         if (k > bk) {  // j ascending: the first of equal keys has the lowest index
             bk = k;
             be = lane + 32 * j;
@@ -372,7 +372,27 @@ select_kernel(float *scores, const float *partials, int nsplit, int write_scores
     // group score: the two largest scores of the group, summed in FP32 (in
     // the lazy mode: the sigmoids of the two largest logits)
     float m1 = -INFINITY, m2 = -INFINITY;  // lane g < G: group g's two largest values
-    if ((32 % gsize) == 0) {
+    unsigned key[8];  // order keys of v, for the warp reductions
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        key[j] = order_key(v[j]);
+    if (gsize == 32) {
+        // group j is row j: its largest value is a warp max over the keys,
+        // the second the max over the other lanes (the same value again if
+        // two lanes hold the largest)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j >= G)
+                break;
+            const unsigned k1 = __reduce_max_sync(full, key[j]);
+            const unsigned twice = __popc(__ballot_sync(full, key[j] == k1)) > 1;
+            const unsigned k2 = twice ? k1 : __reduce_max_sync(full, key[j] == k1 ? 0u : key[j]);
+            if (lane == j) {
+                m1 = key_value(k1);
+                m2 = key_value(k2);
+            }
+        }
+    } else if ((32 % gsize) == 0) {
         // groups are aligned runs of gsize lanes within each 32-expert row:
         // reduce (largest, second largest) pairs across the run with xor
         // shuffles, then lane g fetches group g's pair
@@ -436,7 +456,7 @@ select_kernel(float *scores, const float *partials, int nsplit, int write_scores
         bool ok = true;
         for (int k = 0; k < K; ++k) {
             int be;
-            const unsigned best = warp_argmax(v, cand, lane, &be);
+            const unsigned best = warp_argmax(key, cand, lane, &be);
             ok = ok && best != 0u;
             if (lane == k) {
                 my_e = be;
@@ -444,7 +464,7 @@ select_kernel(float *scores, const float *partials, int nsplit, int write_scores
             }
         }
         int be_next;
-        const unsigned next = warp_argmax(v, cand, lane, &be_next);
+        const unsigned next = warp_argmax(key, cand, lane, &be_next);
         if (ok) {
             if (lane < K)
                 my_v = router_sigmoid(my_l);
@@ -473,8 +493,10 @@ select_kernel(float *scores, const float *partials, int nsplit, int write_scores
         }
         if (!done) {  // a plateau or tie at the boundary: every candidate's score
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < 8; ++j) {
                 v[j] = ((cand0 >> j) & 1u) ? router_sigmoid(v[j]) : -INFINITY;
+                key[j] = order_key(v[j]);
+            }
         }
     }
     if (!done) {
@@ -483,7 +505,7 @@ select_kernel(float *scores, const float *partials, int nsplit, int write_scores
         unsigned cand = cand0;
         for (int k = 0; k < K; ++k) {
             int be;
-            const unsigned best = warp_argmax(v, cand, lane, &be);
+            const unsigned best = warp_argmax(key, cand, lane, &be);
             if (best == 0u && lane == 0)  // no candidate left (non-finite scores)
                 atomicOr(status, kStatusDevice);
             if (lane == k) {
