@@ -289,8 +289,12 @@ int run_route(const void *x, const float *router_w, int64_t T, const beam_moe_cf
         if (nsplit > 1)
             partials = at<float>(ws, L.router_partials);
         CUtensorMap mw, mx;
-        if (!make_map(&mw, at<void>(ws, L.wr_parts), c.hidden, (uint64_t)3 * c.n_experts, 128) ||
-            !make_map(&mx, x, c.hidden, (uint64_t)T, 256))
+        // 32-deep boxes with the 64-byte swizzle the router's descriptors name
+        if (!make_map_2d(&mw, at<void>(ws, L.wr_parts), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                         c.hidden, (uint64_t)3 * c.n_experts, 32, 128,
+                         CU_TENSOR_MAP_SWIZZLE_64B) ||
+            !make_map_2d(&mx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.hidden, (uint64_t)T, 32,
+                         256, CU_TENSOR_MAP_SWIZZLE_64B))
             return BEAM_MOE_ERR_CUDA;
         const unsigned long long tmo =
             c.wait_timeout_ns > 0 ? (unsigned long long)c.wait_timeout_ns : kDefaultTimeoutNs;

@@ -182,15 +182,18 @@ router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr
 
 // Small batches (decode): each output's 5,120-long FMA chain is the critical
 // path and there are few outputs (T x E), so the work is spread thin: a CTA
-// is one warp owning 8 tokens x 8 experts, and lane (tt, ep) runs two
-// independent chains, experts e0 + 2ep and e0 + 2ep + 1 of token t0 + tt
-// (T=32 fills 128 SMs).  Per 8 hidden values a lane issues one 128-bit load
-// of x, eight 64-bit loads of weight pairs and 16 FMAs.  K chunks of 64 flow
-// through a 12-stage cp.async ring (a chunk is ~300 cycles of chain, so the
-// ring runs ~1.5 us ahead of the loads' latency).
-constexpr int kSTM = 8, kSTE = 8, kSKC = 64, kSNS = 12, kSXP = kSKC + 8;
+// of two warps owns 8 tokens x 8 experts, and thread (w, tt, ep) runs the one
+// chain of token t0 + tt and expert e0 + 2ep + w (T=32: 128 CTAs, 8,192
+// threads, one chain each).  The two warps sit on two of the SM's four
+// schedulers, so a chain's FMA issues every ~4 cycles, its latency, instead
+// of sharing one scheduler with a second chain and the loads.  Per 8 hidden
+// values a thread issues one 128-bit load of x, eight 32-bit weight loads
+// and 8 FMAs.  K chunks of 64 flow through a 12-stage cp.async ring filled
+// by both warps (a chunk is ~300 cycles of chain, so the ring runs ~1.5 us
+// ahead of the loads' latency).
+constexpr int kSTM = 8, kSTE = 8, kSKC = 64, kSNS = 12, kSXP = kSKC + 8, kSThreads = 64;
 
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(kSThreads)
 router_scores_small(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H,
                     int E, float *__restrict__ scores, int *status)
 {
@@ -198,26 +201,27 @@ router_scores_small(const uint16_t *__restrict__ x, const float *__restrict__ wr
         *status = 0;
     __shared__ __align__(16) uint16_t xs[kSNS][kSTM][kSXP];
     __shared__ __align__(16) float ws[kSNS][kSKC][kSTE];
-    const int lane = threadIdx.x;
-    const int tt = lane >> 2, ep = lane & 3;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int tt = lane >> 2, el = 2 * (lane & 3) + w;  // token and expert within the tile
     const int t0 = blockIdx.x * kSTM, e0 = blockIdx.y * kSTE;
     const int nk = H / kSKC;
 
     auto load = [&](int st, int k0) {
-        // x: 8 rows x 8 chunks of 16 B; w: 64 rows x two 16-B chunks (4 experts each)
-#pragma unroll
-        for (int c = lane; c < kSTM * (kSKC / 8); c += 32) {
-            const int r = c >> 3, q = c & 7;
+        // x: 8 rows x 8 chunks of 16 B (one per thread); w: 64 rows x two
+        // 16-B chunks of 4 experts (two per thread)
+        {
+            const int r = tid >> 3, q = tid & 7;
             const bool ok = t0 + r < T;
             cp_async16(&xs[st][r][q * 8], x + (size_t)(ok ? t0 + r : 0) * H + k0 + q * 8, ok);
         }
 #pragma unroll
-        for (int c = lane; c < kSKC * 2; c += 32) {
+        for (int c = tid; c < kSKC * 2; c += kSThreads) {
             const int r = c >> 1, h4 = (c & 1) * 4;
             const bool ok = e0 + h4 < E;
             cp_async16(&ws[st][r][h4], wr + (size_t)(k0 + r) * E + (ok ? e0 + h4 : 0), ok);
         }
     };
+    static_assert(kSTM * (kSKC / 8) == kSThreads, "one 16-byte x chunk per thread");
 
 #pragma unroll
     for (int s = 0; s < kSNS - 1; ++s) {
@@ -225,10 +229,12 @@ router_scores_small(const uint16_t *__restrict__ x, const float *__restrict__ wr
             load(s, s * kSKC);
         cp_async_commit();
     }
-    float acc0 = 0.0f, acc1 = 0.0f;
+    float acc = 0.0f;
     for (int kc = 0; kc < nk; ++kc) {
         cp_async_wait<kSNS - 2>();
-        __syncwarp();
+        // every thread's copies of chunk kc have landed, and every thread has
+        // finished chunk kc - 1, whose stage the next load overwrites
+        __syncthreads();
         if (kc + kSNS - 1 < nk)
             load((kc + kSNS - 1) % kSNS, (kc + kSNS - 1) * kSKC);
         cp_async_commit();
@@ -241,20 +247,13 @@ router_scores_small(const uint16_t *__restrict__ x, const float *__restrict__ wr
             for (int i = 0; i < 8; ++i) {
                 const float xf = (i & 1) ? __uint_as_float(xw[i >> 1] & 0xFFFF0000u)
                                          : __uint_as_float(xw[i >> 1] << 16);
-                const float2 w2 = *reinterpret_cast<const float2 *>(&ws[st][k8 + i][2 * ep]);
-                acc0 = __fmaf_rn(xf, w2.x, acc0);
-                acc1 = __fmaf_rn(xf, w2.y, acc1);
+                acc = __fmaf_rn(xf, ws[st][k8 + i][el], acc);
             }
         }
-        __syncwarp();
     }
-    const int t = t0 + tt, e = e0 + 2 * ep;
-    if (t < T) {
-        if (e < E)
-            scores[(size_t)t * E + e] = router_sigmoid(acc0);
-        if (e + 1 < E)
-            scores[(size_t)t * E + e + 1] = router_sigmoid(acc1);
-    }
+    const int t = t0 + tt, e = e0 + el;
+    if (t < T && e < E)
+        scores[(size_t)t * E + e] = router_sigmoid(acc);
 }
 
 // Key of a float under the warp's max/min reductions: larger float, larger
@@ -544,7 +543,7 @@ cudaError_t launch_router_scores(const uint16_t *x, const float *wr, int T, int 
         router_scores_large<4, 4><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
     } else {
         dim3 grid((T + kSTM - 1) / kSTM, (E + kSTE - 1) / kSTE);
-        router_scores_small<<<grid, 32, 0, s>>>(x, wr, T, H, E, scores, status);
+        router_scores_small<<<grid, kSThreads, 0, s>>>(x, wr, T, H, E, scores, status);
     }
     stage_end(kStRouter, s);
     return cudaGetLastError();

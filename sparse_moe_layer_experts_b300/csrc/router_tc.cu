@@ -17,8 +17,9 @@
 //
 // Tile: 128 experts (MMA M, one expert per TMEM lane) x 256 tokens (MMA N,
 // the widest MMA, which costs about as much per instruction as narrower
-// ones), K = H in 64-wide stages (one 128-byte swizzled row per operand row).
-// Per stage: the three 128 x 64 weight parts and the 256 x 64 x tile by TMA;
+// ones), K = H in 32-deep stages (one 64-byte swizzled row per operand row,
+// so that five 40 KB stages fit and four are in flight while the MMAs run).
+// Per stage: the three 128 x 32 weight parts and the 256 x 32 x tile by TMA;
 // per 16-deep k step three MMAs (hi, mid, lo) into one FP32 accumulator.
 // Small batches leave SMs idle with one CTA per (expert tile, token tile),
 // so the hidden dimension is split into S ranges (S a power of two chosen
@@ -42,10 +43,10 @@ namespace {
 
 constexpr int kRE = 128;    // experts per tile (MMA M)
 constexpr int kRN = 256;    // tokens per tile (MMA N)
-constexpr int kRK = 64;     // bf16 per swizzled row
+constexpr int kRK = 32;     // bf16 per swizzled row (64 bytes)
 constexpr int kParts = 3;   // hi, mid, lo
 constexpr int kRThreads = 192;
-constexpr int kRStages = 2;
+constexpr int kRStages = 5;
 
 struct RCfg {
     static constexpr int PART_BYTES = kRE * kRK * 2;
@@ -57,8 +58,25 @@ struct RCfg {
     static constexpr int N_BARS = 2 * STAGES + 2;  // full, empty, accumulator full, drain
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + N_BARS * 8 + 16;
     static_assert(STAGE_BYTES % 1024 == 0 && PART_BYTES % 1024 == 0, "swizzle atoms");
+    static_assert(kRK * 2 == 64, "the tensor maps and descriptors use the 64-byte swizzle");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
+
+// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
+// the 64-byte swizzle: rows of 32 bf16 (64 B), 8-row atoms of 512 B.
+//   bits  0-13 start address >> 4     bits 16-29 leading byte offset >> 4
+//   bits 32-45 stride byte offset >> 4 (512 B between 8-row atoms)
+//   bits 46-47 descriptor version (1)  bits 61-63 layout (4 = 64B swizzle)
+__device__ __forceinline__ uint64_t smem_desc_k64sw(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(16u >> 4) << 16;
+    d |= static_cast<uint64_t>(512u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(4u) << 61;
+    return d;
+}
 
 // Wr [H,E] fp32 (hidden-major) -> parts [3][E][H] bf16 (K-major rows of the
 // MMA's B operand).  32 x 32 tiles through shared memory so both the reads
@@ -199,10 +217,10 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                 const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < kRK / 16; ++kk) {
-                    const uint64_t bd = smem_desc_k128(sb + kk * 32);
+                    const uint64_t bd = smem_desc_k64sw(sb + kk * 32);
 #pragma unroll
                     for (int p = 0; p < kParts; ++p)
-                        mma_bf16_ss(tmem_base, smem_desc_k128(sa + p * C::PART_BYTES + kk * 32), bd,
+                        mma_bf16_ss(tmem_base, smem_desc_k64sw(sa + p * C::PART_BYTES + kk * 32), bd,
                                     idesc, (k != k_begin || kk != 0 || p != 0) ? 1u : 0u);
                 }
                 mma_commit(empty_bar(stage));
@@ -258,7 +276,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 int router_tc_splits(int64_t T, int E, int H, int sms)
 {
     // the largest power of two that keeps the CTA count within the SMs and
-    // gives every split at least one 64-deep k step
+    // gives every split at least one 32-deep k step
     const int64_t tiles = ((T + kRN - 1) / kRN) * ((E + kRE - 1) / kRE);
     int s = 1;
     while (s < kRouterMaxSplits && tiles * 2 * s <= sms && 2 * s <= H / kRK)
