@@ -42,155 +42,17 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Large batches: register-tiled FP32 GEMM, 16x16 threads, RM x RE outputs per
-// thread (CTA tile 16RM tokens x 16RE experts), K chunks of 16 double-buffered
-// in shared memory.  The next chunk of router weights streams in by cp.async
-// and the next x chunk through registers (bf16 -> FP32); inside a chunk the
-// fragments of step k+1 are loaded while step k's FMAs issue.  Every
-// accumulator walks h = 0..H-1 in order, so the tiling does not change any
-// result.
-constexpr int kLKC = 16;
-
-// Q consecutive floats (Q = 4: one 16-byte load, Q = 2: one 8-byte load)
-template <int Q>
-__device__ __forceinline__ void load_quad_or_pair(const float *p, float *dst)
-{
-    if constexpr (Q == 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(p);
-        dst[0] = v.x;
-        dst[1] = v.y;
-        dst[2] = v.z;
-        dst[3] = v.w;
-    } else {
-        const float2 v = *reinterpret_cast<const float2 *>(p);
-        dst[0] = v.x;
-        dst[1] = v.y;
-    }
-}
-
-template <int RM, int RE>
-__global__ void __launch_bounds__(256, 2)
-router_scores_large(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H,
-                    int E, float *__restrict__ scores, int *status)
-{
-    // a thread's RM tokens (and RE experts) sit in two halves of the tile,
-    // QM (QE) consecutive in each
-    constexpr int TM = 16 * RM, TE = 16 * RE, HM = TM / 2, HE = TE / 2, QM = RM / 2,
-                  QE = RE / 2;
-    static_assert((RM == 4 || RM == 8) && (RE == 4 || RE == 8), "thread tile");
-    if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-        *status = 0;
-    __shared__ __align__(16) float xs[2][kLKC][TM + 4];
-    __shared__ __align__(16) float ws[2][kLKC][TE];
-    const int tid = threadIdx.x;
-    const int tx = tid & 15, ty = tid >> 4;
-    const int t0 = blockIdx.x * TM, e0 = blockIdx.y * TE;
-    constexpr int XV = TM * 2;                // 16-byte x vectors per chunk (<= 256)
-    constexpr int WPT = kLKC * TE / 4 / 256;  // float4 of w per thread
-    static_assert(XV <= 256 && WPT >= 1, "loaders");
-    uint4 xq = make_uint4(0, 0, 0, 0);
-    auto xload = [&](int k0) {
-        const int r = tid >> 1, col = (tid & 1) * 8;
-        if (tid < XV)
-            xq = (t0 + r < T) ? *reinterpret_cast<const uint4 *>(x + (size_t)(t0 + r) * H + k0 + col)
-                              : make_uint4(0, 0, 0, 0);
-    };
-    auto xstore = [&](int b) {
-        if (tid < XV) {
-            const int r = tid >> 1, col = (tid & 1) * 8;
-            const uint32_t q[4] = {xq.x, xq.y, xq.z, xq.w};
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                xs[b][col + 2 * p][r] = bf16_bits_to_f32(q[p] & 0xFFFFu);
-                xs[b][col + 2 * p + 1][r] = bf16_bits_to_f32(q[p] >> 16);
-            }
-        }
-    };
-    auto wasync = [&](int b, int k0) {
-#pragma unroll
-        for (int v = 0; v < WPT; ++v) {
-            const int c = tid + v * 256;
-            const int r = c / (TE / 4), col = (c % (TE / 4)) * 4;
-            float *dst = &ws[b][r][col];
-            if (e0 + col < E) {
-                const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d),
-                             "l"(wr + (size_t)(k0 + r) * E + e0 + col)
-                             : "memory");
-            } else {
-                *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    float acc[RM][RE];
-#pragma unroll
-    for (int i = 0; i < RM; ++i)
-#pragma unroll
-        for (int j = 0; j < RE; ++j)
-            acc[i][j] = 0.0f;
-    const int nk = H / kLKC;
-    wasync(0, 0);
-    xload(0);
-    xstore(0);
-    cp_async_wait<0>();
-    __syncthreads();
-    for (int kc = 0; kc < nk; ++kc) {
-        const int b = kc & 1;
-        if (kc + 1 < nk) {
-            wasync(b ^ 1, (kc + 1) * kLKC);
-            xload((kc + 1) * kLKC);
-        }
-        float a[2][RM], bb[2][RE];
-        auto frag = [&](int s, int k) {
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                load_quad_or_pair<QM>(&xs[b][k][h2 * HM + ty * QM], &a[s][h2 * QM]);
-                load_quad_or_pair<QE>(&ws[b][k][h2 * HE + tx * QE], &bb[s][h2 * QE]);
-            }
-        };
-        frag(0, 0);
-#pragma unroll
-        for (int k = 0; k < kLKC; ++k) {
-            if (k + 1 < kLKC)
-                frag((k + 1) & 1, k + 1);
-#pragma unroll
-            for (int i = 0; i < RM; ++i)
-#pragma unroll
-                for (int j = 0; j < RE; ++j)
-                    acc[i][j] = __fmaf_rn(a[k & 1][i], bb[k & 1][j], acc[i][j]);
-        }
-        if (kc + 1 < nk) {
-            xstore(b ^ 1);
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < RM; ++i) {
-        const int t = t0 + (i / QM) * HM + ty * QM + (i % QM);
-        if (t >= T)
-            continue;
-#pragma unroll
-        for (int j = 0; j < RE; ++j) {
-            const int e = e0 + (j / QE) * HE + tx * QE + (j % QE);
-            if (e < E)
-                scores[(size_t)t * E + e] = router_sigmoid(acc[i][j]);
-        }
-    }
-}
-
-// Small batches (decode): each output's 5,120-long FMA chain is the critical
-// path and there are few outputs (T x E), so the work is spread thin: a CTA
-// of two warps owns 8 tokens x 8 experts, and thread (w, tt, ep) runs the one
-// chain of token t0 + tt and expert e0 + 2ep + w (T=32: 128 CTAs, 8,192
-// threads, one chain each).  The two warps sit on two of the SM's four
-// schedulers, so a chain's FMA issues every ~4 cycles, its latency, instead
-// of sharing one scheduler with a second chain and the loads.  Per 8 hidden
-// values a thread issues one 128-bit load of x, eight 32-bit weight loads
-// and 8 FMAs.  K chunks of 64 flow through a 12-stage cp.async ring filled
-// by both warps (a chunk is ~300 cycles of chain, so the ring runs ~1.5 us
-// ahead of the loads' latency).
+// Batches below the tensor-core threshold: each output's 5,120-long FMA chain
+// is the critical path and there are few outputs (T x E), so the work is
+// spread thin: a CTA of two warps owns 8 tokens x 8 experts, and thread
+// (w, tt, ep) runs the one chain of token t0 + tt and expert e0 + 2ep + w
+// (T=32: 128 CTAs, 8,192 threads, one chain each, the two warps of a CTA on
+// two of the SM's four schedulers; T=255: 1,024 CTAs, five per SM).  Per 8
+// hidden values a thread issues one 128-bit load of x, eight 32-bit weight
+// loads, 8 unpacks and 8 FMAs: about 4 instructions per hidden value at
+// about 2 cycles each (ncu at T=32), twice the 4-cycle latency of the chain's
+// FMA.  K chunks of 64 flow through a 12-stage cp.async ring filled by both
+// warps (the ring runs microseconds ahead of the loads' latency).
 constexpr int kSTM = 8, kSTE = 8, kSKC = 64, kSNS = 12, kSXP = kSKC + 8, kSThreads = 64;
 
 __global__ void __launch_bounds__(kSThreads)
@@ -528,23 +390,8 @@ cudaError_t launch_router_scores(const uint16_t *x, const float *wr, int T, int 
                                  float *scores, int *status, cudaStream_t s)
 {
     stage_begin(kStRouter, s);
-    // CTA tiles: 128 x 128 from T = 16384; 128 tokens x 64 experts from
-    // T = 8192 (twice the CTAs of the square tile: 0.58 -> 0.53 ms at
-    // T = 8192); 64 x 64 below (at T = 4096 the 128 x 64 tile leaves too few
-    // CTAs and measured slower)
-    if (T >= 16384) {
-        dim3 grid((T + 127) / 128, (E + 127) / 128);
-        router_scores_large<8, 8><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
-    } else if (T >= 8192) {
-        dim3 grid((T + 127) / 128, (E + 63) / 64);
-        router_scores_large<8, 4><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
-    } else if (T >= 128) {
-        dim3 grid((T + 63) / 64, (E + 63) / 64);
-        router_scores_large<4, 4><<<grid, 256, 0, s>>>(x, wr, T, H, E, scores, status);
-    } else {
-        dim3 grid((T + kSTM - 1) / kSTM, (E + kSTE - 1) / kSTE);
-        router_scores_small<<<grid, kSThreads, 0, s>>>(x, wr, T, H, E, scores, status);
-    }
+    const dim3 grid((T + kSTM - 1) / kSTM, (E + kSTE - 1) / kSTE);
+    router_scores_small<<<grid, kSThreads, 0, s>>>(x, wr, T, H, E, scores, status);
     stage_end(kStRouter, s);
     return cudaGetLastError();
 }
